@@ -1,0 +1,340 @@
+"""Pins of the fp64 oracle: facts the FASA pages and the mathematics fix.
+
+Each ``check_*`` takes the oracle module (so a test can hand it a copy with a
+planted mistake) and raises AssertionError when the pin does not hold.  None
+of them retypes the oracle's own formula: each compares against an
+independent statement of the same fact (a closed form, a library routine, a
+brute-force enumeration, an invariant or a number the pages print).
+"""
+
+import itertools
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --- P2: RoPE -----------------------------------------------------------------
+def check_rope_complex_closed_form(o):
+    """R_{m,theta_i} acting on (x_2i, x_2i+1) is multiplication of the complex
+    number x_2i + i x_2i+1 by exp(i m theta_i), with theta_i = B^(-2i/d)
+    written as exp(-(2i/d) ln B)."""
+    rng = _rng(1)
+    for d, base in ((8, 1e4), (64, 1e4), (128, 5e5)):
+        x = rng.standard_normal((5, d))
+        pos = np.array([0, 1, 17, 1024, 131072])
+        y = o.rope_rotate(x, pos, base)
+        theta = np.exp(-(2.0 * np.arange(d // 2) / d) * np.log(base))
+        z = (x[:, 0::2] + 1j * x[:, 1::2]) * np.exp(1j * pos[:, None] * theta[None, :])
+        assert np.allclose(y[:, 0::2], z.real, rtol=0, atol=1e-9), "RoPE even dims"
+        assert np.allclose(y[:, 1::2], z.imag, rtol=0, atol=1e-9), "RoPE odd dims"
+
+
+def check_rope_norm_and_relative(o):
+    """Each FC keeps its norm; (R_m q).(R_n k) depends only on m - n."""
+    rng = _rng(2)
+    d, base = 128, 1e6
+    q = rng.standard_normal(d)
+    k = rng.standard_normal(d)
+    for m in (0, 5, 4096):
+        qm = o.rope_rotate(q, m, base)
+        assert np.allclose(qm[0::2] ** 2 + qm[1::2] ** 2, q[0::2] ** 2 + q[1::2] ** 2,
+                           rtol=1e-12, atol=1e-12), "RoPE changed an FC norm"
+    for (m, n, s) in ((10, 3, 100), (4096, 4000, 7), (1, 0, 30000)):
+        a = np.dot(o.rope_rotate(q, m, base), o.rope_rotate(k, n, base))
+        b = np.dot(o.rope_rotate(q, m + s, base), o.rope_rotate(k, n + s, base))
+        assert abs(a - b) <= 1e-9 * (1 + abs(a)), "score depends on absolute position"
+    # q R_{dt} k^T with the block-diagonal R of the pages: rotating q by m and
+    # k by n gives the pre-RoPE pair rotated by the relative angle.
+    m, n = 777, 123
+    lhs = np.dot(o.rope_rotate(q, m, base), o.rope_rotate(k, n, base))
+    theta = np.exp(-(2.0 * np.arange(d // 2) / d) * np.log(base))
+    qc = q[0::2] + 1j * q[1::2]
+    kc = k[0::2] + 1j * k[1::2]
+    rhs = np.sum((qc * np.conj(kc) * np.exp(1j * (m - n) * theta)).real)
+    assert abs(lhs - rhs) <= 1e-9 * (1 + abs(rhs)), "relative-position form"
+
+
+def check_fc_frequencies(o):
+    """theta_0 = 1, theta_i strictly decreasing (low FC index = high
+    frequency), constant ratio B^(2/d), theta_{d/2} would be 1/B."""
+    for d, base in ((64, 1e4), (128, 5e5)):
+        th = o.fc_frequencies(base, d)
+        assert th.shape == (d // 2,)
+        assert th[0] == 1.0
+        assert np.all(np.diff(th) < 0)
+        r = th[:-1] / th[1:]
+        assert np.allclose(r, base ** (2.0 / d), rtol=1e-12)
+        assert np.isclose(th[-1] / base ** (2.0 / d), 1.0 / base, rtol=1e-12)
+
+
+def check_rope_matches_cached_key_convention(o):
+    """The oracle's query rotation and the generator's stored-key rotation use
+    one convention: q'_m . k'_n equals the relative-angle complex form."""
+    from workload import configs, synth
+    cfg = configs.CONFIGS["tiny_fp32_ctx1k"].with_(context=64)
+    kk, _ = synth.gen_kv_head(cfg, 0, 0, 0, t_count=64)   # post-RoPE keys, fp64
+    rng = _rng(3)
+    d = cfg.head_dim
+    q = rng.standard_normal(d)
+    m = 64
+    qr = o.rope_rotate(q, m, cfg.rope_theta)
+    # undo the key rotation independently through the complex form
+    theta = np.exp(-(2.0 * np.arange(d // 2) / d) * np.log(cfg.rope_theta))
+    for n in (0, 1, 33, 63):
+        kc_post = kk[n, 0::2] + 1j * kk[n, 1::2]
+        kc_pre = kc_post * np.exp(-1j * n * theta)
+        qc = q[0::2] + 1j * q[1::2]
+        rhs = np.sum((qc * np.conj(kc_pre) * np.exp(1j * (m - n) * theta)).real)
+        assert abs(np.dot(qr, kk[n]) - rhs) <= 1e-9 * (1 + abs(rhs))
+
+
+# --- P1 / P3: the FC decomposition is exact -----------------------------------
+def check_all_fcs_equal_full_logits(o):
+    """With I_dom = all d/2 FCs, S = q.K^T exactly (G = 1), and for a GQA group
+    S = (sum_g q_g).K^T (the score is linear in the query)."""
+    rng = _rng(4)
+    d = 64
+    K = rng.standard_normal((50, d))
+    q = rng.standard_normal((1, d))
+    s = o.tip_scores_unit(q, K, np.arange(d // 2))
+    assert np.allclose(s, K @ q[0], rtol=1e-12, atol=1e-12), "sum over all FCs != full dot"
+    qg = rng.standard_normal((3, d))
+    s = o.tip_scores_unit(qg, K, np.arange(d // 2))
+    assert np.allclose(s, K @ qg.sum(0), rtol=1e-12, atol=1e-11)
+
+
+def check_fc_additivity(o):
+    """Scores over a partition of the FCs add up to the score over their union."""
+    rng = _rng(5)
+    d = 128
+    K = rng.standard_normal((40, d))
+    q = rng.standard_normal((4, d))
+    perm = rng.permutation(d // 2)
+    parts = [perm[:5], perm[5:20], perm[20:21], perm[21:]]
+    total = sum(o.tip_scores_unit(q, K, p) for p in parts)
+    assert np.allclose(total, K @ q.sum(0), rtol=1e-12, atol=1e-11)
+    # restricting to FCs touches exactly the pair (2i, 2i+1): zeroing every
+    # other dimension of K does not change the restricted score
+    dom = perm[:7]
+    mask = np.zeros(d)
+    mask[2 * dom] = 1
+    mask[2 * dom + 1] = 1
+    assert np.allclose(o.tip_scores_unit(q, K, dom), (K * mask) @ q.sum(0), rtol=1e-12, atol=1e-11)
+
+
+def check_dom_order_invariance(o):
+    """S is a sum over a set: the order of I_dom does not matter (P9)."""
+    rng = _rng(6)
+    K = rng.standard_normal((30, 64))
+    q = rng.standard_normal((2, 64))
+    dom = np.array([3, 17, 4, 30, 9])
+    a = o.tip_scores_unit(q, K, dom)
+    b = o.tip_scores_unit(q, K, dom[::-1])
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+# --- P5 / P6 / P9: TopK-I ------------------------------------------------------
+def check_topk_bruteforce(o):
+    """TopK-I equals the max-sum subset of size k, ties resolved to the
+    lexicographically smallest index set (= smaller index first)."""
+    rng = _rng(7)
+    for trial in range(60):
+        n = int(rng.integers(1, 10))
+        k = int(rng.integers(1, 12))
+        s = rng.integers(-3, 4, size=n).astype(np.float64)   # many ties
+        if trial % 3 == 0:
+            s = rng.standard_normal(n)
+        kk = min(k, n)
+        best = None
+        for sub in itertools.combinations(range(n), kk):
+            val = s[list(sub)].sum()
+            key = (-val, sub)
+            if best is None or key < best:
+                best = key
+        got = o.topk_select_unit(s, k)
+        assert tuple(int(x) for x in got) == best[1], (s, k, got, best)
+
+
+def check_topk_signed_zero_and_order(o):
+    """-0 and +0 are equal scores; output is ascending; k >= len keeps all."""
+    s = np.array([0.0, -0.0, 1.0, -0.0, 0.0])
+    assert list(o.topk_select_unit(s, 3)) == [0, 1, 2]
+    s = np.array([5.0, 1.0, 7.0, 3.0])
+    assert list(o.topk_select_unit(s, 2)) == [0, 2]
+    assert list(o.topk_select_unit(s, 10)) == [0, 1, 2, 3]
+
+
+def check_topk_permutation(o):
+    """Permuting tie-free scores permutes the selected set the same way."""
+    rng = _rng(8)
+    s = rng.standard_normal(200)
+    perm = rng.permutation(200)
+    a = set(int(x) for x in o.topk_select_unit(s, 17))
+    b = set(int(perm[x]) for x in o.topk_select_unit(s[perm], 17))
+    assert a == b
+
+
+def check_query_scale_invariance(o):
+    """Scaling the query by c > 0 scales every S by c: the selection is unchanged."""
+    rng = _rng(9)
+    K = rng.standard_normal((300, 64))
+    q = rng.standard_normal((2, 64))
+    dom = np.array([1, 5, 9, 20])
+    a = o.topk_select_unit(o.tip_scores_unit(q, K, dom), 20)
+    b = o.topk_select_unit(o.tip_scores_unit(3.7 * q, K, dom), 20)
+    assert np.array_equal(a, b)
+
+
+# --- P4 / P6 / P7: FAC ---------------------------------------------------------
+def check_fac_weights(o):
+    """Weights are >= 0 and sum to 1 over T; rows outside T get no weight
+    (changing them leaves the output unchanged); the output is a convex
+    combination of the selected value rows."""
+    rng = _rng(10)
+    d = 64
+    K = rng.standard_normal((80, d))
+    V = rng.standard_normal((80, d))
+    q = rng.standard_normal((3, d)) * 3
+    idx = np.array([2, 9, 10, 40, 79])
+    out, w = o.focused_attention_unit(q, K, V, idx, return_weights=True)
+    assert np.all(w >= 0) and np.allclose(w.sum(1), 1.0, atol=1e-12)
+    K2, V2 = K.copy(), V.copy()
+    others = np.setdiff1d(np.arange(80), idx)
+    K2[others] = 1e3
+    V2[others] = -1e3
+    assert np.allclose(o.focused_attention_unit(q, K2, V2, idx), out, atol=1e-12)
+    lo, hi = V[idx].min(0), V[idx].max(0)
+    assert np.all(out >= lo - 1e-12) and np.all(out <= hi + 1e-12)
+
+
+def check_fac_single_token(o):
+    """k = 1: the output is exactly the value row of the top-scored token."""
+    rng = _rng(11)
+    K = rng.standard_normal((64, 32))
+    V = rng.standard_normal((64, 32))
+    q = rng.standard_normal((2, 32))
+    s = o.tip_scores_unit(q, K, np.arange(16))
+    sel = o.topk_select_unit(s, 1)
+    assert sel[0] == int(np.argmax(s))
+    out = o.focused_attention_unit(q, K, V, sel)
+    assert np.array_equal(out, np.stack([V[sel[0]]] * 2))
+
+
+def check_fac_vs_sdpa(o):
+    """Dense attention (T = all tokens) equals torch's scaled_dot_product_attention
+    in fp64 on the CPU, including the GQA mapping hq -> hq // G."""
+    import torch
+    rng = _rng(12)
+    B, Hq, Hkv, T, d = 2, 6, 2, 37, 64
+    q = rng.standard_normal((B, Hq, d))
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = rng.standard_normal((B, Hkv, T, d))
+    lens = np.array([37, 20])
+    out = o.dense_attention(q, K, V, lens)
+    G = Hq // Hkv
+    for b in range(B):
+        L = lens[b]
+        qt = torch.from_numpy(q[b][:, None, :])                               # [Hq,1,d]
+        kt = torch.from_numpy(np.repeat(K[b, :, :L], G, axis=0))              # [Hq,L,d]
+        vt = torch.from_numpy(np.repeat(V[b, :, :L], G, axis=0))
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+        assert np.allclose(out[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def check_full_budget_equals_dense(o):
+    """All FCs dominant and budget = len: the FASA step equals dense attention
+    of the rotated query (the pages' correctness guarantee with nothing
+    evicted), and the TIP scores equal the summed full logits."""
+    import torch
+    rng = _rng(13)
+    B, Hq, Hkv, T, d, base = 1, 4, 2, 48, 64, 1e4
+    q = rng.standard_normal((B, Hq, d))
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = rng.standard_normal((B, Hkv, T, d))
+    lens = np.array([T])
+    pos = np.array([T])
+    dom = np.tile(np.arange(d // 2), (Hkv, 1))
+    out, idx, cnt, sc = o.decode_step(q, pos, K, V, dom, lens, T, base)
+    assert int(cnt[0, 0]) == T and np.array_equal(idx[0, 0], np.arange(T))
+    # independent rotation through the complex form, then SDPA
+    theta = np.exp(-(2.0 * np.arange(d // 2) / d) * np.log(base))
+    z = (q[..., 0::2] + 1j * q[..., 1::2]) * np.exp(1j * T * theta)
+    qr = np.empty_like(q)
+    qr[..., 0::2], qr[..., 1::2] = z.real, z.imag
+    G = Hq // Hkv
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qr[0][:, None, :]),
+        torch.from_numpy(np.repeat(K[0], G, axis=0)),
+        torch.from_numpy(np.repeat(V[0], G, axis=0)))[:, 0].numpy()
+    assert np.allclose(out[0], ref, rtol=1e-11, atol=1e-11)
+    for h in range(Hkv):
+        assert np.allclose(sc[0, h], K[0, h] @ qr[0, h * G:(h + 1) * G].sum(0), rtol=1e-11, atol=1e-10)
+
+
+def check_gqa_mapping(o):
+    """Query head hq attends to KV head hq // G: with every value row of KV
+    head h equal to h + 1, the output of head hq is hq // G + 1."""
+    rng = _rng(14)
+    B, Hq, Hkv, T, d = 2, 8, 2, 40, 64
+    q = rng.standard_normal((B, Hq, d))
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = np.zeros((B, Hkv, T, d))
+    for h in range(Hkv):
+        V[:, h] = h + 1
+    dom = np.tile(np.arange(4), (Hkv, 1))
+    out, _, _, _ = o.decode_step(q, np.array([T, T]), K, V, dom, np.array([T, 25]), 7, 1e4)
+    for hq in range(Hq):
+        assert np.allclose(out[:, hq], hq // (Hq // Hkv) + 1, atol=1e-12)
+
+
+def check_decode_stored(o):
+    """bf16 bit patterns promote exactly (torch's bfloat16 -> float64 agrees)."""
+    import torch
+    rng = _rng(15)
+    x = torch.from_numpy(rng.standard_normal(1000).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o.decode_stored(bits, "bf16"), x.to(torch.float64).numpy())
+    f = rng.standard_normal(10).astype(np.float32)
+    assert np.array_equal(o.decode_stored(f, "f32"), f.astype(np.float64))
+
+
+def check_build_kdom_layout(o):
+    """K_dom is FC-major: K_dom[b,h,j,tau,c] holds K[b,h,tau,2 dom[h,j] + c].
+    Keys that encode their own coordinates make the layout self-evident."""
+    B, H, T, d = 2, 3, 10, 16
+    K = np.zeros((B, H, T, d), dtype=np.float32)
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                K[b, h, t] = b * 1e6 + h * 1e4 + t * 100 + np.arange(d)
+    dom = np.array([[0, 5, 7], [1, 2, 3], [7, 6, 0]])
+    kd = o.build_kdom(K, dom)
+    assert kd.shape == (B, H, 3, T, 2)
+    assert kd[1, 2, 0, 4, 1] == 1e6 + 2e4 + 400 + 15      # FC 7 -> dims 14, 15
+    assert kd[0, 0, 1, 9, 0] == 900 + 10                  # FC 5 -> dim 10
+    assert kd[1, 1, 2, 0, 0] == 1e6 + 1e4 + 6             # FC 3 -> dim 6
+
+
+def check_byte_model(o):
+    """The numbers the pages print for the FASA-C memory-movement model."""
+    with open(os.path.join(GOLDEN, "byte_model.json")) as f:
+        g = json.load(f)["cases"]
+    c = g[0]
+    assert abs(o.bytes_fraction(c["n_tip"], c["d"], c["budget"], c["t"]) - c["fraction"]) <= c["abs_tol"]
+    c = g[1]
+    assert np.isclose(o.bytes_fraction(c["n_tip"], c["d"], 0, 10 ** 6), c["tip_fraction"], rtol=1e-12)
+    c = g[2]
+    assert np.isclose(o.theoretical_speedup(c["n_tip"], c["d"], 0, 10 ** 6), c["speedup_limit"], rtol=1e-12)
+    assert o.theoretical_speedup(c["n_tip"], c["d"], 256, 10 ** 9) < c["speedup_limit"]
+    c = g[3]
+    assert abs(c["t"] / c["budget"] - c["fac_ratio_approx"]) / c["fac_ratio_approx"] <= c["rel_tol"]
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]
