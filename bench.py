@@ -1,0 +1,510 @@
+"""Benchmark of the FASA decode step on GB300.
+
+One step = one fused decode step (RoPE(q) -> TIP -> top-k -> FAC) over one
+batch of the named workload, launched through the C ABI.  Inputs are
+synthetic (seeded) and resident in HBM; each step reads a different replica
+so that the replicas together exceed the L2 cache several times over.
+
+Prints ONE JSON line.  `value` is the achieved HBM throughput in TB/s of the
+algorithmic bytes (K_dom columns of the cached tokens + selected K/V rows +
+query + output), summed over ranks and divided by the slowest rank's time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fasa|reference]
+                    [--workload NAME]
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this path).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import configs, synth  # noqa: E402
+
+METRIC = "FASA decode-step µs and achieved HBM TB/s (TIP+top-k+FAC) at 32K ctx"
+DEFAULT_WORKLOAD = "llama3_8b_ctx32k"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_cluster.cuh",
+                  "kv_cache_token_tip_gb300/csrc/fasa_ptx.cuh",
+                  "kv_cache_token_tip_gb300/csrc/fasa_internal.h",
+                  "kv_cache_token_tip_gb300/csrc/fasa_api.cu"]
+
+
+# ----------------------------------------------------------------------------
+# Byte model (FASA-C memory movement, per step)
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(cfg, lens) -> dict:
+    """Bytes one decode step must move: every cached token's dominant-FC key
+    columns (TIP), the selected K and V rows (FAC), the query, the fp32 output
+    and the small index tables."""
+    es = cfg.elem_bytes
+    H, d, n = cfg.n_kv_heads, cfg.head_dim, cfg.n_tip
+    lens = np.asarray(lens, dtype=np.int64)
+    tip = int(np.sum(lens) * H * n * 2 * es)
+    sel = int(np.sum(np.minimum(lens, cfg.budget)) * H * 2 * d * es)
+    q = cfg.batch * cfg.n_q_heads * d * es
+    out = cfg.batch * cfg.n_q_heads * d * 4
+    small = H * n * 4 + 2 * cfg.batch * 4
+    dense = int(np.sum(lens) * H * 2 * d * es) + q + out + 2 * cfg.batch * 4
+    return dict(tip=tip, fac=sel, q=q, out=out, small=small,
+                total=tip + sel + q + out + small, dense_total=dense)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"fasa_step_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != want:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU, independent replicas)
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("FASA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None and pg.get_backend() == "nccl":
+            pg.barrier(device_ids=[device])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle leg (bounded sample)
+# ----------------------------------------------------------------------------
+def unit_bytes(cfg, L: int) -> int:
+    """Algorithmic bytes of one (batch, KV head) unit of length L."""
+    es, G, d = cfg.elem_bytes, cfg.group, cfg.head_dim
+    return L * cfg.n_tip * 2 * es + min(L, cfg.budget) * 2 * d * es + G * d * es + G * d * 4
+
+
+def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 2):
+    """Times the fp64 oracle (as it stands, single-threaded numpy) on a bounded
+    sample of the workload: each step is one (batch, KV head) unit of the
+    decode step -- RoPE of its query group, TIP over its cached tokens, TopK-I
+    and FAC -- cycling over the first `n_units` units, host-generated with the
+    workload's recipe.  Runs `warmup` untimed steps, then timed steps until
+    `max_steps` or `seconds` is reached.  Returns (seconds, steps, bytes)."""
+    import oracle as O
+    lens = synth.seq_lens(cfg)
+    G = cfg.group
+    q_all = O.decode_stored(synth.store(synth.gen_q(cfg, 0), cfg.dtype), cfg.dtype)
+    dom = synth.dominant_fcs(cfg, 0)
+    units = []
+    for u in range(min(n_units, cfg.batch * cfg.n_kv_heads)):
+        b, h = divmod(u, cfg.n_kv_heads)
+        L = int(lens[b])
+        kk, vv = synth.gen_kv_head(cfg, 0, b, h, t_count=L)
+        K = O.decode_stored(synth.store(kk, cfg.dtype), cfg.dtype)
+        V = O.decode_stored(synth.store(vv, cfg.dtype), cfg.dtype)
+        units.append((q_all[b, h * G:(h + 1) * G], int(lens[b]), K, V, dom[h], unit_bytes(cfg, L)))
+
+    def one(i):
+        q, pos, K, V, dfc, nb = units[i % len(units)]
+        q_rot = O.apply_rope_q(q[None], np.array([pos]), cfg.rope_theta)[0]
+        s = O.tip_scores_unit(q_rot, K, dfc)
+        idx = O.topk_select_unit(s, cfg.budget)
+        O.focused_attention_unit(q_rot, K, V, idx)
+        return nb
+
+    for i in range(warmup):
+        one(i)
+    steps, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while steps < max_steps:
+        nbytes += one(steps)
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return time.perf_counter() - t0, steps, nbytes
+
+
+def run_oracle_leg(cfg, seconds: float, max_steps: int = 10 ** 9, warmup: int = 0):
+    """Runs oracle_sample in a child process with BLAS limited to one thread so
+    the reported core count is exact."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; from workload import configs; "
+            "cfg = configs.CONFIGS[%r]; t, n, b = bench.oracle_sample(cfg, %r, %r, %r); "
+            "print(json.dumps({'seconds': t, 'steps': n, 'bytes': b}))"
+            % (ROOT, cfg.name, seconds, max_steps, warmup))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def make_replicas(cfg, R, dims):
+    import torch
+    from kv_cache_token_tip_gb300 import fasa_build_kdom
+    from workload import gpu_gen
+    reps = []
+    for r in range(R):
+        L = gpu_gen.make_layer(cfg, layer=r)
+        kd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.n_tip, cfg.context, 2), dtype=L.k.dtype, device="cuda")
+        fasa_build_kdom(L.k, L.dom_fc, L.seq_lens, kd, dims)
+        reps.append((L, kd))
+    torch.cuda.synchronize()
+    return reps
+
+
+def capture(fn, n_steps, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                fn(i)
+    return g
+
+
+def run_gpu(args):
+    import torch
+    from kv_cache_token_tip_gb300 import build as kbuild
+    kbuild.build()
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_apply_rope_q, fasa_cluster_size, fasa_decode_step,
+                                          fasa_dense_attention, fasa_device_status, fasa_workspace_size)
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    cfg = configs.CONFIGS[args.workload]
+    dims = dims_for(cfg)
+    lens = synth.seq_lens(cfg)
+    model = algorithmic_bytes(cfg, lens)
+    per_step = model["total"]
+    R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
+    R = min(R, 64)
+    reps = make_replicas(cfg, R, dims)
+    B, Hq, H, d, k = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.budget
+    ws_bytes = fasa_workspace_size(dims, k)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    outs = [torch.empty((B, Hq, d), dtype=torch.float32, device="cuda") for _ in range(R)]
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        L, kd = reps[i % R]
+        fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, k, outs[i % R],
+                         None, None, ws, dims, stream=stream)
+
+    # dense comparison: the same kernels over every cached row
+    q_rots = []
+    for L, _ in reps:
+        qr = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        fasa_apply_rope_q(L.q, L.pos, qr, dims)
+        q_rots.append(qr)
+
+    def dense_step(i):
+        L, _ = reps[i % R]
+        fasa_dense_attention(q_rots[i % R], L.k, L.v, L.seq_lens, outs[i % R], dims, stream=stream)
+
+    step(0)            # first calls outside capture: attribute set-up and caches
+    dense_step(0)
+    torch.cuda.synchronize()
+    chunk = R * max(1, 512 // R)
+    K, W = args.steps, args.warmup
+    g_chunk = capture(step, chunk, stream)
+    rem = K % chunk
+    g_rem = capture(step, rem, stream) if rem else None
+    g_warm = capture(step, W, stream) if W else None
+    torch.cuda.synchronize()
+    if g_warm is not None:
+        g_warm.replay()
+    torch.cuda.synchronize()
+    status = fasa_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(K // chunk):
+            g_chunk.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(pg, ms_total)
+    sec_per_step = ms_total / 1e3 / K
+
+    # dense baseline (same machinery), fewer steps
+    Kd = max(R, min(K // 8, 4096))
+    g_dense = capture(dense_step, Kd, stream)
+    g_dense.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g_dense.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dense_sec = e0.elapsed_time(e1) / 1e3 / Kd
+
+    # end to end through the public API: pinned host q/pos/lens in, out back,
+    # synchronised every step (graph-free launches)
+    E = min(2000, max(50, K // 100))
+    h_q = [torch.empty(reps[0][0].q.shape, dtype=reps[0][0].q.dtype).pin_memory() for _ in range(R)]
+    for r in range(R):
+        h_q[r].copy_(reps[r][0].q.cpu())
+    h_pos = torch.from_numpy(np.asarray(lens, dtype=np.int32)).pin_memory()
+    h_out = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
+    d_q = [torch.empty_like(reps[r][0].q) for r in range(R)]
+    d_pos = torch.empty(B, dtype=torch.int32, device="cuda")
+    d_lens = torch.empty(B, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(E):
+            r = i % R
+            L, kd = reps[r]
+            d_q[r].copy_(h_q[r], non_blocking=True)
+            d_pos.copy_(h_pos, non_blocking=True)
+            d_lens.copy_(h_pos, non_blocking=True)
+            fasa_decode_step(d_q[r], d_pos, L.k, L.v, kd, L.dom_fc, d_lens, k, outs[r], None, None, ws, dims,
+                             stream=stream)
+            h_out.copy_(outs[r], non_blocking=True)
+            stream.synchronize()
+    e2e_sec = time.perf_counter() - t0
+    e2e_sec = max_over_ranks(pg, e2e_sec)
+    e2e_per_step = e2e_sec / E
+    status = fasa_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    peak, peak_kind = measured_peak()
+    achieved_gbs = per_step / sec_per_step / 1e9
+    clocks = clk.summary()
+    C = fasa_cluster_size(dims)
+    line = None
+    if args.cpu_baseline and rank == 0 and world == 1:
+        cb = run_oracle_leg(cfg, args.cpu_seconds)
+        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s "
+                         f"(host-generated inputs, numpy fp64, 1 BLAS thread); "
+                         f"{cb['seconds'] / cb['steps'] * B * H * 1e6:.0f} us per whole decode step"}
+    else:
+        cpu = None
+    if rank == 0:
+        h2d = int(h_q[0].numel() * h_q[0].element_size() + 2 * h_pos.numel() * 4)
+        d2h = int(h_out.numel() * 4)
+        line = {
+            "metric": METRIC,
+            "value": round(world * per_step / sec_per_step / 1e12, 4),
+            "unit": "TB/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(sec_per_step * 1e3, 6),
+            "us_per_step": round(sec_per_step * 1e6, 3),
+            "tokens_per_s": round(world * B / sec_per_step, 1),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": cfg.dtype,
+            "data": "synthetic (seeded; pre-RoPE q/k ~ N(0,1) with x8 outlier FCs, v ~ N(0,1))",
+            "config": {"workload": cfg.name, "batch": B, "q_heads": Hq, "kv_heads": H, "head_dim": d,
+                       "context": cfg.context, "n_tip": cfg.n_tip, "budget": k, "rope_theta": cfg.rope_theta,
+                       "cluster_ctas": C, "replicas": R,
+                       "l2": f"inputs larger than L2: {R} replicas x {per_step / 1e6:.2f} MB/step "
+                             f"rotate ({R * per_step / L2_BYTES:.1f}x L2)",
+                       "launch": "CUDA graph of fasa_decode_step launches, one kernel per step",
+                       "parallelism": f"replicas x{world}"},
+            "bytes_per_step": per_step,
+            "bytes_breakdown": {kk: model[kk] for kk in ("tip", "fac", "q", "out", "small")},
+            "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),
+                         "peak_kind": peak_kind, "kernel": "fasa_cluster_kernel<bf16,128>"},
+            "dense": {"us_per_step": round(dense_sec * 1e6, 3),
+                      "achieved_gbs": round(model["dense_total"] / dense_sec / 1e9, 1),
+                      "sparse_vs_dense_speedup": round(dense_sec / sec_per_step, 3)},
+            "e2e": {"value": round(world * per_step / e2e_per_step / 1e12, 4), "unit": "TB/s",
+                    "us_per_step": round(e2e_per_step * 1e6, 3),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return line
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle timed on the host cores.  Each step is
+    one (batch, KV head) unit of the workload (a bounded sample); W untimed
+    warm-up steps, then at most K timed steps, stopped after --cpu-seconds."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return None
+    cfg = configs.CONFIGS[args.workload]
+    cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps, args.warmup)
+    val = cb["bytes"] / cb["seconds"] / 1e12
+    per_unit = cb["seconds"] / cb["steps"]
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
+        "steps": cb["steps"], "warmup": args.warmup,
+        "ms_per_step": per_unit * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, host-generated)",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.n_q_heads,
+                   "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "context": cfg.context,
+                   "n_tip": cfg.n_tip, "budget": cfg.budget,
+                   "step": "one (batch, KV head) unit of the decode step"},
+        "cpu_baseline": {"value": val, "unit": "TB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{cb['steps']} units in {cb['seconds']:.1f} s, bounded to "
+                                   f"~{args.cpu_seconds:.0f} s (numpy fp64, 1 BLAS thread)"},
+        "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2048)
+    ap.add_argument("--impl", choices=["fasa", "reference"], default="fasa")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * fasa.h -- C ABI of the FASA decode-step library (libfasa.so, sm_103a).
+ *
+ * FASA ("FASA: Frequency-aware Sparse Attention") splits one decode step of
+ * attention into Token Importance Prediction (TIP), a per-(batch, KV head)
+ * top-k, and Focused Attention Computation (FAC).  The functions below are
+ * those stages, a fused step, a dense baseline built from the same kernels,
+ * and the maintenance of the dominant-key side copy the TIP stage reads.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  Nothing
+ *    is allocated or freed by the library.  Calls are asynchronous on
+ *    `stream` (NULL = the legacy default stream).
+ *  - Return value: FASA_OK, or an error code.  Arguments are validated on
+ *    the host before any launch; on an error nothing is launched and nothing
+ *    is written.  Values that live in device memory (sequence lengths,
+ *    positions, FC indices, index lists) cannot be checked on the host: the
+ *    kernels clamp them into range and raise FASA_DEV_BAD_INPUT in the device
+ *    status word (see fasa_device_status).
+ *  - Shapes (row-major, contiguous):
+ *      q         [B, Hq, d]            storage dtype, pre-RoPE query
+ *      q_rot     [B, Hq, d]            fp32, rotated query
+ *      pos       [B]                   int32, query position (usually = len)
+ *      k_cache   [B, Hkv, T_max, d]    storage dtype, keys AFTER RoPE
+ *      v_cache   [B, Hkv, T_max, d]    storage dtype
+ *      k_dom     [B, Hkv, n_tip, T_max, 2]  storage dtype, FC-major side copy
+ *                                      of the dominant key columns
+ *      dom_fc    [Hkv, n_tip]          int32, dominant FC indices in [0, d/2)
+ *      seq_lens  [B]                   int32, cached tokens 0..len-1
+ *      scores    [B, Hkv, T_max]       fp32 (entries tau >= len unspecified)
+ *      idx       [B, Hkv, budget]      int32, ascending; -1 past count
+ *      count     [B, Hkv]              int32, = min(budget, len)
+ *      out       [B, Hq, d]            fp32
+ *    Query head hq belongs to KV head hq / G, G = Hq / Hkv.
+ *  - Frequency chunk (FC) i is the interleaved pair of dimensions (2i, 2i+1).
+ *  - Alignment: k_cache, v_cache, k_dom, scores, q_rot and out must be
+ *    16-byte aligned; T_max must be a multiple of 16.
+ *  - Supported: dtype FASA_F32 or FASA_BF16 (q, caches and k_dom share it),
+ *    head_dim 64 or 128, 1 <= G <= 8, 1 <= budget <= fasa_max_budget().
+ */
+#ifndef FASA_H_
+#define FASA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* fasa_stream_t;
+
+/* Host-side status codes. */
+enum {
+  FASA_OK = 0,
+  FASA_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, misalignment, bad budget */
+  FASA_ERR_UNSUPPORTED = 2,  /* dtype / head_dim / group size not compiled in   */
+  FASA_ERR_WORKSPACE = 3,    /* workspace missing or too small                  */
+  FASA_ERR_CUDA = 4          /* a CUDA call failed; see fasa_last_cuda_error()  */
+};
+
+/* Device status word bits (fasa_device_status). */
+enum {
+  FASA_DEV_BAD_INPUT = 1,    /* a device-resident value was out of range and clamped */
+  FASA_DEV_TIMEOUT = 2       /* a bounded wait for an asynchronous copy expired      */
+};
+
+enum { FASA_F32 = 0, FASA_BF16 = 1 };
+
+typedef struct fasa_dims {
+  int32_t batch;       /* B                                   */
+  int32_t n_q_heads;   /* Hq                                  */
+  int32_t n_kv_heads;  /* Hkv (Hq % Hkv == 0)                 */
+  int32_t head_dim;    /* d: 64 or 128                        */
+  int32_t t_max;       /* cache capacity per (b, KV head)     */
+  int32_t n_tip;       /* dominant FCs per KV head, 1..d/2    */
+  int32_t dtype;       /* FASA_F32 or FASA_BF16               */
+  int32_t reserved;    /* must be 0                           */
+  double rope_theta;   /* RoPE base B: theta_i = B^(-2i/d)    */
+} fasa_dims_t;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int fasa_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* fasa_status_string(int status);
+
+/* The cudaError_t of the last call that returned FASA_ERR_CUDA. */
+int fasa_last_cuda_error(void);
+
+/* Largest budget (N_fac) the selection kernels accept for these dims. */
+int fasa_max_budget(const fasa_dims_t* dims, int32_t* max_budget);
+
+/*
+ * Workspace bytes fasa_decode_step needs for these dims and budget (0 when
+ * every intermediate fits in on-chip shared memory, which holds for T_max up
+ * to 131072).  The workspace is device memory owned by the caller.
+ */
+int fasa_workspace_size(const fasa_dims_t* dims, int32_t budget, size_t* bytes);
+
+/*
+ * RoPE of the query ("FASA: Frequency-aware Sparse Attention", §3.4 "RoPE from
+ * a Frequency-Chunk Perspective": theta_i = B^(-2i/d); each FC is turned by the
+ * 2x2 rotation R_{m,theta_i}, m = pos[b]).  q_rot = R(pos) q, fp32.
+ * Angles are formed and range-reduced in fp64.
+ */
+int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot,
+                      const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * Builds the dominant key cache C_key^dom (same page, "Hardware-Aware Variants",
+ * FASA-M/FASA-C: t x d_dom per head, d_dom = 2 N_tip) in FC-major layout:
+ * k_dom[b,h,j,tau,0:2] = k_cache[b,h,tau, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2] for
+ * tau < seq_lens[b] (all tau < T_max when seq_lens is NULL).  A pure copy.
+ */
+int fasa_build_kdom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens,
+                    void* k_dom, const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * Appends one token per sequence to k_dom: k_new [B, Hkv, d] holds the new
+ * post-RoPE keys, tok_pos [B] their cache slots (< T_max).
+ */
+int fasa_append_kdom(const void* k_new, const int32_t* dom_fc, const int32_t* tok_pos,
+                     void* k_dom, const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * TIP (same page, §3.4 "Online Stage 1: Token Importance Predictor"): for
+ * every cached token tau < len_b,
+ *   scores[b,h,tau] = sum_{hq in group(h)} sum_j q_rot[b,hq]^[dom_fc[h,j]] . k_dom[b,h,j,tau,:]
+ * i.e. the FC-restricted score S_t summed over the GQA group (no 1/sqrt(d)).
+ */
+int fasa_tip_score(const float* q_rot, const void* k_dom, const int32_t* dom_fc,
+                   const int32_t* seq_lens, float* scores,
+                   const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * T_t = TopK-I(S_t, N_fac) (same page, token-selection equation) per (b, KV
+ * head): the min(budget, len) largest scores; equal scores keep the smaller
+ * token index; -0 equals +0.  idx ascending, -1 padded; count = min(budget, len).
+ */
+int fasa_topk_select(const float* scores, const int32_t* seq_lens, int32_t budget,
+                     int32_t* idx, int32_t* count,
+                     const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * FAC (same page, §3.4 "Online Stage 2: Focused Attention Computation"): for
+ * every query head, softmax(q_rot K_T^T / sqrt(d)) V_T over the rows
+ * T = idx[b,h,0:count[b,h]] gathered at their original positions.
+ * Indices must lie in [0, len_b).  idx rows have stride `budget`.
+ */
+int fasa_focused_attention(const float* q_rot, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, const int32_t* idx, const int32_t* count,
+                           int32_t budget, float* out,
+                           const fasa_dims_t* dims, fasa_stream_t stream);
+
+/* Dense full-KV decode attention (FAC with T = all tokens 0..len-1). */
+int fasa_dense_attention(const float* q_rot, const void* k_cache, const void* v_cache,
+                         const int32_t* seq_lens, float* out,
+                         const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * One FASA decode step, fused: RoPE(q) -> TIP over k_dom -> top-k -> FAC over
+ * k_cache/v_cache -> out.  idx_out / count_out may be NULL.  workspace may be
+ * NULL when fasa_workspace_size reports 0.
+ */
+int fasa_decode_step(const void* q, const int32_t* pos,
+                     const void* k_cache, const void* v_cache, const void* k_dom,
+                     const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget,
+                     float* out, int32_t* idx_out, int32_t* count_out,
+                     void* workspace, size_t workspace_bytes,
+                     const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * Synchronises `stream`, stores the device status word of the current device
+ * in *status (FASA_DEV_* bits, 0 = clean) and clears it.
+ */
+int fasa_device_status(fasa_stream_t stream, int32_t* status);
+
+/* Cluster size (CTAs per (b, KV head)) the fused kernels use on this device. */
+int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FASA_H_ */

@@ -1,0 +1,15 @@
+"""GB300-native FASA decode step (frequency-aware sparse attention).
+
+The compute lives in ``libfasa.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/fasa.h``).  This package is its thin Python binding: argument
+marshalling from torch tensors (device pointers and the current stream) to the
+C entry points of the same names.  There is no CPU fallback: if the library
+is not built, every call raises.
+"""
+
+from .fasa import (  # noqa: F401
+    FASA_BF16, FASA_F32, FasaDims, FasaError, dims_for, fasa_append_kdom, fasa_apply_rope_q,
+    fasa_build_kdom, fasa_cluster_size, fasa_decode_step, fasa_dense_attention, fasa_device_status,
+    fasa_focused_attention, fasa_max_budget, fasa_tip_score, fasa_topk_select, fasa_workspace_size,
+    lib, library_path,
+)

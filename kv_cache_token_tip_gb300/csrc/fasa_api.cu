@@ -1,0 +1,577 @@
+// Host side of the C ABI: argument validation, shared-memory planning,
+// cluster sizing and launches; plus the small auxiliary kernels (query RoPE,
+// dominant-key copy build and append).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/fasa.h"
+#include "fasa_cluster.cuh"
+#include "fasa_internal.h"
+
+using namespace fasa;
+
+namespace {
+
+__device__ int g_status;  // FASA_DEV_* bits, per device
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return FASA_ERR_CUDA;
+}
+
+constexpr int SMEM_LIMIT = 232448;  // 227 KB per CTA
+constexpr int S_CAP_MAX = 8192;     // scores per CTA kept in shared memory
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int align_up(int x, int a) { return (x + a - 1) / a * a; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int check_dims(const fasa_dims_t* d) {
+  if (!d) return FASA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1) return FASA_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads) return FASA_ERR_INVALID_ARG;
+  if (d->head_dim < 2 || (d->head_dim & 1)) return FASA_ERR_INVALID_ARG;
+  if (d->t_max < 1 || (d->t_max % 16)) return FASA_ERR_INVALID_ARG;
+  if (d->n_tip < 1 || d->n_tip > d->head_dim / 2) return FASA_ERR_INVALID_ARG;
+  if (!(d->rope_theta > 0.0) || !isfinite(d->rope_theta)) return FASA_ERR_INVALID_ARG;
+  if (d->reserved < 0 || d->reserved > C_MAX) return FASA_ERR_INVALID_ARG;
+  if (d->dtype != FASA_F32 && d->dtype != FASA_BF16) return FASA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return FASA_ERR_UNSUPPORTED;
+  if (d->n_q_heads / d->n_kv_heads > G_MAX) return FASA_ERR_UNSUPPORTED;
+  if ((long long)d->batch * d->n_kv_heads > 65535) return FASA_ERR_UNSUPPORTED;
+  return FASA_OK;
+}
+
+int elem_size(const fasa_dims_t* d) { return d->dtype == FASA_F32 ? 4 : 2; }
+
+struct DevInfo {
+  int sms = 0;
+  int* status = nullptr;
+};
+
+int device_info(DevInfo* out) {
+  static std::mutex mu;
+  static std::map<int, DevInfo> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    DevInfo di;
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    it = cache.emplace(dev, di).first;
+  }
+  *out = it->second;
+  return FASA_OK;
+}
+
+// Whether a cluster of C CTAs with `smem` bytes each can be resident.
+bool cluster_fits(int dtype, int D, int C, int smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int>, bool> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, dtype, D, C, smem);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const int n = dtype == FASA_F32 ? max_active_clusters_f32(D, C, smem) : max_active_clusters_bf16(D, C, smem);
+  const bool ok = n >= 1;
+  cache.emplace(key, ok);
+  return ok;
+}
+
+// Shared-memory plan of one launch.  Returns FASA_OK, or FASA_ERR_UNSUPPORTED
+// when it cannot fit.  *ws = global workspace bytes the plan needs.
+int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, size_t* ws) {
+  const int D = d->head_dim, es = elem_size(d), G = d->n_q_heads / d->n_kv_heads;
+  const int nfc = d->n_tip;
+  int off = 0;
+  p.off_bar = off;
+  off += 64;
+  p.off_misc = off;
+  off += MISC_BYTES;
+  p.off_qrot = off;
+  off += G_MAX * D * 4;
+  p.off_qbar = off;
+  off += align_up(2 * nfc * 4, 16);
+  p.off_stile = off;
+  off += G_MAX * RT * 4;
+  p.off_hist = off;
+  off += 2 * 256 * 4;
+
+  // TIP staging tile
+  int tile = 0, stages = 0, tip_big = 0;
+  if (flags & F_TIP) {
+    tile = 1024;
+    while (tile > 256 && nfc * tile * 2 * es > 65536) tile /= 2;
+    const int stage = nfc * tile * 2 * es;
+    stages = 131072 / stage;
+    stages = stages < 1 ? 1 : (stages > 4 ? 4 : stages);
+    tip_big = stages * stage;
+  }
+  p.tip_tile = tile > 0 ? tile : 256;
+  p.tip_stages = stages > 0 ? stages : 1;
+
+  const bool select = (flags & F_SELECT) != 0;
+  int sel_big = 0;
+  if (select) {
+    const int want = 16 * 1024 * 8;  // room for 16K candidates when it fits
+    sel_big = want > 8 * p.budget ? want : 8 * p.budget;
+  }
+  const int fac_big = (flags & (F_FAC | F_DENSE)) ? FAC_STAGES * 2 * RT * (D * es + 16) : 0;
+
+  p.idx_cap = (flags & (F_SELECT | F_IDX_IN)) ? align_up(p.budget, 4) : 0;
+  p.hpc = ceil_div(G, C);
+  const int part_bytes = (flags & (F_FAC | F_DENSE)) ? p.hpc * C * (D + 2) * 4 : 0;
+
+  // scores in shared memory when the fused path holds them
+  int s_cap = 0;
+  *ws = 0;
+  if ((flags & F_TIP) && select) {
+    const int chunk = align_up(ceil_div(d->t_max, C), 16);
+    if (chunk <= S_CAP_MAX) s_cap = chunk;
+  }
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    int o = off;
+    p.off_sc = o;
+    o += s_cap * 4;
+    p.off_idx = o;
+    o += p.idx_cap * 4;
+    p.off_part = o;
+    o += part_bytes;
+    o = align_up(o, 128);
+    p.off_big = o;
+    int bigsz = tip_big;
+    if (fac_big > bigsz) bigsz = fac_big;
+    int room = SMEM_LIMIT - o;
+    if (select) {
+      // candidates take whatever is left, at least the budget
+      int cand_bytes = sel_big;
+      if (cand_bytes > room) cand_bytes = room;
+      if (cand_bytes < bigsz) cand_bytes = bigsz;
+      cand_bytes &= ~7;
+      p.cand_cap = cand_bytes / 8;
+      if (cand_bytes > bigsz) bigsz = cand_bytes;
+    } else {
+      p.cand_cap = 0;
+    }
+    p.smem_total = o + bigsz;
+    const bool ok = p.smem_total <= SMEM_LIMIT && (!select || p.cand_cap >= p.budget);
+    if (ok) {
+      p.s_cap = s_cap;
+      if ((flags & F_TIP) && select && s_cap == 0) {
+        if (!allow_ws) return FASA_ERR_UNSUPPORTED;
+        *ws = (size_t)d->batch * d->n_kv_heads * d->t_max * 4;
+      }
+      return FASA_OK;
+    }
+    if (s_cap == 0) break;
+    s_cap = 0;  // retry with the scores in the global workspace
+  }
+  return FASA_ERR_UNSUPPORTED;
+}
+
+// Cluster size: the explicit override, else as many CTAs per unit as fill the
+// SMs once (at most 16), reduced until the cluster is schedulable.
+int choose_cluster(const fasa_dims_t* d, int units, int sms) {
+  if (d->reserved > 0) return d->reserved;
+  int C = sms / (units > 0 ? units : 1);
+  if (C > C_MAX) C = C_MAX;
+  if (C < 1) C = 1;
+  return C;
+}
+
+void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
+  memset(&p, 0, sizeof(p));
+  p.B = d->batch;
+  p.Hq = d->n_q_heads;
+  p.Hkv = d->n_kv_heads;
+  p.G = d->n_q_heads / d->n_kv_heads;
+  p.T_max = d->t_max;
+  p.n_tip = d->n_tip;
+  p.budget = budget;
+  p.rope_theta = d->rope_theta;
+  p.status = status;
+}
+
+// Plans and launches the cluster kernel with the largest workable cluster.
+int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t ws_bytes, bool launch,
+                    size_t* ws_need, int* C_out, cudaStream_t stream) {
+  DevInfo di;
+  int st = device_info(&di);
+  if (st) return st;
+  p.status = di.status;
+  p.flags = flags;
+  const int units = d->batch * d->n_kv_heads;
+  int C = choose_cluster(d, units, di.sms);
+  const bool forced = d->reserved > 0;
+  while (true) {
+    size_t need = 0;
+    st = plan_smem(p, d, C, flags, true, &need);
+    if (st == FASA_OK && cluster_fits(d->dtype, d->head_dim, C, p.smem_total)) {
+      if (ws_need) *ws_need = need;
+      if (C_out) *C_out = C;
+      if (!launch) return FASA_OK;
+      if (need > 0) {
+        if (!ws || ws_bytes < need || !aligned16(ws)) return FASA_ERR_WORKSPACE;
+        p.scores = reinterpret_cast<float*>(ws);
+      }
+      const cudaError_t e = d->dtype == FASA_F32 ? launch_cluster_f32(p, d->head_dim, C, stream)
+                                                 : launch_cluster_bf16(p, d->head_dim, C, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      return FASA_OK;
+    }
+    if (forced || C == 1) return st ? st : FASA_ERR_UNSUPPORTED;
+    C = C > 8 ? 8 : C / 2;
+  }
+}
+
+// ---------------------------------------------------------------- aux kernels
+template <typename T, int D>
+__global__ void rope_q_kernel(const T* q, const int* pos, float* q_rot, int Hq, double base) {
+  __shared__ float2 cs[D / 2];
+  const int b = blockIdx.x;
+  const int m = pos[b];
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) cs[i] = rope_cos_sin(base, i, D, m);
+  __syncthreads();
+  const T* qb = q + (size_t)b * Hq * D;
+  float* ob = q_rot + (size_t)b * Hq * D;
+  for (int x = threadIdx.x; x < Hq * (D / 2); x += blockDim.x) {
+    const int hq = x / (D / 2), i = x - hq * (D / 2);
+    const float x0 = to_f32<T>(qb[hq * D + 2 * i]), x1 = to_f32<T>(qb[hq * D + 2 * i + 1]);
+    const float2 c = cs[i];
+    ob[hq * D + 2 * i] = x0 * c.x - x1 * c.y;
+    ob[hq * D + 2 * i + 1] = x0 * c.y + x1 * c.x;
+  }
+}
+
+// One FC pair (2 elements) moved as a single word.
+template <typename T>
+struct Pair;
+template <>
+struct Pair<float> {
+  using type = float2;
+};
+template <>
+struct Pair<__nv_bfloat16> {
+  using type = uint32_t;
+};
+
+template <typename T>
+__global__ void build_kdom_kernel(const T* K, const int* dom, const int* lens, T* kd, int Hkv, int T_max, int D,
+                                  int n, int* status) {
+  using P = typename Pair<T>::type;
+  const int unit = blockIdx.y;
+  const int b = unit / Hkv, h = unit - b * Hkv;
+  int len = T_max;
+  if (lens) {
+    len = lens[b];
+    if (len < 0 || len > T_max) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, 1);
+      len = min(max(len, 0), T_max);
+    }
+  }
+  const int tau = blockIdx.x * blockDim.x + threadIdx.x;
+  if (tau >= len) return;
+  const P* row = reinterpret_cast<const P*>(K + ((size_t)unit * T_max + tau) * D);
+  P* dst = reinterpret_cast<P*>(kd) + (size_t)unit * n * T_max + tau;
+  for (int j = 0; j < n; ++j) {
+    int i = dom[h * n + j];
+    if (i < 0 || i >= D / 2) {
+      atomicOr(status, 1);
+      i = min(max(i, 0), D / 2 - 1);
+    }
+    dst[(size_t)j * T_max] = row[i];
+  }
+}
+
+template <typename T>
+__global__ void append_kdom_kernel(const T* k_new, const int* dom, const int* tok_pos, T* kd, int Hkv, int T_max,
+                                   int D, int n, int* status) {
+  using P = typename Pair<T>::type;
+  const int unit = blockIdx.x;
+  const int b = unit / Hkv, h = unit - b * Hkv;
+  int t = tok_pos[b];
+  if (t < 0 || t >= T_max) {
+    if (threadIdx.x == 0) atomicOr(status, 1);
+    return;
+  }
+  const P* row = reinterpret_cast<const P*>(k_new + (size_t)unit * D);
+  P* dst = reinterpret_cast<P*>(kd) + (size_t)unit * n * T_max + t;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    int i = dom[h * n + j];
+    if (i < 0 || i >= D / 2) {
+      atomicOr(status, 1);
+      i = min(max(i, 0), D / 2 - 1);
+    }
+    dst[(size_t)j * T_max] = row[i];
+  }
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+int fasa_version(void) { return 100; }
+
+const char* fasa_status_string(int status) {
+  switch (status) {
+    case FASA_OK: return "FASA_OK";
+    case FASA_ERR_INVALID_ARG: return "FASA_ERR_INVALID_ARG";
+    case FASA_ERR_UNSUPPORTED: return "FASA_ERR_UNSUPPORTED";
+    case FASA_ERR_WORKSPACE: return "FASA_ERR_WORKSPACE";
+    case FASA_ERR_CUDA: return "FASA_ERR_CUDA";
+    default: return "FASA_ERR_UNKNOWN";
+  }
+}
+
+int fasa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int fasa_max_budget(const fasa_dims_t* dims, int32_t* max_budget) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!max_budget) return FASA_ERR_INVALID_ARG;
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  // the fused step has the tightest shared-memory plan; search its limit
+  int lo = 0, hi = 1 << 20;
+  const int flags = F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    Params p;
+    fill_common(p, dims, mid, di.status);
+    size_t ws = 0;
+    bool ok = false;
+    for (int C = choose_cluster(dims, dims->batch * dims->n_kv_heads, di.sms); C >= 1; C = C > 8 ? 8 : C / 2) {
+      if (plan_smem(p, dims, C, flags, true, &ws) == FASA_OK) {
+        ok = true;
+        break;
+      }
+      if (dims->reserved > 0) break;
+    }
+    if (ok) lo = mid;
+    else hi = mid - 1;
+  }
+  *max_budget = lo;
+  return FASA_OK;
+}
+
+int fasa_workspace_size(const fasa_dims_t* dims, int32_t budget, size_t* bytes) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!bytes || budget < 1) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  return plan_and_launch(p, dims, F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT, nullptr, 0, false, bytes, nullptr,
+                         nullptr);
+}
+
+int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!ctas) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, 1, nullptr);
+  int C = 0;
+  st = plan_and_launch(p, dims, F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT, nullptr, 0, false, nullptr, &C,
+                       nullptr);
+  if (st) return st;
+  *ctas = C;
+  return FASA_OK;
+}
+
+int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot, const fasa_dims_t* dims,
+                      fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q || !pos || !q_rot) return FASA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int D = dims->head_dim;
+  const dim3 grid(dims->batch);
+  const int Hq = dims->n_q_heads;
+  if (dims->dtype == FASA_F32) {
+    if (D == 128) rope_q_kernel<float, 128><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, dims->rope_theta);
+    else rope_q_kernel<float, 64><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, dims->rope_theta);
+  } else {
+    using B16 = __nv_bfloat16;
+    if (D == 128) rope_q_kernel<B16, 128><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, dims->rope_theta);
+    else rope_q_kernel<B16, 64><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, dims->rope_theta);
+  }
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+int fasa_build_kdom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens, void* k_dom,
+                    const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!k_cache || !dom_fc || !k_dom) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(k_dom)) return FASA_ERR_INVALID_ARG;
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(ceil_div(dims->t_max, 256), dims->batch * dims->n_kv_heads);
+  if (dims->dtype == FASA_F32)
+    build_kdom_kernel<float><<<grid, 256, 0, s>>>((const float*)k_cache, dom_fc, seq_lens, (float*)k_dom,
+                                                  dims->n_kv_heads, dims->t_max, dims->head_dim, dims->n_tip,
+                                                  di.status);
+  else
+    build_kdom_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)k_cache, dom_fc, seq_lens,
+                                                          (__nv_bfloat16*)k_dom, dims->n_kv_heads, dims->t_max,
+                                                          dims->head_dim, dims->n_tip, di.status);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+int fasa_append_kdom(const void* k_new, const int32_t* dom_fc, const int32_t* tok_pos, void* k_dom,
+                     const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!k_new || !dom_fc || !tok_pos || !k_dom) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_dom)) return FASA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) & (uintptr_t)(2 * elem_size(dims) - 1)) != 0) return FASA_ERR_INVALID_ARG;
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(dims->batch * dims->n_kv_heads);
+  const int threads = dims->n_tip < 32 ? 32 : 64;
+  if (dims->dtype == FASA_F32)
+    append_kdom_kernel<float><<<grid, threads, 0, s>>>((const float*)k_new, dom_fc, tok_pos, (float*)k_dom,
+                                                       dims->n_kv_heads, dims->t_max, dims->head_dim, dims->n_tip,
+                                                       di.status);
+  else
+    append_kdom_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>((const __nv_bfloat16*)k_new, dom_fc, tok_pos,
+                                                               (__nv_bfloat16*)k_dom, dims->n_kv_heads,
+                                                               dims->t_max, dims->head_dim, dims->n_tip, di.status);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+int fasa_tip_score(const float* q_rot, const void* k_dom, const int32_t* dom_fc, const int32_t* seq_lens,
+                   float* scores, const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q_rot || !k_dom || !dom_fc || !seq_lens || !scores) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_dom) || !aligned16(scores) || !aligned16(q_rot)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, 1, nullptr);
+  p.q_rot = q_rot;
+  p.k_dom = k_dom;
+  p.dom_fc = dom_fc;
+  p.seq_lens = seq_lens;
+  p.scores = scores;
+  return plan_and_launch(p, dims, F_TIP, nullptr, 0, true, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fasa_topk_select(const float* scores, const int32_t* seq_lens, int32_t budget, int32_t* idx, int32_t* count,
+                     const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!scores || !seq_lens || !idx || !count || budget < 1) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(scores)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.scores_in = scores;
+  p.seq_lens = seq_lens;
+  p.idx_out = idx;
+  p.count_out = count;
+  return plan_and_launch(p, dims, F_SC_IN | F_SELECT | F_IDX_OUT, nullptr, 0, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fasa_focused_attention(const float* q_rot, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                           const int32_t* idx, const int32_t* count, int32_t budget, float* out,
+                           const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q_rot || !k_cache || !v_cache || !seq_lens || !idx || !count || !out || budget < 1)
+    return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_rot) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.q_rot = q_rot;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.seq_lens = seq_lens;
+  p.idx_in = idx;
+  p.count_in = count;
+  p.out = out;
+  return plan_and_launch(p, dims, F_FAC | F_IDX_IN, nullptr, 0, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fasa_dense_attention(const float* q_rot, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                         float* out, const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q_rot || !k_cache || !v_cache || !seq_lens || !out) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_rot) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, 1, nullptr);
+  p.q_rot = q_rot;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  return plan_and_launch(p, dims, F_DENSE, nullptr, 0, true, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fasa_decode_step(const void* q, const int32_t* pos, const void* k_cache, const void* v_cache, const void* k_dom,
+                     const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget, float* out, int32_t* idx_out,
+                     int32_t* count_out, void* workspace, size_t workspace_bytes, const fasa_dims_t* dims,
+                     fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q || !pos || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
+    return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.q = q;
+  p.pos = pos;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_dom = k_dom;
+  p.dom_fc = dom_fc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.idx_out = idx_out;
+  p.count_out = count_out;
+  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC;
+  if (idx_out || count_out) flags |= F_IDX_OUT;
+  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fasa_device_status(fasa_stream_t stream, int32_t* status) {
+  if (!status) return FASA_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  *status = v;
+  return FASA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,18 @@
+// Instantiations of the cluster kernel for bf16 storage.
+#include "fasa_cluster.cuh"
+
+namespace fasa {
+
+cudaError_t launch_cluster_bf16(const Params& p, int head_dim, int C, cudaStream_t s) {
+  if (head_dim == 128) return launch_cluster_t<__nv_bfloat16, 128>(p, C, s);
+  if (head_dim == 64) return launch_cluster_t<__nv_bfloat16, 64>(p, C, s);
+  return cudaErrorInvalidValue;
+}
+
+int max_active_clusters_bf16(int head_dim, int C, int smem_bytes) {
+  if (head_dim == 128) return max_clusters_t<__nv_bfloat16, 128>(C, smem_bytes);
+  if (head_dim == 64) return max_clusters_t<__nv_bfloat16, 64>(C, smem_bytes);
+  return 0;
+}
+
+}  // namespace fasa

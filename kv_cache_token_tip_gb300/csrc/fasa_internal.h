@@ -1,0 +1,67 @@
+// Internal definitions shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fasa {
+
+constexpr int NT = 256;          // threads per CTA of the cluster kernel
+constexpr int NW = NT / 32;      // warps per CTA
+constexpr int RT = 32;           // FAC rows per pipeline tile
+constexpr int FAC_STAGES = 4;    // cp.async ring depth of the FAC gather
+constexpr int G_MAX = 8;         // largest GQA group
+constexpr int C_MAX = 16;        // largest cluster
+constexpr int MISC_BYTES = 4096; // broadcast / reduction scratch in shared memory
+
+// What one launch of the cluster kernel does.
+enum : int {
+  F_ROPE = 1 << 0,     // q is the pre-RoPE stored query: rotate in the kernel
+  F_TIP = 1 << 1,      // compute TIP scores from k_dom
+  F_SC_IN = 1 << 2,    // take scores from p.scores_in instead
+  F_SELECT = 1 << 3,   // top-k selection
+  F_IDX_OUT = 1 << 4,  // write idx / count
+  F_FAC = 1 << 5,      // attention over the selected rows
+  F_IDX_IN = 1 << 6,   // selected rows come from p.idx_in / p.count_in
+  F_DENSE = 1 << 7,    // attention over every cached row
+};
+
+struct Params {
+  int B, Hq, Hkv, G, T_max, n_tip, budget, flags;
+  double rope_theta;
+  const void* q;            // pre-RoPE stored query (F_ROPE)
+  const float* q_rot;       // rotated fp32 query (otherwise)
+  const int* pos;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_dom;
+  const int* dom_fc;
+  const int* seq_lens;
+  const float* scores_in;   // F_SC_IN
+  float* scores;            // TIP output (s_cap == 0) -- global [B,Hkv,T_max]
+  const int* idx_in;        // F_IDX_IN
+  const int* count_in;
+  int* idx_out;             // F_IDX_OUT
+  int* count_out;
+  float* out;               // [B,Hq,D] fp32
+  int* status;              // device status word
+  // shared-memory layout (bytes), computed by the host
+  int s_cap;                // scores kept per CTA in shared memory (0: global)
+  int tip_tile;             // tokens per TIP pipeline tile
+  int tip_stages;           // TIP ring depth
+  int cand_cap;             // candidate entries per CTA
+  int idx_cap;              // selected-index entries per CTA
+  int hpc;                  // heads combined per CTA = ceil(G / C)
+  int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hist, off_sc, off_idx, off_part,
+      off_big, smem_total;
+};
+
+// Kernel launchers (one translation unit per storage type).
+cudaError_t launch_cluster_bf16(const Params& p, int head_dim, int C, cudaStream_t s);
+cudaError_t launch_cluster_f32(const Params& p, int head_dim, int C, cudaStream_t s);
+// Prepares function attributes and returns the number of co-resident clusters
+// of size C for this configuration (0 if C cannot be launched).
+int max_active_clusters_bf16(int head_dim, int C, int smem_bytes);
+int max_active_clusters_f32(int head_dim, int C, int smem_bytes);
+
+}  // namespace fasa

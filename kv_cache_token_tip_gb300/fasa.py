@@ -1,0 +1,226 @@
+"""ctypes binding of libfasa.so.
+
+Each function has the name of its C entry point and takes torch CUDA tensors
+(or raw device addresses as ints).  It checks dtypes and contiguity, passes
+``data_ptr()`` and the current CUDA stream, and raises ``FasaError`` on a
+non-zero status.  Nothing here computes on the data.
+"""
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "libfasa.so")
+
+FASA_F32, FASA_BF16 = 0, 1
+FASA_DEV_BAD_INPUT, FASA_DEV_TIMEOUT = 1, 2
+
+EXPORTS = [
+    "fasa_version", "fasa_status_string", "fasa_last_cuda_error", "fasa_max_budget",
+    "fasa_workspace_size", "fasa_apply_rope_q", "fasa_build_kdom", "fasa_append_kdom",
+    "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
+    "fasa_decode_step", "fasa_device_status", "fasa_cluster_size",
+]
+
+
+class FasaError(RuntimeError):
+    def __init__(self, fn, status, lib):
+        msg = lib.fasa_status_string(status).decode()
+        if status == 4:
+            msg += f" (cudaError {lib.fasa_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+class FasaDims(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("t_max", ctypes.c_int32), ("n_tip", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_double),
+    ]
+
+
+def dims_for(cfg, cluster_ctas: int = 0, **override) -> FasaDims:
+    """FasaDims from a workload config (anything with the same field names)."""
+    d = dict(batch=cfg.batch, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+             head_dim=cfg.head_dim, t_max=cfg.context, n_tip=cfg.n_tip,
+             dtype=FASA_F32 if cfg.dtype == "f32" else FASA_BF16, rope_theta=cfg.rope_theta)
+    d.update(override)
+    return FasaDims(d["batch"], d["n_q_heads"], d["n_kv_heads"], d["head_dim"], d["t_max"],
+                    d["n_tip"], d["dtype"], cluster_ctas, float(d["rope_theta"]))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libfasa.so once.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -m kv_cache_token_tip_gb300.build` (there is no fallback)")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        dp = ctypes.POINTER(FasaDims)
+        sig = {
+            "fasa_version": ([], ctypes.c_int),
+            "fasa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "fasa_last_cuda_error": ([], ctypes.c_int),
+            "fasa_max_budget": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
+            "fasa_workspace_size": ([dp, i32, ctypes.POINTER(sz)], ctypes.c_int),
+            "fasa_cluster_size": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
+            "fasa_apply_rope_q": ([vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_build_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_append_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_tip_score": ([vp, vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_topk_select": ([vp, vp, i32, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_focused_attention": ([vp, vp, vp, vp, vp, vp, i32, vp, dp, vp], ctypes.c_int),
+            "fasa_dense_attention": ([vp, vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_decode_step": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
+                                 ctypes.c_int),
+            "fasa_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr(x, dtype=None, name="tensor"):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and x.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {x.dtype}, expected {dtype}")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _store_dtypes():
+    import torch
+    return (torch.float32, torch.bfloat16)
+
+
+def _check(fn, st):
+    if st != 0:
+        raise FasaError(fn, st, lib())
+
+
+def _i32():
+    import torch
+    return torch.int32
+
+
+def _f32():
+    import torch
+    return torch.float32
+
+
+# ---------------------------------------------------------------- entry points
+def fasa_max_budget(dims: FasaDims) -> int:
+    out = ctypes.c_int32(0)
+    _check("fasa_max_budget", lib().fasa_max_budget(ctypes.byref(dims), ctypes.byref(out)))
+    return out.value
+
+
+def fasa_workspace_size(dims: FasaDims, budget: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("fasa_workspace_size", lib().fasa_workspace_size(ctypes.byref(dims), budget, ctypes.byref(out)))
+    return out.value
+
+
+def fasa_cluster_size(dims: FasaDims) -> int:
+    out = ctypes.c_int32(0)
+    _check("fasa_cluster_size", lib().fasa_cluster_size(ctypes.byref(dims), ctypes.byref(out)))
+    return out.value
+
+
+def fasa_apply_rope_q(q, pos, q_rot, dims: FasaDims, stream=None):
+    _check("fasa_apply_rope_q", lib().fasa_apply_rope_q(
+        _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"), _ptr(q_rot, _f32(), "q_rot"),
+        ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_build_kdom(k_cache, dom_fc, seq_lens, k_dom, dims: FasaDims, stream=None):
+    _check("fasa_build_kdom", lib().fasa_build_kdom(
+        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens"), _ptr(k_dom, _store_dtypes(), "k_dom"),
+        ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_append_kdom(k_new, dom_fc, tok_pos, k_dom, dims: FasaDims, stream=None):
+    _check("fasa_append_kdom", lib().fasa_append_kdom(
+        _ptr(k_new, _store_dtypes(), "k_new"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(tok_pos, _i32(), "tok_pos"), _ptr(k_dom, _store_dtypes(), "k_dom"),
+        ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_tip_score(q_rot, k_dom, dom_fc, seq_lens, scores, dims: FasaDims, stream=None):
+    _check("fasa_tip_score", lib().fasa_tip_score(
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_dom, _store_dtypes(), "k_dom"),
+        _ptr(dom_fc, _i32(), "dom_fc"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(scores, _f32(), "scores"), ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_topk_select(scores, seq_lens, budget: int, idx, count, dims: FasaDims, stream=None):
+    _check("fasa_topk_select", lib().fasa_topk_select(
+        _ptr(scores, _f32(), "scores"), _ptr(seq_lens, _i32(), "seq_lens"), int(budget),
+        _ptr(idx, _i32(), "idx"), _ptr(count, _i32(), "count"), ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_focused_attention(q_rot, k_cache, v_cache, seq_lens, idx, count, budget: int, out,
+                           dims: FasaDims, stream=None):
+    _check("fasa_focused_attention", lib().fasa_focused_attention(
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
+        _ptr(v_cache, _store_dtypes(), "v_cache"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(idx, _i32(), "idx"), _ptr(count, _i32(), "count"), int(budget),
+        _ptr(out, _f32(), "out"), ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_dense_attention(q_rot, k_cache, v_cache, seq_lens, out, dims: FasaDims, stream=None):
+    _check("fasa_dense_attention", lib().fasa_dense_attention(
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
+        _ptr(v_cache, _store_dtypes(), "v_cache"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(out, _f32(), "out"), ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: int, out,
+                     idx_out=None, count_out=None, workspace=None, dims: FasaDims = None, stream=None):
+    ws_bytes = 0
+    if workspace is not None and not isinstance(workspace, int):
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fasa_decode_step", lib().fasa_decode_step(
+        _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"),
+        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
+        _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
+        _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_device_status(stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("fasa_device_status", lib().fasa_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
