@@ -267,7 +267,8 @@ def make_replicas(cfg, R, dims):
     reps = []
     for r in range(R):
         L = gpu_gen.make_layer(cfg, layer=r)
-        kd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.n_tip, cfg.context, 2), dtype=L.k.dtype, device="cuda")
+        kd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.context // 64, cfg.n_tip, 64, 2), dtype=L.k.dtype,
+                         device="cuda")
         fasa_build_kdom(L.k, L.dom_fc, L.seq_lens, kd, dims)
         reps.append((L, kd))
     torch.cuda.synchronize()
@@ -334,7 +335,8 @@ def run_gpu(args):
     g_warm = capture(step, W, stream) if W else None
     torch.cuda.synchronize()
     if g_warm is not None:
-        g_warm.replay()
+        with torch.cuda.stream(stream):
+            g_warm.replay()
     torch.cuda.synchronize()
     status = fasa_device_status(stream)
     if status:
@@ -344,12 +346,13 @@ def run_gpu(args):
     barrier(pg, local)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for _ in range(K // chunk):
-            g_chunk.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):   # graphs replay on the current stream
+            ev0.record(stream)
+            for _ in range(K // chunk):
+                g_chunk.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
         torch.cuda.synchronize()
     barrier(pg, local)
     torch.cuda.synchronize()
@@ -360,12 +363,13 @@ def run_gpu(args):
     # dense baseline (same machinery), fewer steps
     Kd = max(R, min(K // 8, 4096))
     g_dense = capture(dense_step, Kd, stream)
-    g_dense.replay()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g_dense.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        g_dense.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        g_dense.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     dense_sec = e0.elapsed_time(e1) / 1e3 / Kd
 

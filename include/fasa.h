@@ -24,8 +24,9 @@
  *      pos       [B]                   int32, query position (usually = len)
  *      k_cache   [B, Hkv, T_max, d]    storage dtype, keys AFTER RoPE
  *      v_cache   [B, Hkv, T_max, d]    storage dtype
- *      k_dom     [B, Hkv, n_tip, T_max, 2]  storage dtype, FC-major side copy
- *                                      of the dominant key columns
+ *      k_dom     [B, Hkv, T_max/64, n_tip, 64, 2]  storage dtype: the
+ *                                      dominant key columns, FC-major within
+ *                                      blocks of 64 tokens
  *      dom_fc    [Hkv, n_tip]          int32, dominant FC indices in [0, d/2)
  *      seq_lens  [B]                   int32, cached tokens 0..len-1
  *      scores    [B, Hkv, T_max]       fp32 (entries tau >= len unspecified)
@@ -35,7 +36,7 @@
  *    Query head hq belongs to KV head hq / G, G = Hq / Hkv.
  *  - Frequency chunk (FC) i is the interleaved pair of dimensions (2i, 2i+1).
  *  - Alignment: k_cache, v_cache, k_dom, scores, q_rot and out must be
- *    16-byte aligned; T_max must be a multiple of 16.
+ *    16-byte aligned; T_max must be a multiple of 64.
  *  - Supported: dtype FASA_F32 or FASA_BF16 (q, caches and k_dom share it),
  *    head_dim 64 or 128, 1 <= G <= 8, 1 <= budget <= fasa_max_budget().
  */
@@ -77,7 +78,7 @@ typedef struct fasa_dims {
   int32_t t_max;       /* cache capacity per (b, KV head)     */
   int32_t n_tip;       /* dominant FCs per KV head, 1..d/2    */
   int32_t dtype;       /* FASA_F32 or FASA_BF16               */
-  int32_t reserved;    /* must be 0                           */
+  int32_t reserved;    /* 0, or a cluster size 1..16 to force  */
   double rope_theta;   /* RoPE base B: theta_i = B^(-2i/d)    */
 } fasa_dims_t;
 
@@ -104,16 +105,20 @@ int fasa_workspace_size(const fasa_dims_t* dims, int32_t budget, size_t* bytes);
  * RoPE of the query ("FASA: Frequency-aware Sparse Attention", §3.4 "RoPE from
  * a Frequency-Chunk Perspective": theta_i = B^(-2i/d); each FC is turned by the
  * 2x2 rotation R_{m,theta_i}, m = pos[b]).  q_rot = R(pos) q, fp32.
- * Angles are formed and range-reduced in fp64.
+ * The angle m * theta_i is formed exactly in 64-bit fixed-point turns
+ * (theta_i / 2pi tabulated from a double-precision pow), so its error does not
+ * grow with the position; cos/sin are evaluated in fp32.
  */
 int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot,
                       const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
  * Builds the dominant key cache C_key^dom (same page, "Hardware-Aware Variants",
- * FASA-M/FASA-C: t x d_dom per head, d_dom = 2 N_tip) in FC-major layout:
- * k_dom[b,h,j,tau,0:2] = k_cache[b,h,tau, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2] for
- * tau < seq_lens[b] (all tau < T_max when seq_lens is NULL).  A pure copy.
+ * FASA-M/FASA-C: t x d_dom per head, d_dom = 2 N_tip), FC-major within blocks
+ * of 64 tokens: k_dom[b,h,tau/64,j,tau%64,0:2] =
+ * k_cache[b,h,tau, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2] for tau < seq_lens[b]
+ * (all tau < T_max when seq_lens is NULL).  A pure copy; one tile of whole
+ * blocks is one contiguous range, so the TIP stage moves it with one bulk copy.
  */
 int fasa_build_kdom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens,
                     void* k_dom, const fasa_dims_t* dims, fasa_stream_t stream);
@@ -128,7 +133,7 @@ int fasa_append_kdom(const void* k_new, const int32_t* dom_fc, const int32_t* to
 /*
  * TIP (same page, §3.4 "Online Stage 1: Token Importance Predictor"): for
  * every cached token tau < len_b,
- *   scores[b,h,tau] = sum_{hq in group(h)} sum_j q_rot[b,hq]^[dom_fc[h,j]] . k_dom[b,h,j,tau,:]
+ *   scores[b,h,tau] = sum_{hq in group(h)} sum_j q_rot[b,hq]^[dom_fc[h,j]] . k_dom[b,h,tau/64,j,tau%64,:]
  * i.e. the FC-restricted score S_t summed over the GQA group (no 1/sqrt(d)).
  */
 int fasa_tip_score(const float* q_rot, const void* k_dom, const int32_t* dom_fc,

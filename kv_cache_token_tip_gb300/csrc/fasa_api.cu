@@ -39,7 +39,7 @@ int check_dims(const fasa_dims_t* d) {
   if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1) return FASA_ERR_INVALID_ARG;
   if (d->n_q_heads % d->n_kv_heads) return FASA_ERR_INVALID_ARG;
   if (d->head_dim < 2 || (d->head_dim & 1)) return FASA_ERR_INVALID_ARG;
-  if (d->t_max < 1 || (d->t_max % 16)) return FASA_ERR_INVALID_ARG;
+  if (d->t_max < 1 || (d->t_max % KDOM_BLOCK)) return FASA_ERR_INVALID_ARG;
   if (d->n_tip < 1 || d->n_tip > d->head_dim / 2) return FASA_ERR_INVALID_ARG;
   if (!(d->rope_theta > 0.0) || !isfinite(d->rope_theta)) return FASA_ERR_INVALID_ARG;
   if (d->reserved < 0 || d->reserved > C_MAX) return FASA_ERR_INVALID_ARG;
@@ -54,6 +54,7 @@ int elem_size(const fasa_dims_t* d) { return d->dtype == FASA_F32 ? 4 : 2; }
 
 struct DevInfo {
   int sms = 0;
+  int smem_optin = 0;
   int* status = nullptr;
 };
 
@@ -69,6 +70,9 @@ int device_info(DevInfo* out) {
     DevInfo di;
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (di.smem_optin > SMEM_LIMIT) di.smem_optin = SMEM_LIMIT;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_status);
     if (e != cudaSuccess) return cuda_fail(e);
     it = cache.emplace(dev, di).first;
@@ -77,27 +81,41 @@ int device_info(DevInfo* out) {
   return FASA_OK;
 }
 
-// Whether a cluster of C CTAs with `smem` bytes each can be resident.
-bool cluster_fits(int dtype, int D, int C, int smem) {
+// How many clusters of C CTAs with `smem` bytes each can be resident at once
+// (0: the cluster cannot be launched).  Cached per configuration.
+int cluster_capacity(int flags, int dtype, int D, int C, int smem) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int>, bool> cache;
+  static std::map<std::tuple<int, int, int, int, int, int>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, dtype, D, C, smem);
+  const int kind = kind_of(flags);
+  const auto key = std::make_tuple(dev, kind, dtype, D, C, smem);
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const int n = dtype == FASA_F32 ? max_active_clusters_f32(D, C, smem) : max_active_clusters_bf16(D, C, smem);
-  const bool ok = n >= 1;
-  cache.emplace(key, ok);
-  return ok;
+  const int n = dtype == FASA_F32 ? max_active_clusters_f32(flags, D, C, smem)
+                                  : max_active_clusters_bf16(flags, D, C, smem);
+  cache.emplace(key, n);
+  return n;
 }
 
-// Shared-memory plan of one launch.  Returns FASA_OK, or FASA_ERR_UNSUPPORTED
-// when it cannot fit.  *ws = global workspace bytes the plan needs.
-int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, size_t* ws) {
+// Shared-memory plan of one launch (byte offsets into dynamic shared memory).
+//
+// Persistent regions: mbarriers, scratch, rotated queries, the query restricted
+// to the dominant FCs, the tile logits, the local and cluster histograms, the
+// CTA's scores, the selected-index list, this CTA's candidate list (read by
+// the other CTAs) and the partial attention record (read by the combining
+// CTA).  The "big" region is the TIP ring during the scan, then the pulled
+// candidate list followed by the FAC ring.
+//
+// Returns FASA_OK, or FASA_ERR_UNSUPPORTED when it cannot fit in `limit`
+// bytes.  *ws = global workspace bytes needed.
+int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, size_t* ws, int limit) {
   const int D = d->head_dim, es = elem_size(d), G = d->n_q_heads / d->n_kv_heads;
   const int nfc = d->n_tip;
+  const bool select = (flags & F_SELECT) != 0;
+  const bool tip = (flags & F_TIP) != 0;
+  const bool fac = (flags & (F_FAC | F_DENSE)) != 0;
   int off = 0;
   p.off_bar = off;
   off += 64;
@@ -109,39 +127,19 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   off += align_up(2 * nfc * 4, 16);
   p.off_stile = off;
   off += G_MAX * RT * 4;
-  p.off_hist = off;
-  off += 2 * 256 * 4;
-
-  // TIP staging tile
-  int tile = 0, stages = 0, tip_big = 0;
-  if (flags & F_TIP) {
-    tile = 1024;
-    while (tile > 256 && nfc * tile * 2 * es > 65536) tile /= 2;
-    const int stage = nfc * tile * 2 * es;
-    stages = 131072 / stage;
-    stages = stages < 1 ? 1 : (stages > 4 ? 4 : stages);
-    tip_big = stages * stage;
-  }
-  p.tip_tile = tile > 0 ? tile : 256;
-  p.tip_stages = stages > 0 ? stages : 1;
-
-  const bool select = (flags & F_SELECT) != 0;
-  int sel_big = 0;
-  if (select) {
-    const int want = 16 * 1024 * 8;  // room for 16K candidates when it fits
-    sel_big = want > 8 * p.budget ? want : 8 * p.budget;
-  }
-  const int fac_big = (flags & (F_FAC | F_DENSE)) ? FAC_STAGES * 2 * RT * (D * es + 16) : 0;
-
+  p.off_hloc = off;
+  off += select ? HLOC_BINS * 4 : 0;
+  p.off_hlead = off;
+  off += select ? HLEAD_BINS * 4 : 0;
   p.idx_cap = (flags & (F_SELECT | F_IDX_IN)) ? align_up(p.budget, 4) : 0;
   p.hpc = ceil_div(G, C);
-  const int part_bytes = (flags & (F_FAC | F_DENSE)) ? p.hpc * C * (D + 2) * 4 : 0;
+  const int part_bytes = fac ? G * (D + 4) * 4 : 0;
+  const int fac_big = fac ? FAC_STAGES * 2 * RT * (D * es + 16) : 0;
 
-  // scores in shared memory when the fused path holds them
   int s_cap = 0;
   *ws = 0;
-  if ((flags & F_TIP) && select) {
-    const int chunk = align_up(ceil_div(d->t_max, C), 16);
+  if (tip && select) {
+    const int chunk = align_up(ceil_div(d->t_max, C), KDOM_BLOCK);
     if (chunk <= S_CAP_MAX) s_cap = chunk;
   }
   for (int attempt = 0; attempt < 2; ++attempt) {
@@ -150,29 +148,47 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
     o += s_cap * 4;
     p.off_idx = o;
     o += p.idx_cap * 4;
+    // candidate capacity: the budget plus as much slack (up to 4096) as fits
+    // next to the FAC ring
+    int cap = 0;
+    if (select) {
+      cap = (limit - (o + part_bytes + 256) - fac_big) / 8;
+      if (cap > p.budget + 4096) cap = p.budget + 4096;
+      cap &= ~15;
+    }
+    p.cand_cap = cap;
+    p.off_own = o;
+    o += cap * 8;
     p.off_part = o;
     o += part_bytes;
     o = align_up(o, 128);
     p.off_big = o;
-    int bigsz = tip_big;
-    if (fac_big > bigsz) bigsz = fac_big;
-    int room = SMEM_LIMIT - o;
-    if (select) {
-      // candidates take whatever is left, at least the budget
-      int cand_bytes = sel_big;
-      if (cand_bytes > room) cand_bytes = room;
-      if (cand_bytes < bigsz) cand_bytes = bigsz;
-      cand_bytes &= ~7;
-      p.cand_cap = cand_bytes / 8;
-      if (cand_bytes > bigsz) bigsz = cand_bytes;
-    } else {
-      p.cand_cap = 0;
+    p.fac_off = 0;
+    int bigsz = fac_big;
+    int tile = 256, stages = 1;
+    if (tip) {
+      // the largest tile with at least two stages in the room left, up to a
+      // ring of 4 stages / 128 KB
+      const int tiles[3] = {1024, 512, 256};
+      for (int ti = 0; ti < 3; ++ti) {
+        const int stage = nfc * tiles[ti] * 2 * es;
+        int st = 131072 / stage;
+        st = st < 1 ? 1 : (st > 4 ? 4 : st);
+        while (st > 1 && o + (st * stage > bigsz ? st * stage : bigsz) > limit) --st;
+        tile = tiles[ti];
+        stages = st;
+        if (st >= 2) break;
+      }
+      const int stage = nfc * tile * 2 * es;
+      if (stages * stage > bigsz) bigsz = stages * stage;
     }
+    p.tip_tile = tile;
+    p.tip_stages = stages;
     p.smem_total = o + bigsz;
-    const bool ok = p.smem_total <= SMEM_LIMIT && (!select || p.cand_cap >= p.budget);
+    const bool ok = p.smem_total <= limit && (!select || cap >= p.budget);
     if (ok) {
       p.s_cap = s_cap;
-      if ((flags & F_TIP) && select && s_cap == 0) {
+      if (tip && select && s_cap == 0) {
         if (!allow_ws) return FASA_ERR_UNSUPPORTED;
         *ws = (size_t)d->batch * d->n_kv_heads * d->t_max * 4;
       }
@@ -184,14 +200,24 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   return FASA_ERR_UNSUPPORTED;
 }
 
-// Cluster size: the explicit override, else as many CTAs per unit as fill the
-// SMs once (at most 16), reduced until the cluster is schedulable.
-int choose_cluster(const fasa_dims_t* d, int units, int sms) {
-  if (d->reserved > 0) return d->reserved;
-  int C = sms / (units > 0 ? units : 1);
-  if (C > C_MAX) C = C_MAX;
-  if (C < 1) C = 1;
-  return C;
+// theta_i / (2 pi) as 64-bit fixed-point turns, theta_i = B^(-2i/d)
+// (cached for the last base and head dim).
+void fill_rope_turns(Params& p, const fasa_dims_t* d) {
+  static std::mutex mu;
+  static double c_theta = -1.0;
+  static int c_dim = -1;
+  static unsigned long long c_turns[64];
+  std::lock_guard<std::mutex> lk(mu);
+  if (c_theta != d->rope_theta || c_dim != d->head_dim) {
+    const long double two64_over_2pi = 18446744073709551616.0L / (2.0L * 3.14159265358979323846264338327950288L);
+    for (int i = 0; i < d->head_dim / 2 && i < 64; ++i) {
+      const double th = pow(d->rope_theta, -2.0 * i / d->head_dim);
+      c_turns[i] = (unsigned long long)((long double)th * two64_over_2pi);
+    }
+    c_theta = d->rope_theta;
+    c_dim = d->head_dim;
+  }
+  memcpy(p.rope_turns, c_turns, sizeof(c_turns));
 }
 
 void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
@@ -203,11 +229,14 @@ void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
   p.T_max = d->t_max;
   p.n_tip = d->n_tip;
   p.budget = budget;
-  p.rope_theta = d->rope_theta;
+  fill_rope_turns(p, d);
   p.status = status;
 }
 
-// Plans and launches the cluster kernel with the largest workable cluster.
+// Plans and launches the cluster kernel.  Cluster size: the explicit
+// override (dims->reserved), else the largest C (at most 16) for which every
+// unit's cluster is resident at once (one wave); when no C gives one wave,
+// the largest C <= 4 that can be launched.
 int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t ws_bytes, bool launch,
                     size_t* ws_need, int* C_out, cudaStream_t stream) {
   DevInfo di;
@@ -216,36 +245,50 @@ int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t
   p.status = di.status;
   p.flags = flags;
   const int units = d->batch * d->n_kv_heads;
-  int C = choose_cluster(d, units, di.sms);
-  const bool forced = d->reserved > 0;
-  while (true) {
-    size_t need = 0;
-    st = plan_smem(p, d, C, flags, true, &need);
-    if (st == FASA_OK && cluster_fits(d->dtype, d->head_dim, C, p.smem_total)) {
-      if (ws_need) *ws_need = need;
-      if (C_out) *C_out = C;
-      if (!launch) return FASA_OK;
-      if (need > 0) {
-        if (!ws || ws_bytes < need || !aligned16(ws)) return FASA_ERR_WORKSPACE;
-        p.scores = reinterpret_cast<float*>(ws);
-      }
-      const cudaError_t e = d->dtype == FASA_F32 ? launch_cluster_f32(p, d->head_dim, C, stream)
-                                                 : launch_cluster_bf16(p, d->head_dim, C, stream);
-      if (e != cudaSuccess) return cuda_fail(e);
-      return FASA_OK;
+  int C = 0;
+  size_t need = 0;
+  if (d->reserved > 0) {
+    st = plan_smem(p, d, d->reserved, flags, true, &need, di.smem_optin);
+    if (st) return st;
+    if (cluster_capacity(flags, d->dtype, d->head_dim, d->reserved, p.smem_total) < 1) return FASA_ERR_UNSUPPORTED;
+    C = d->reserved;
+  } else {
+    for (int c = C_MAX; c >= 1 && !C; --c) {
+      if (plan_smem(p, d, c, flags, true, &need, di.smem_optin) != FASA_OK) continue;
+      if (cluster_capacity(flags, d->dtype, d->head_dim, c, p.smem_total) >= units) C = c;
     }
-    if (forced || C == 1) return st ? st : FASA_ERR_UNSUPPORTED;
-    C = C > 8 ? 8 : C / 2;
+    for (int c = 4; c >= 1 && !C; --c) {
+      if (plan_smem(p, d, c, flags, true, &need, di.smem_optin) != FASA_OK) continue;
+      if (cluster_capacity(flags, d->dtype, d->head_dim, c, p.smem_total) >= 1) C = c;
+    }
+    if (!C) return FASA_ERR_UNSUPPORTED;
+    st = plan_smem(p, d, C, flags, true, &need, di.smem_optin);
+    if (st) return st;
   }
+  if (ws_need) *ws_need = need;
+  if (C_out) *C_out = C;
+  if (!launch) return FASA_OK;
+  if (need > 0) {
+    if (!ws || ws_bytes < need || !aligned16(ws)) return FASA_ERR_WORKSPACE;
+    p.scores = reinterpret_cast<float*>(ws);
+  }
+  const cudaError_t e = d->dtype == FASA_F32 ? launch_cluster_f32(p, d->head_dim, C, stream)
+                                             : launch_cluster_bf16(p, d->head_dim, C, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FASA_OK;
 }
 
 // ---------------------------------------------------------------- aux kernels
+struct RopeTurns {
+  unsigned long long t[64];
+};
+
 template <typename T, int D>
-__global__ void rope_q_kernel(const T* q, const int* pos, float* q_rot, int Hq, double base) {
+__global__ void rope_q_kernel(const T* q, const int* pos, float* q_rot, int Hq, const __grid_constant__ RopeTurns rt) {
   __shared__ float2 cs[D / 2];
   const int b = blockIdx.x;
   const int m = pos[b];
-  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) cs[i] = rope_cos_sin(base, i, D, m);
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) cs[i] = rope_cos_sin(rt.t[i], m);
   __syncthreads();
   const T* qb = q + (size_t)b * Hq * D;
   float* ob = q_rot + (size_t)b * Hq * D;
@@ -287,14 +330,16 @@ __global__ void build_kdom_kernel(const T* K, const int* dom, const int* lens, T
   const int tau = blockIdx.x * blockDim.x + threadIdx.x;
   if (tau >= len) return;
   const P* row = reinterpret_cast<const P*>(K + ((size_t)unit * T_max + tau) * D);
-  P* dst = reinterpret_cast<P*>(kd) + (size_t)unit * n * T_max + tau;
+  // blocked FC-major layout [unit][tau / KB][j][tau % KB]
+  P* dst = reinterpret_cast<P*>(kd) + ((size_t)unit * (T_max / KDOM_BLOCK) + tau / KDOM_BLOCK) * n * KDOM_BLOCK +
+           tau % KDOM_BLOCK;
   for (int j = 0; j < n; ++j) {
     int i = dom[h * n + j];
     if (i < 0 || i >= D / 2) {
       atomicOr(status, 1);
       i = min(max(i, 0), D / 2 - 1);
     }
-    dst[(size_t)j * T_max] = row[i];
+    dst[(size_t)j * KDOM_BLOCK] = row[i];
   }
 }
 
@@ -310,14 +355,15 @@ __global__ void append_kdom_kernel(const T* k_new, const int* dom, const int* to
     return;
   }
   const P* row = reinterpret_cast<const P*>(k_new + (size_t)unit * D);
-  P* dst = reinterpret_cast<P*>(kd) + (size_t)unit * n * T_max + t;
+  P* dst = reinterpret_cast<P*>(kd) + ((size_t)unit * (T_max / KDOM_BLOCK) + t / KDOM_BLOCK) * n * KDOM_BLOCK +
+           t % KDOM_BLOCK;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
     int i = dom[h * n + j];
     if (i < 0 || i >= D / 2) {
       atomicOr(status, 1);
       i = min(max(i, 0), D / 2 - 1);
     }
-    dst[(size_t)j * T_max] = row[i];
+    dst[(size_t)j * KDOM_BLOCK] = row[i];
   }
 }
 
@@ -357,8 +403,8 @@ int fasa_max_budget(const fasa_dims_t* dims, int32_t* max_budget) {
     fill_common(p, dims, mid, di.status);
     size_t ws = 0;
     bool ok = false;
-    for (int C = choose_cluster(dims, dims->batch * dims->n_kv_heads, di.sms); C >= 1; C = C > 8 ? 8 : C / 2) {
-      if (plan_smem(p, dims, C, flags, true, &ws) == FASA_OK) {
+    for (int C = dims->reserved > 0 ? dims->reserved : C_MAX; C >= 1; --C) {
+      if (plan_smem(p, dims, C, flags, true, &ws, di.smem_optin) == FASA_OK) {
         ok = true;
         break;
       }
@@ -404,13 +450,17 @@ int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot, const fas
   const int D = dims->head_dim;
   const dim3 grid(dims->batch);
   const int Hq = dims->n_q_heads;
+  Params tmp;
+  fill_rope_turns(tmp, dims);
+  RopeTurns rt;
+  memcpy(rt.t, tmp.rope_turns, sizeof(rt.t));
   if (dims->dtype == FASA_F32) {
-    if (D == 128) rope_q_kernel<float, 128><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, dims->rope_theta);
-    else rope_q_kernel<float, 64><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, dims->rope_theta);
+    if (D == 128) rope_q_kernel<float, 128><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, rt);
+    else rope_q_kernel<float, 64><<<grid, 256, 0, s>>>((const float*)q, pos, q_rot, Hq, rt);
   } else {
     using B16 = __nv_bfloat16;
-    if (D == 128) rope_q_kernel<B16, 128><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, dims->rope_theta);
-    else rope_q_kernel<B16, 64><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, dims->rope_theta);
+    if (D == 128) rope_q_kernel<B16, 128><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, rt);
+    else rope_q_kernel<B16, 64><<<grid, 256, 0, s>>>((const B16*)q, pos, q_rot, Hq, rt);
   }
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);

@@ -3,21 +3,24 @@
 // One thread-block cluster of C CTAs owns one (batch, KV head) unit and runs
 // the whole path on it without leaving the chip:
 //
-//   1. RoPE of the G query heads of the group (angles in fp64), and the
-//      GQA-summed query restricted to the dominant FCs.
+//   1. RoPE of the G query heads of the group and the GQA-summed query
+//      restricted to the dominant FCs.  Angles come from fixed-point turns
+//      (pos * theta_i / 2pi in 64-bit integer arithmetic), so no fp64 is used.
 //   2. TIP: each CTA streams its contiguous token range of the FC-major
 //      dominant key copy with 1-D bulk (TMA) copies into a shared-memory ring
-//      and forms S_tau = sum_j qbar^[j] . k_dom[j, tau] (fp32).  Scores stay in
-//      shared memory.
-//   3. Top-k: a radix select over order-preserving 32-bit keys, distributed
-//      over the cluster.  Each CTA histograms its scores (8-bit digits); the
-//      CTAs read each other's histograms through distributed shared memory
-//      and all reach the same digit.  Once the threshold bucket is small the
-//      CTAs push their candidate (key, token) pairs, in token order, into
-//      every CTA's shared memory; each CTA then finishes the selection
-//      locally and compacts the selected tokens in ascending order.
+//      and forms S_tau = sum_j qbar^[j] . k_dom[j, tau] in fp32.  The scores
+//      stay in shared memory; the first 12-bit histogram of their
+//      order-preserving keys is built on the way.
+//   3. Top-k: a radix select over 32-bit keys with digits of 12, 10 and 10
+//      bits.  Each CTA adds its non-zero histogram bins into the leader CTA
+//      with distributed-shared-memory reductions; after one cluster barrier
+//      every CTA reads the totals and finds the same threshold digit.  When
+//      the keys at or above the threshold bucket fit the candidate buffer,
+//      each CTA lists its own candidates (token order) and every CTA pulls the
+//      concatenated list, finishes the selection locally and compacts the
+//      chosen tokens in ascending order.
 //   4. FAC: the selected rows are split evenly over the cluster; each CTA
-//      gathers its K and V rows with cp.async into a padded ring, computes the
+//      gathers its K and V rows with cp.async into a padded ring, forms the
 //      logits and an online softmax in fp32 (exp2 of log2(e)/sqrt(d)-scaled
 //      logits), and pushes its partial (m, l, o) per head to the CTA that
 //      combines that head.
@@ -41,14 +44,13 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s for one bulk-copy wait
 enum : int { MODE_NONE = 0, MODE_FILL = 1, MODE_TIES = 2, MODE_CAND = 3 };
 
 struct Misc {
-  int dstar, cnt_gt, bucket, failed;
-  int ncand, pad0, pad1, pad2;
-  int aboveR[C_MAX];
-  int bucketR[C_MAX];
-  int needR[C_MAX];
+  int dstar, cnt_gt, bucket, my_count;
+  int ncand, my_above, my_ties, pad0;
+  int cntR[C_MAX];
   int offR[C_MAX];
-  int wsum[NW][C_MAX];
+  int tiesR[C_MAX];
   int scan[NW];
+  int scan2[NW];
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -60,6 +62,34 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sums eight per-lane values over the 32 lanes of a warp with 9 shuffles
+// (instead of 8 x 5): each halving step exchanges the half of the values the
+// partner keeps.  On return lane L holds the total of value index
+// ((L >> 2) & 7) in bit order (bit 4 of L selects the upper four values,
+// bit 3 the upper two of those, bit 2 the odd one).
+__device__ __forceinline__ float warp_sum8(const float (&a)[8], int lane) {
+  float b[4], c[2];
+  const bool u4 = lane & 16, u2 = lane & 8, u1 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u4 ? a[i] : a[i + 4];
+    const float keep = u4 ? a[i + 4] : a[i];
+    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u2 ? b[i] : b[i + 2];
+    const float keep = u2 ? b[i + 2] : b[i];
+    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float send = u1 ? c[0] : c[1];
+  const float keep = u1 ? c[1] : c[0];
+  float v = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
   return v;
 }
 
@@ -87,15 +117,6 @@ __device__ __forceinline__ int block_excl_scan(int x, int* scratch, int& total) 
   return before + incl - x;
 }
 
-// Warp-aggregated histogram increment; all 32 lanes must call it.
-__device__ __forceinline__ void hist_add(uint32_t* H, uint32_t bin, bool valid, int lane) {
-  const unsigned m = __ballot_sync(0xffffffffu, valid);
-  if (valid) {
-    const unsigned peers = __match_any_sync(m, bin);
-    if (lane == __ffs(peers) - 1) atomicAdd(&H[bin], (uint32_t)__popc(peers));
-  }
-}
-
 // Four consecutive scores starting at p[tl] (tl multiple of 4); entries at or
 // past n are marked invalid.
 __device__ __forceinline__ void load4(const float* p, int tl, int n, float (&v)[4], bool (&ok)[4]) {
@@ -112,15 +133,15 @@ __device__ __forceinline__ void load4(const float* p, int tl, int n, float (&v)[
   }
 }
 
-// RoPE angle of FC i at position m: theta_i = B^(-2i/d), a = m theta_i formed
-// and reduced modulo 2 pi in fp64; cos/sin of the reduced angle in fp32.
-__device__ __forceinline__ float2 rope_cos_sin(double base, int i, int d, int m) {
-  const double th = exp2(-(2.0 * i / d) * log2(base));
-  const double a = (double)m * th;
-  const double k = rint(a * 0.15915494309189535);  // a / (2 pi)
-  const double r = fma(-k, 6.283185307179586, a);
+// cos / sin of the RoPE angle m * theta_i.  `turns` = theta_i / (2 pi) * 2^64;
+// the wrapped 64-bit product is the angle in turns, exact up to the rounding
+// of `turns`.  Its top 32 bits as a signed fraction x in [-1, 1) give the
+// angle pi * x, evaluated with sincospif.
+__device__ __forceinline__ float2 rope_cos_sin(unsigned long long turns, int m) {
+  const unsigned long long t = (unsigned long long)(long long)m * turns;
+  const float x = (float)(int)(t >> 32) * 4.656612873077393e-10f;  // 2^-31
   float s, c;
-  sincosf((float)r, &s, &c);
+  sincospif(x, &s, &c);
   return make_float2(c, s);
 }
 
@@ -146,12 +167,67 @@ __device__ __forceinline__ void load_row(const unsigned char* p, float (&x)[EPL]
   }
 }
 
-template <typename T, int D>
+// Radix digits of the keys: 12, 10, 10 bits, from the top.
+__device__ __forceinline__ int dig_bits(int p) { return p == 0 ? 12 : 10; }
+__device__ __forceinline__ int dig_shift(int p) { return p == 0 ? 20 : (p == 1 ? 10 : 0); }
+__device__ __forceinline__ int lead_off(int p) { return p == 0 ? 0 : (p == 1 ? 4096 : 5120); }
+
+// Finds the digit holding the k_rem-th largest key in a histogram of NB bins
+// in this CTA's shared memory.  Thread t owns the NB/NT consecutive bins
+// counted from the top.  Writes dstar / cnt_gt (keys in larger digits) /
+// bucket into `ms`.  Every thread must call it.
+template <int NB>
+__device__ __forceinline__ void radix_find(const uint32_t* hist, int k_rem, Misc* ms) {
+  constexpr int M = NB / NT;
+  static_assert(M >= 1 && NB % NT == 0, "bins per thread");
+  const int tid = threadIdx.x;
+  const int base = NB - (tid + 1) * M;
+  uint32_t c[M];
+  if constexpr (M % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < M / 4; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(hist + base)[q];
+      c[4 * q] = v.x; c[4 * q + 1] = v.y; c[4 * q + 2] = v.z; c[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < M; ++i) c[i] = hist[base + i];
+  }
+  int tsum = 0;
+#pragma unroll
+  for (int i = 0; i < M; ++i) tsum += (int)c[i];
+  int total;
+  int run = block_excl_scan(tsum, ms->scan, total);
+#pragma unroll
+  for (int i = M - 1; i >= 0; --i) {
+    const int ci = (int)c[i];
+    if (run < k_rem && k_rem <= run + ci) {
+      ms->dstar = base + i;
+      ms->cnt_gt = run;
+      ms->bucket = ci;
+    }
+    run += ci;
+  }
+  __syncthreads();
+}
+
+// KIND names the launch in profiles and lets the compiler drop unused phases:
+// KIND_STEP = fused decode step, KIND_DENSE = dense attention, KIND_STAGE =
+// the separate stage entry points (phases chosen by p.flags).
+enum : int { KIND_STEP = 0, KIND_DENSE = 1, KIND_STAGE = 2 };
+
+__host__ __device__ constexpr int kind_flags(int kind, int flags) {
+  return kind == KIND_STEP ? (flags & (F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT))
+         : kind == KIND_DENSE ? F_DENSE
+                              : flags;
+}
+
+template <typename T, int D, int KIND>
 __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int ES = sizeof(T);
   constexpr int EPL = D / 32;           // FAC elements per lane
-  constexpr int TPV = 16 / (2 * ES);    // k_dom tokens per 16 bytes
+  constexpr int KB = KDOM_BLOCK;        // k_dom tokens per block
   constexpr int ROWB = D * ES;          // bytes of one K/V row
   constexpr int ROWS = ROWB + 16;       // padded row stride in shared memory
   constexpr int CPR = ROWB / 16;        // 16-byte chunks per row
@@ -162,91 +238,117 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   const int unit = blockIdx.y;
   const int b = unit / p.Hkv, h = unit - (unit / p.Hkv) * p.Hkv;
   const int G = p.G;
-  const int flags = p.flags;
+  const int flags = kind_flags(KIND, p.flags);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   Misc* ms = reinterpret_cast<Misc*>(smem + p.off_misc);
   float* qrot = reinterpret_cast<float*>(smem + p.off_qrot);
   float* qbar = reinterpret_cast<float*>(smem + p.off_qbar);
   float* stile = reinterpret_cast<float*>(smem + p.off_stile);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + p.off_hist);
+  uint32_t* hloc = reinterpret_cast<uint32_t*>(smem + p.off_hloc);
+  uint32_t* hlead = reinterpret_cast<uint32_t*>(smem + p.off_hlead);
   float* sc_s = reinterpret_cast<float*>(smem + p.off_sc);
   int* idx_s = reinterpret_cast<int*>(smem + p.off_idx);
+  uint2* own2 = reinterpret_cast<uint2*>(smem + p.off_own);
   float* part = reinterpret_cast<float*>(smem + p.off_part);
   unsigned char* big = smem + p.off_big;
 
+  // Shared-memory set-up first: the release below then has no outstanding
+  // global loads to wait for.
+  const int nfc = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
+  if (tid == 0) {
+    for (int s = 0; s < ns; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  if (flags & F_SELECT) {
+    uint4* z = reinterpret_cast<uint4*>(hloc);
+    for (int i = tid; i < HLOC_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    z = reinterpret_cast<uint4*>(hlead);
+    for (int i = tid; i < HLEAD_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // release: the zeroed histograms are visible before any CTA adds into them;
+  // completed by cluster_wait() before the first DSMEM access
+  cluster_arrive();
+  __syncthreads();
+
+  // every small input is loaded up front so the loads overlap each other
+  // (and go out before the bulk TIP traffic)
   bool bad = false;
   int len = p.seq_lens[b];
+  const int m_pos = (flags & F_ROPE) ? p.pos[b] : 0;
+  const int dom_i = (tid < p.n_tip && (flags & F_TIP)) ? p.dom_fc[h * p.n_tip + tid] : 0;
+  constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;  // query pairs per thread
+  float2 qv[QPAIRS];
+#pragma unroll
+  for (int k = 0; k < QPAIRS; ++k) {
+    const int x = tid + k * NT;
+    qv[k] = make_float2(0.f, 0.f);
+    if (x < G * (D / 2)) {
+      const int g = x / (D / 2), i = x - g * (D / 2);
+      const size_t off = ((size_t)b * p.Hq + (size_t)h * G + g) * D + 2 * i;
+      if (flags & F_ROPE) {
+        const T* qg = reinterpret_cast<const T*>(p.q) + off;
+        qv[k] = make_float2(to_f32<T>(qg[0]), to_f32<T>(qg[1]));
+      } else if (flags & (F_TIP | F_FAC | F_DENSE)) {
+        qv[k] = *reinterpret_cast<const float2*>(p.q_rot + off);
+      }
+    }
+  }
   if (len < 0 || len > p.T_max) {
     bad = true;
     len = min(max(len, 0), p.T_max);
   }
+
   const int k_eff = min(p.budget, len);
   const bool sel_flag = (flags & F_SELECT) != 0;
   const bool need_select = sel_flag && len > p.budget;
   const bool do_tip = (flags & F_TIP) && (!sel_flag || need_select);
   const bool read_sc = (flags & F_SC_IN) && need_select;
 
-  // contiguous token range of this CTA (start aligned to 16 tokens)
-  const int chunk = ((len + C - 1) / C + 15) & ~15;
+  // contiguous token range of this CTA (start aligned to a k_dom block)
+  const int chunk = ((len + C - 1) / C + KB - 1) / KB * KB;
   const int t0 = min(len, (int)crank * chunk);
   const int t1 = min(len, t0 + chunk);
   const int nloc = t1 - t0;
 
-  const int nfc = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
-  if (tid == 0) {
-    for (int s = 0; s < ns; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
-    ms->failed = 0;
-  }
-  for (int i = tid; i < 512; i += NT) hist[i] = 0u;
-  cluster_arrive_relaxed();  // completed by cluster_wait() before any DSMEM access
-  __syncthreads();
-
   // ---------------------------------------------------------------- TIP loads
   const int ntiles = do_tip ? (nloc + tt - 1) / tt : 0;
-  const uint32_t fc_bytes_tile = (uint32_t)tt * 2 * ES;
-  const uint32_t stage_bytes = (uint32_t)nfc * fc_bytes_tile;
+  // k_dom is [.., T_max/KB, n_tip, KB, 2]: a tile of whole blocks is one
+  // contiguous range, moved by a single bulk copy
+  const uint32_t fc_row_bytes = (uint32_t)KB * 2 * ES;
+  const uint32_t blk_bytes = (uint32_t)nfc * fc_row_bytes;
+  const uint32_t stage_bytes = (uint32_t)(tt / KB) * blk_bytes;
   const T* kd_unit = reinterpret_cast<const T*>(p.k_dom) + (size_t)unit * nfc * p.T_max * 2;
-  auto tip_issue = [&](int it) {  // warp 0
+  auto tip_issue = [&](int it) {  // one thread
     const int s = it % ns;
     const int tau0 = t0 + it * tt;
-    const int ntok = min(tt, t1 - tau0);
-    const int ntokp = (ntok + TPV - 1) / TPV * TPV;
-    const uint32_t bytes = (uint32_t)ntokp * 2 * ES;
+    const int nblk = (min(tt, t1 - tau0) + KB - 1) / KB;
+    const uint32_t bytes = (uint32_t)nblk * blk_bytes;
     const uint32_t bar = smem_u32(&bars[s]);
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes * nfc);
-    __syncwarp();
-    for (int j = lane; j < nfc; j += 32)
-      bulk_g2s(smem_u32(big + s * stage_bytes + j * fc_bytes_tile),
-               kd_unit + ((size_t)j * p.T_max + tau0) * 2, bytes, bar);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(big + s * stage_bytes), kd_unit + (size_t)(tau0 / KB) * nfc * KB * 2, bytes, bar);
   };
-  if (warp == 0)
+  if (tid == 0)
     for (int it = 0; it < min(ns, ntiles); ++it) tip_issue(it);
 
   // ------------------------------------------------------------ query prep
-  if (flags & F_ROPE) {
-    float2* cs = reinterpret_cast<float2*>(stile);
-    const int m = p.pos[b];
-    for (int i = tid; i < D / 2; i += NT) cs[i] = rope_cos_sin(p.rope_theta, i, D, m);
-    __syncthreads();
-    const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D;
-    for (int x = tid; x < G * (D / 2); x += NT) {
+#pragma unroll
+  for (int k = 0; k < QPAIRS; ++k) {
+    const int x = tid + k * NT;
+    if (x < G * (D / 2)) {
       const int g = x / (D / 2), i = x - g * (D / 2);
-      const float x0 = to_f32<T>(qg[g * D + 2 * i]);
-      const float x1 = to_f32<T>(qg[g * D + 2 * i + 1]);
-      const float2 c = cs[i];
-      qrot[g * D + 2 * i] = x0 * c.x - x1 * c.y;
-      qrot[g * D + 2 * i + 1] = x0 * c.y + x1 * c.x;
+      float2 r = qv[k];
+      if (flags & F_ROPE) {
+        const float2 c = rope_cos_sin(p.rope_turns[i], m_pos);
+        r = make_float2(qv[k].x * c.x - qv[k].y * c.y, qv[k].x * c.y + qv[k].y * c.x);
+      }
+      *reinterpret_cast<float2*>(&qrot[g * D + 2 * i]) = r;
     }
-  } else if (flags & (F_TIP | F_FAC | F_DENSE)) {
-    const float* qg = p.q_rot + ((size_t)b * p.Hq + (size_t)h * G) * D;
-    for (int x = tid; x < G * D; x += NT) qrot[x] = qg[x];
   }
   __syncthreads();
   if (do_tip) {
     for (int j = tid; j < nfc; j += NT) {
-      int i = p.dom_fc[h * nfc + j];
+      int i = (j == tid) ? dom_i : p.dom_fc[h * nfc + j];
       if (i < 0 || i >= D / 2) {
         bad = true;
         i = min(max(i, 0), D / 2 - 1);
@@ -273,41 +375,72 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const int tau_base = it * tt;
     const int ntok = min(tt, nloc - tau_base);
     const unsigned char* st = big + s * stage_bytes;
-    for (int gb = warp * 32; gb * 4 < ntok; gb += NT) {  // warp-uniform
-      const int tl = (gb + lane) * 4;
-      const bool act = tl < ntok;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (act) {
-        for (int j = 0; j < nfc; ++j) {
-          const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
-          const unsigned char* row = st + j * fc_bytes_tile + tl * 2 * ES;
-          if constexpr (ES == 2) {
-            const uint4 w = *reinterpret_cast<const uint4*>(row);
-            acc[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), acc[0]));
-            acc[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), acc[1]));
-            acc[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), acc[2]));
-            acc[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), acc[3]));
-          } else {
-            const float4 w0 = *reinterpret_cast<const float4*>(row);
-            const float4 w1 = *reinterpret_cast<const float4*>(row + 16);
-            acc[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, acc[0]));
-            acc[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, acc[1]));
-            acc[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, acc[2]));
-            acc[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, acc[3]));
-          }
-        }
-        const int tloc = tau_base + tl;
-        if (tl + 4 <= ntok) {
-          *reinterpret_cast<float4*>(scw + tloc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    for (int tl = tid * 4; tl < ntok; tl += NT * 4) {
+      // two independent accumulator sets (even / odd FC) for latency hiding
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      const unsigned char* row = st + (tl / KB) * blk_bytes + (tl % KB) * 2 * ES;
+      int j = 0;
+#pragma unroll 4
+      for (; j + 2 <= nfc; j += 2) {
+        const float4 qq = *reinterpret_cast<const float4*>(&qbar[2 * j]);
+        if constexpr (ES == 2) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
+          const uint4 u = *reinterpret_cast<const uint4*>(row + (j + 1) * fc_row_bytes);
+          a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
+          a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
+          a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
+          a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
+          a1[0] = fmaf(qq.z, bf16_lo(u.x), fmaf(qq.w, bf16_hi(u.x), a1[0]));
+          a1[1] = fmaf(qq.z, bf16_lo(u.y), fmaf(qq.w, bf16_hi(u.y), a1[1]));
+          a1[2] = fmaf(qq.z, bf16_lo(u.z), fmaf(qq.w, bf16_hi(u.z), a1[2]));
+          a1[3] = fmaf(qq.z, bf16_lo(u.w), fmaf(qq.w, bf16_hi(u.w), a1[3]));
         } else {
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (tl + t < ntok) scw[tloc + t] = acc[t];
+          const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
+          const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
+          const float4 u0 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes);
+          const float4 u1 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes + 16);
+          a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
+          a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
+          a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
+          a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
+          a1[0] = fmaf(qq.z, u0.x, fmaf(qq.w, u0.y, a1[0]));
+          a1[1] = fmaf(qq.z, u0.z, fmaf(qq.w, u0.w, a1[1]));
+          a1[2] = fmaf(qq.z, u1.x, fmaf(qq.w, u1.y, a1[2]));
+          a1[3] = fmaf(qq.z, u1.z, fmaf(qq.w, u1.w, a1[3]));
         }
+      }
+      if (j < nfc) {
+        const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
+        if constexpr (ES == 2) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
+          a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
+          a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
+          a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
+          a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
+        } else {
+          const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
+          const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
+          a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
+          a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
+          a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
+          a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
+        }
+      }
+      float acc[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) acc[t] = a0[t] + a1[t];
+      const int tloc = tau_base + tl;
+      if (tl + 4 <= ntok) {
+        *reinterpret_cast<float4*>(scw + tloc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (tl + t < ntok) scw[tloc + t] = acc[t];
       }
       if (need_select) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) hist_add(hist, score_key(acc[t]) >> 24, act && (tl + t < ntok), lane);
+        for (int t = 0; t < 4; ++t)
+          if (tl + t < ntok) atomicAdd(&hloc[score_key(acc[t]) >> 20], 1u);
       }
     }
     const int anyfail = __syncthreads_or(fail);
@@ -321,288 +454,333 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       __syncthreads();
       break;
     }
-    if (warp == 0 && it + ns < ntiles) {
+    if (tid == 0 && it + ns < ntiles) {
       fence_proxy_async();
       tip_issue(it + ns);
     }
   }
 
+  // ----------------------------------------------------- FAC row source
+  // The attention rows of this CTA: fr_n rows, either contiguous tokens
+  // fr_r0.. or a token list -- fr_list (int) or fr_pairs ((key, token)
+  // pairs); a set high bit in a list entry masks the row.  K/V rows are
+  // staged with cp.async in a FAC_STAGES-deep ring at the start of `big`
+  // (the TIP ring is no longer needed once they are issued).
+  unsigned char* fac_stage = big;
+  constexpr uint32_t FAC_STAGE_B = 2u * RT * ROWS;
+  const int* fr_list = nullptr;
+  const uint2* fr_pairs = nullptr;
+  int fr_n = 0, fr_r0 = 0;
+  bool fr_contig = true, fac_started = false;
+  const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * D;
+  const T* Vb = reinterpret_cast<const T*>(p.v_cache) + (size_t)unit * p.T_max * D;
+  auto row_token = [&](int i) -> int {
+    if (fr_contig) return fr_r0 + i;
+    if (fr_pairs) return (int)(fr_pairs[i].y & 0x7FFFFFFFu);
+    return fr_list[i] & 0x7FFFFFFF;
+  };
+  auto row_masked = [&](int i) -> bool {
+    if (fr_contig) return false;
+    if (fr_pairs) return (fr_pairs[i].y >> 31) != 0u;
+    return fr_list[i] < 0;
+  };
+  auto fac_issue = [&](int t) {
+    const int ntile = (fr_n + RT - 1) / RT;
+    if (t < ntile) {
+      const int s = t % FAC_STAGES;
+      const int rows_t = min(RT, fr_n - t * RT);
+      const uint32_t st0 = smem_u32(fac_stage) + s * FAC_STAGE_B;
+      for (int c = tid; c < 2 * rows_t * CPR; c += NT) {
+        const int which = c / (rows_t * CPR);
+        const int rc = c - which * rows_t * CPR;
+        const int rr = rc / CPR;
+        const int ch = rc - rr * CPR;
+        const int tau = row_token(t * RT + rr);
+        const T* src = (which ? Vb : Kb) + (size_t)tau * D + ch * (16 / ES);
+        cp_async16(st0 + which * RT * ROWS + rr * ROWS + ch * 16, src);
+      }
+    }
+    cp_async_commit();
+  };
+  auto fac_start = [&]() {
+#pragma unroll
+    for (int s = 0; s < FAC_STAGES - 1; ++s) fac_issue(s);
+    fac_started = true;
+  };
+
   // ---------------------------------------------------------------- top-k
+  // Cluster radix select with digits of 12, 10 and 10 bits.  After the first
+  // digit every CTA lists its own candidates (keys at or above the threshold
+  // bucket) in token order and starts gathering their K/V rows; the later
+  // digits are resolved on those short lists.  The selection ends either with
+  // an exactly filled bucket (every key >= a bound) or, after all 32 bits,
+  // with ties on one key K*, shared out in token order.
+  int own_n = 0;        // entries of own2
+  bool own_list = false;  // own2 lists every candidate of this CTA (else: scan the scores)
   if (need_select) {
     const float* scr = read_sc ? (p.scores_in + (size_t)unit * p.T_max + t0) : scw;
     if (read_sc) {
-      for (int c0 = 0; c0 < nloc; c0 += NT * 4) {
+      for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
         float v[4];
         bool ok[4];
-        load4(scr, c0 + 4 * tid, nloc, v, ok);
+        load4(scr, tl, nloc, v, ok);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) hist_add(hist, score_key(v[t]) >> 24, ok[t], lane);
+        for (int t = 0; t < 4; ++t)
+          if (ok[t]) atomicAdd(&hloc[score_key(v[t]) >> 20], 1u);
       }
     }
-    if (tid < C_MAX) ms->aboveR[tid] = 0;
     __syncthreads();
 
-    int k_rem = k_eff, above_total = 0, mode = MODE_NONE, shift = 24, last_pass = 0;
+    const uint32_t hglob_l = smem_u32(hlead);
+    int k_rem = k_eff, mode = MODE_NONE, shift = 20;
     uint32_t prefix = 0u;
-    for (int pass = 0; pass < 4; ++pass) {
-      shift = 24 - 8 * pass;
-      last_pass = pass;
-      uint32_t* H = hist + (pass & 1) * 256;
-      if (pass > 0) {
-        // H was last read by the other CTAs two passes ago, before the
-        // previous cluster barrier.
-        for (int i = tid; i < 256; i += NT) H[i] = 0u;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int bits = dig_bits(pass);
+      const int nb = 1 << bits;
+      shift = dig_shift(pass);
+      int lo_bin = 0;
+      if (pass == 0) {
+        // Bins below this CTA's own k-th largest key cannot hold the global
+        // threshold (the global k-th key is at least every CTA's local k-th
+        // key), so only the bins from there up are sent.
+        if (nloc >= k_eff) {
+          radix_find<4096>(hloc, k_eff, ms);
+          lo_bin = ms->dstar;
+        }
+      } else {
+        // local histogram of the keys inside the current prefix
+        for (int i = tid; i < nb; i += NT) hloc[i] = 0u;
         __syncthreads();
-        for (int c0 = 0; c0 < nloc; c0 += NT * 4) {
-          float v[4];
-          bool ok[4];
-          load4(scr, c0 + 4 * tid, nloc, v, ok);
+        if (own_list) {
+          for (int e = tid; e < own_n; e += NT) {
+            const uint32_t key = own2[e].x;
+            if ((key >> (shift + bits)) == prefix) atomicAdd(&hloc[(key >> shift) & (nb - 1)], 1u);
+          }
+        } else {
+          for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
+            float v[4];
+            bool ok[4];
+            load4(scr, tl, nloc, v, ok);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t key = score_key(v[t]);
-            hist_add(H, (key >> shift) & 255u, ok[t] && (key >> (shift + 8)) == prefix, lane);
+            for (int t = 0; t < 4; ++t) {
+              const uint32_t key = score_key(v[t]);
+              if (ok[t] && (key >> (shift + bits)) == prefix) atomicAdd(&hloc[(key >> shift) & (nb - 1)], 1u);
+            }
+          }
+        }
+        __syncthreads();
+      }
+      // add the non-zero bins into every CTA's copy of the cluster totals
+      const uint32_t dst = hglob_l + lead_off(pass) * 4;
+      for (int i = lo_bin + tid; i < nb; i += NT) {
+        const uint32_t c = hloc[i];
+        if (c)
+          for (int r = 0; r < C; ++r) dsmem_red_add_u32(dsmem_map(dst + i * 4, (uint32_t)r), c);
+      }
+      cluster_sync();
+      if (pass == 0) radix_find<4096>(hlead + lead_off(0), k_rem, ms);
+      else radix_find<1024>(hlead + lead_off(pass), k_rem, ms);
+      const int cnt_gt = ms->cnt_gt, bucket = ms->bucket;
+      k_rem -= cnt_gt;
+      prefix = (prefix << bits) | (uint32_t)ms->dstar;
+      if (bucket == k_rem) mode = MODE_FILL;
+      else if (pass == 2) mode = MODE_TIES;
+      __syncthreads();
+
+      if (pass == 0) {
+        // this CTA's candidates (top 12 bits >= prefix), token order, into
+        // own2 when they fit; each thread takes a contiguous run of tokens
+        // (odd length: conflict-free strides) and one block scan places them
+        const int seg = ((nloc + NT - 1) / NT) | 1;
+        const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
+        int cnt = 0;
+        for (int i = s0; i < s1; ++i) cnt += (score_key(scr[i]) >> 20) >= prefix;
+        int total;
+        const int before = block_excl_scan(cnt, ms->scan, total);
+        own_list = total <= p.cand_cap;
+        if (own_list) {
+          int pos = before;
+          for (int i = s0; i < s1 && pos < before + cnt; ++i) {
+            const uint32_t key = score_key(scr[i]);
+            if ((key >> 20) >= prefix) own2[pos++] = make_uint2(key, (uint32_t)(t0 + i));
+          }
+          own_n = total;
+          __syncthreads();
+          if (flags & F_FAC) {
+            fr_pairs = own2;
+            fr_n = own_n;
+            fr_contig = false;
+            fac_start();  // gather now; the later digits only mask rows out
           }
         }
       }
-      __syncthreads();
-      cluster_sync();
-      // thread tid holds digit 255 - tid: an exclusive scan counts larger digits
-      const int bin = 255 - tid;
-      const uint32_t la = smem_u32(&H[bin]);
-      uint32_t v[C_MAX];
-      uint32_t tot = 0u;
-#pragma unroll
-      for (int r = 0; r < C_MAX; ++r) {
-        v[r] = (r < C) ? dsmem_ld_u32(dsmem_map(la, (uint32_t)r)) : 0u;
-        tot += v[r];
-      }
-      int total;
-      const int excl = block_excl_scan((int)tot, ms->scan, total);
-      if (excl < k_rem && k_rem <= excl + (int)tot) {
-        ms->dstar = bin;
-        ms->cnt_gt = excl;
-        ms->bucket = (int)tot;
-#pragma unroll
-        for (int r = 0; r < C_MAX; ++r)
-          if (r < C) ms->bucketR[r] = (int)v[r];
-      }
-      __syncthreads();
-      const int dstar = ms->dstar, cnt_gt = ms->cnt_gt, bucket = ms->bucket;
-      const bool above = bin > dstar;
-#pragma unroll
-      for (int r = 0; r < C_MAX; ++r) {
-        const unsigned x = __reduce_add_sync(0xffffffffu, above ? v[r] : 0u);
-        if (lane == 0) ms->wsum[warp][r] = (int)x;
-      }
-      __syncthreads();
-      if (tid < C) {
-        int s = 0;
-        for (int w = 0; w < NW; ++w) s += ms->wsum[w][tid];
-        ms->aboveR[tid] += s;
-      }
-      k_rem -= cnt_gt;
-      above_total += cnt_gt;
-      prefix = (prefix << 8) | (uint32_t)dstar;
-      if (bucket == k_rem) mode = MODE_FILL;
-      else if (pass == 3) mode = MODE_TIES;
-      else if (above_total + bucket <= p.cand_cap) mode = MODE_CAND;
-      __syncthreads();
       if (mode != MODE_NONE) break;
     }
 
-    // per-CTA candidate counts and offsets (identical in every CTA)
-    if (tid == 0) {
-      int run = 0, ties_before = 0;
-      for (int r = 0; r < C; ++r) {
-        int need = ms->bucketR[r];
-        if (mode == MODE_TIES) {
-          need = min(max(k_rem - ties_before, 0), ms->bucketR[r]);
-          ties_before += ms->bucketR[r];
+    // TIES: the threshold key K* (= prefix) has more copies than needed.  The
+    // CTAs exchange their tie counts; CTA r keeps the first ties in token
+    // order after those of CTAs 0..r-1.
+    int my_need = 0;
+    if (mode == MODE_TIES) {
+      int ties = 0;
+      if (own_list) {
+        for (int e = tid; e < own_n; e += NT) ties += own2[e].x == prefix;
+      } else {
+        for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
+          float v[4];
+          bool ok[4];
+          load4(scr, tl, nloc, v, ok);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) ties += (ok[t] && score_key(v[t]) == prefix);
         }
-        ms->needR[r] = need;
+      }
+      int tot;
+      block_excl_scan(ties, ms->scan, tot);
+      if (tid == 0) ms->my_ties = tot;
+      cluster_sync();
+      if (tid < C) ms->tiesR[tid] = (int)dsmem_ld_u32(dsmem_map(smem_u32(&ms->my_ties), (uint32_t)tid));
+      __syncthreads();
+      int before = 0;
+      for (int r = 0; r < (int)crank; ++r) before += ms->tiesR[r];
+      my_need = min(max(k_rem - before, 0), ms->tiesR[crank]);
+    }
+
+    // Final selection of this CTA's tokens.  List mode: mask the candidates
+    // that are not selected.  Scan mode: list the selected tokens now.
+    // Either way the selected tokens, in order, also go to idx_s.
+    const bool ties_mode = mode == MODE_TIES;
+    auto selected = [&](uint32_t key, int tie_rank) -> bool {
+      if (ties_mode) return key > prefix || (key == prefix && tie_rank < my_need);
+      return (key >> shift) >= prefix;
+    };
+    if (own_list) {
+      int run_t = 0, run_s = 0;
+      for (int e0 = 0; e0 < own_n; e0 += NT) {
+        const int e = e0 + tid;
+        const bool valid = e < own_n;
+        const uint32_t key = valid ? own2[e].x : 0u;
+        const bool tie = valid && ties_mode && key == prefix;
+        int tot_t = 0;
+        const int tr = ties_mode ? run_t + block_excl_scan((int)tie, ms->scan, tot_t) : 0;
+        const bool sel = valid && selected(key, tr);
+        int tot_s;
+        const int ps = run_s + block_excl_scan((int)sel, ms->scan, tot_s);
+        if (valid && !sel) own2[e].y |= 0x80000000u;
+        if (sel && ps < p.idx_cap) idx_s[ps] = (int)own2[e].y;
+        run_t += tot_t;
+        run_s += tot_s;
+      }
+      if (tid == 0) ms->my_count = run_s;
+    } else {
+      const int seg = ((nloc + NT - 1) / NT) | 1;
+      const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
+      int ct = 0;
+      if (ties_mode)
+        for (int i = s0; i < s1; ++i) ct += score_key(scr[i]) == prefix;
+      int tot_t = 0;
+      int tr = ties_mode ? block_excl_scan(ct, ms->scan, tot_t) : 0;
+      int cs = 0;
+      {
+        int trr = tr;
+        for (int i = s0; i < s1; ++i) {
+          const uint32_t key = score_key(scr[i]);
+          cs += selected(key, trr);
+          trr += ties_mode && key == prefix;
+        }
+      }
+      int tot_s;
+      int ps = block_excl_scan(cs, ms->scan, tot_s);
+      for (int i = s0; i < s1; ++i) {
+        const uint32_t key = score_key(scr[i]);
+        if (selected(key, tr) && ps < p.cand_cap) {
+          own2[ps] = make_uint2(key, (uint32_t)(t0 + i));
+          if (ps < p.idx_cap) idx_s[ps] = t0 + i;
+          ++ps;
+        }
+        tr += ties_mode && key == prefix;
+      }
+      own_n = min(tot_s, p.cand_cap);
+      if (tid == 0) ms->my_count = own_n;
+      __syncthreads();
+      if (flags & F_FAC) {
+        fr_pairs = own2;
+        fr_n = own_n;
+        fr_contig = false;
+        fac_start();
+      }
+    }
+    __syncthreads();
+  }
+
+  // idx_out / count_out: the selected tokens of every CTA, concatenated in
+  // cluster-rank (= token) order; CTA 0 pulls them once the lists are final.
+  auto write_idx_out = [&]() {
+    if (crank != 0) return;
+    if (p.count_out && tid == 0) p.count_out[unit] = k_eff;
+    if (!p.idx_out) return;
+    int* io = p.idx_out + (size_t)unit * p.budget;
+    if (!need_select) {
+      for (int i = tid; i < p.budget; i += NT) io[i] = (i < k_eff) ? i : -1;
+      return;
+    }
+    if (tid < C) ms->cntR[tid] = (int)dsmem_ld_u32(dsmem_map(smem_u32(&ms->my_count), (uint32_t)tid));
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int r = 0; r < C; ++r) {
         ms->offR[r] = run;
-        run += ms->aboveR[r] + need;
+        run += ms->cntR[r];
       }
       ms->ncand = run;
     }
     __syncthreads();
-    const int my_off = ms->offR[crank], my_need = ms->needR[crank], ncand = ms->ncand;
-    uint32_t* ckey = reinterpret_cast<uint32_t*>(big);
-    int* ctau = reinterpret_cast<int*>(big + (size_t)p.cand_cap * 4);
-    const uint32_t ckey_l = smem_u32(ckey), ctau_l = smem_u32(ctau);
-
-    // push this CTA's candidates, in token order, to every CTA of the cluster
-    int run_s = 0, run_t = 0;
-    for (int c0 = 0; c0 < nloc; c0 += NT * 4) {
-      float v[4];
-      bool ok[4];
-      load4(scr, c0 + 4 * tid, nloc, v, ok);
-      uint32_t key[4];
-      bool strict[4], tie[4];
-      int cs_ = 0, ct_ = 0;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        key[t] = score_key(v[t]);
-        if (mode == MODE_TIES) {
-          strict[t] = ok[t] && key[t] > prefix;
-          tie[t] = ok[t] && key[t] == prefix;
-        } else {
-          strict[t] = ok[t] && (key[t] >> shift) >= prefix;
-          tie[t] = false;
-        }
-        cs_ += strict[t];
-        ct_ += tie[t];
-      }
-      int tot;
-      const int ex = block_excl_scan(cs_ | (ct_ << 16), ms->scan, tot);
-      int s_before = run_s + (ex & 0xFFFF), t_before = run_t + (ex >> 16);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const bool take = strict[t] || (tie[t] && t_before < my_need);
-        if (take) {
-          const int pos = my_off + s_before + min(t_before, my_need);
-          const uint32_t tau = (uint32_t)(t0 + c0 + 4 * tid + t);
-          for (int r = 0; r < C; ++r) {
-            dsmem_st_u32(dsmem_map(ckey_l + pos * 4, (uint32_t)r), key[t]);
-            dsmem_st_u32(dsmem_map(ctau_l + pos * 4, (uint32_t)r), tau);
-          }
-        }
-        s_before += strict[t];
-        t_before += tie[t];
-      }
-      run_s += tot & 0xFFFF;
-      run_t += tot >> 16;
+    const int total = min(ms->ncand, p.budget);
+    for (int e = tid; e < total; e += NT) {
+      int r = 0;
+      while (r + 1 < C && ms->offR[r + 1] <= e) ++r;
+      io[e] = (int)dsmem_ld_u32(dsmem_map(smem_u32(idx_s + (e - ms->offR[r])), (uint32_t)r));
     }
-    cluster_sync();
-
-    // finish the selection locally on the (identical) candidate list
-    long long kthr = -1;
-    int ties_take = 0;
-    if (mode == MODE_CAND) {
-      uint32_t pre = prefix;
-      int kr = k_rem;
-      for (int qp = last_pass + 1; qp < 4; ++qp) {
-        const int s2 = 24 - 8 * qp;
-        for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-        __syncthreads();
-        for (int e0 = 0; e0 < ncand; e0 += NT) {
-          const int e = e0 + tid;
-          const uint32_t key = (e < ncand) ? ckey[e] : 0u;
-          hist_add(hist, (key >> s2) & 255u, e < ncand && (key >> (s2 + 8)) == pre, lane);
-        }
-        __syncthreads();
-        const int bin = 255 - tid;
-        const int cnt = (int)hist[bin];
-        int total;
-        const int excl = block_excl_scan(cnt, ms->scan, total);
-        if (excl < kr && kr <= excl + cnt) {
-          ms->dstar = bin;
-          ms->cnt_gt = excl;
-          ms->bucket = cnt;
-        }
-        __syncthreads();
-        kr -= ms->cnt_gt;
-        pre = (pre << 8) | (uint32_t)ms->dstar;
-        const int bucket = ms->bucket;
-        __syncthreads();
-        if (bucket == kr) {
-          kthr = ((long long)pre << s2) - 1;
-          ties_take = 0;
-          break;
-        }
-        if (qp == 3) {
-          kthr = (long long)pre;
-          ties_take = kr;
-        }
-      }
-    }
-    int run = 0, runq = 0;
-    for (int e0 = 0; e0 < ncand; e0 += NT) {
-      const int e = e0 + tid;
-      const bool valid = e < ncand;
-      const long long key = valid ? (long long)ckey[e] : -1;
-      const bool gt = valid && key > kthr;
-      const bool eq = valid && key == kthr && ties_take > 0;
-      int tot;
-      const int ex = block_excl_scan((int)gt | ((int)eq << 16), ms->scan, tot);
-      const int tb = runq + (ex >> 16);
-      if (gt || (eq && tb < ties_take)) idx_s[run + (ex & 0xFFFF) + min(tb, ties_take)] = ctau[e];
-      run += tot & 0xFFFF;
-      runq += tot >> 16;
-    }
+    for (int i = total + tid; i < p.budget; i += NT) io[i] = -1;
     __syncthreads();
-  }
-
-  if ((flags & F_IDX_OUT) && crank == 0) {
-    if (p.idx_out) {
-      int* io = p.idx_out + (size_t)unit * p.budget;
-      for (int i = tid; i < p.budget; i += NT) io[i] = (i < k_eff) ? (need_select ? idx_s[i] : i) : -1;
-    }
-    if (p.count_out && tid == 0) p.count_out[unit] = k_eff;
-  }
+  };
 
   // ---------------------------------------------------------------- FAC
   if (flags & (F_FAC | F_DENSE)) {
-    int n_total;
-    bool contiguous;
-    int lofs = 0;
-    if (flags & F_DENSE) {
-      n_total = len;
-      contiguous = true;
-    } else if (flags & F_IDX_IN) {
-      n_total = p.count_in[unit];
-      if (n_total < 0 || n_total > k_eff) {
-        bad = true;
-        n_total = min(max(n_total, 0), k_eff);
-      }
-      contiguous = false;
-    } else if (need_select) {
-      n_total = k_eff;
-      contiguous = false;
-    } else {
-      n_total = k_eff;
-      contiguous = true;
-    }
-    const int r0 = (int)(((long long)n_total * crank) / C);
-    const int r1 = (int)(((long long)n_total * (crank + 1)) / C);
-    const int nrows = r1 - r0;
-    if (flags & F_IDX_IN) {
-      const int* gi = p.idx_in + (size_t)unit * p.budget + r0;
-      for (int i = tid; i < nrows; i += NT) {
-        int t = gi[i];
-        if (t < 0 || t >= len) {
+    if (!fac_started) {
+      int n_total;
+      if (flags & F_DENSE) {
+        n_total = len;
+        fr_contig = true;
+      } else if (flags & F_IDX_IN) {
+        n_total = p.count_in[unit];
+        if (n_total < 0 || n_total > k_eff) {
           bad = true;
-          t = min(max(t, 0), len - 1);
+          n_total = min(max(n_total, 0), k_eff);
         }
-        idx_s[i] = t;
+        fr_contig = false;
+      } else {
+        n_total = k_eff;  // every cached token is selected
+        fr_contig = true;
       }
-      __syncthreads();
-    } else if (!contiguous) {
-      lofs = r0;
-    }
-
-    const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * D;
-    const T* Vb = reinterpret_cast<const T*>(p.v_cache) + (size_t)unit * p.T_max * D;
-    const int ntile = (nrows + RT - 1) / RT;
-    constexpr uint32_t STAGE_B = 2u * RT * ROWS;
-    const uint32_t fac_l = smem_u32(big);
-    auto fac_issue = [&](int t) {
-      if (t < ntile) {
-        const int s = t % FAC_STAGES;
-        for (int c = tid; c < 2 * RT * CPR; c += NT) {
-          const int which = c / (RT * CPR);
-          const int rr = (c / CPR) % RT;
-          const int ch = c % CPR;
-          const int i = t * RT + rr;
-          if (i < nrows) {
-            const int tau = contiguous ? (r0 + i) : idx_s[lofs + i];
-            const T* src = (which ? Vb : Kb) + (size_t)tau * D + ch * (16 / ES);
-            cp_async16(fac_l + s * STAGE_B + which * RT * ROWS + rr * ROWS + ch * 16, src);
+      const int r0 = (n_total * (int)crank) / C;
+      const int r1 = (n_total * ((int)crank + 1)) / C;
+      fr_n = r1 - r0;
+      fr_r0 = r0;
+      if (flags & F_IDX_IN) {
+        const int* gi = p.idx_in + (size_t)unit * p.budget + r0;
+        for (int i = tid; i < fr_n; i += NT) {
+          int t = gi[i];
+          if (t < 0 || t >= len) {
+            bad = true;
+            t = min(max(t, 0), len - 1);
           }
+          idx_s[i] = t;
         }
+        fr_list = idx_s;
+        __syncthreads();
       }
-      cp_async_commit();
-    };
+      fac_start();
+    }
 
     const float qs = 1.4426950408889634f * rsqrtf((float)D);
     float qreg[G_MAX][EPL];
@@ -618,29 +796,29 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o_run[e] = 0.f;
 
-#pragma unroll
-    for (int s = 0; s < FAC_STAGES - 1; ++s) fac_issue(s);
+    const int ntile = (fr_n + RT - 1) / RT;
     for (int t = 0; t < ntile; ++t) {
       cp_async_wait<FAC_STAGES - 2>();
       __syncthreads();
       fac_issue(t + FAC_STAGES - 1);
       const int s = t % FAC_STAGES;
-      const unsigned char* Ks = big + s * STAGE_B;
+      const unsigned char* Ks = fac_stage + s * FAC_STAGE_B;
       const unsigned char* Vs = Ks + RT * ROWS;
-      const int rows_t = min(RT, nrows - t * RT);
+      const int rows_t = min(RT, fr_n - t * RT);
       for (int rr = warp; rr < rows_t; rr += NW) {
         float kv[EPL];
         load_row<T, EPL>(Ks + rr * ROWS + lane * EPL * ES, kv);
+        float a[G_MAX];
 #pragma unroll
         for (int g = 0; g < G_MAX; ++g) {
-          if (g < G) {
-            float a = 0.f;
+          a[g] = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) a = fmaf(qreg[g][e], kv[e], a);
-            a = warp_sum(a);
-            if (lane == g) stile[g * RT + rr] = a;
-          }
+          for (int e = 0; e < EPL; ++e) a[g] = fmaf(qreg[g][e], kv[e], a[g]);
         }
+        float v = warp_sum8(a, lane);
+        if (row_masked(t * RT + rr)) v = -CUDART_INF_F;
+        const int g = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+        if ((lane & 3) == 0 && g < G) stile[g * RT + rr] = v;
       }
       __syncthreads();
       if (pv_warp) {
@@ -648,27 +826,33 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         if (nr > 0) {
           const float sv = (lane < nr) ? stile[my_g * RT + my_part + lane * nparts] : -CUDART_INF_F;
           const float m_new = fmaxf(m_run, warp_max(sv));
-          const float scale = exp2f(m_run - m_new);
-          const float pe = (lane < nr) ? exp2f(sv - m_new) : 0.f;
-          l_run = l_run * scale + warp_sum(pe);
+          if (m_new != -CUDART_INF_F) {  // every row of this part may be masked
+            const float scale = exp2f(m_run - m_new);
+            const float pe = (lane < nr) ? exp2f(sv - m_new) : 0.f;
+            l_run = l_run * scale + warp_sum(pe);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o_run[e] *= scale;
-          for (int i = 0; i < nr; ++i) {
-            const float pi = __shfl_sync(0xffffffffu, pe, i);
-            float vv[EPL];
-            load_row<T, EPL>(Vs + (my_part + i * nparts) * ROWS + lane * EPL * ES, vv);
+            for (int e = 0; e < EPL; ++e) o_run[e] *= scale;
+            for (int i = 0; i < nr; ++i) {
+              const float pi = __shfl_sync(0xffffffffu, pe, i);
+              if (pi != 0.f) {
+                float vv[EPL];
+                load_row<T, EPL>(Vs + (my_part + i * nparts) * ROWS + lane * EPL * ES, vv);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o_run[e] = fmaf(pi, vv[e], o_run[e]);
+                for (int e = 0; e < EPL; ++e) o_run[e] = fmaf(pi, vv[e], o_run[e]);
+              }
+            }
+            m_run = m_new;
           }
-          m_run = m_new;
         }
       }
     }
     cp_async_wait<0>();
     __syncthreads();
 
-    // merge the row-parts of each head, then push the CTA partial
-    float* mst = reinterpret_cast<float*>(big);
+    // merge the row-parts of each head into this CTA's partial record
+    // part[g] = (o[0..D), m, l) with m in log2 units; other CTAs pull it
+    constexpr int PSTRIDE = D + 4;
+    float* mst = reinterpret_cast<float*>(fac_stage);
     if (pv_warp) {
       float* dst = mst + (my_g * nparts + my_part) * (D + 2);
 #pragma unroll
@@ -692,85 +876,144 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         }
         val = acc;
       }
-      const uint32_t dst = smem_u32(part + ((g / C) * C + (int)crank) * (D + 2) + e);
-      dsmem_st_f32(dsmem_map(dst, (uint32_t)(g % C)), val);
+      part[g * PSTRIDE + e] = val;
     }
     cluster_sync();
-    for (int x = tid; x < p.hpc * D; x += NT) {
-      const int hs = x / D, e = x - hs * D;
-      const int g = hs * C + (int)crank;
-      if (g < G) {
-        const float* base = part + hs * C * (D + 2);
-        float M = -CUDART_INF_F;
-        for (int r = 0; r < C; ++r) M = fmaxf(M, base[r * (D + 2) + D]);
-        float L = 0.f, O = 0.f;
-        if (M != -CUDART_INF_F) {
-          for (int r = 0; r < C; ++r) {
-            const float* sp = base + r * (D + 2);
-            if (sp[D] != -CUDART_INF_F) {
-              const float w = exp2f(sp[D] - M);
-              L += w * sp[D + 1];
-              O += w * sp[e];
-            }
-          }
-        }
-        p.out[((size_t)b * p.Hq + (size_t)h * G + g) * D + e] = (L > 0.f) ? O / L : 0.f;
-      }
+
+    if (flags & F_IDX_OUT) write_idx_out();
+
+    // combine: the G*D outputs are split into C contiguous slices of
+    // 4-element groups; CTA r pulls every CTA's partial for its slice
+    const uint32_t part_l = smem_u32(part);
+    const int ngrp = G * (D / 4);
+    const int q0 = (ngrp * (int)crank) / C, q1 = (ngrp * ((int)crank + 1)) / C;
+    const int g_lo = q0 / (D / 4), g_hi = q1 > q0 ? (q1 - 1) / (D / 4) : g_lo - 1;
+    // (m, l) of every CTA for the heads in the slice -> stile[(g - g_lo) * 2 * C_MAX + ...]
+    for (int x = tid; x < (g_hi - g_lo + 1) * C; x += NT) {
+      const int gg = x / C, r = x - gg * C;
+      const uint32_t a = dsmem_map(part_l + ((g_lo + gg) * PSTRIDE + D) * 4, (uint32_t)r);
+      const uint2 ml = dsmem_ld_v2(a);
+      stile[gg * 2 * C_MAX + r] = __uint_as_float(ml.x);
+      stile[gg * 2 * C_MAX + C_MAX + r] = __uint_as_float(ml.y);
     }
+    __syncthreads();
+    for (int q = q0 + tid; q < q1; q += NT) {
+      const int g = q / (D / 4), e4 = q - g * (D / 4);
+      const float* ml = stile + (g - g_lo) * 2 * C_MAX;
+      float M = -CUDART_INF_F;
+      for (int r = 0; r < C; ++r) M = fmaxf(M, ml[r]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -CUDART_INF_F) {
+        for (int r = 0; r < C; ++r) {
+          if (ml[r] == -CUDART_INF_F) continue;
+          const float w = exp2f(ml[r] - M);
+          L += w * ml[C_MAX + r];
+          const uint4 v = dsmem_ld_v4(dsmem_map(part_l + (g * PSTRIDE + e4 * 4) * 4, (uint32_t)r));
+          acc.x = fmaf(w, __uint_as_float(v.x), acc.x);
+          acc.y = fmaf(w, __uint_as_float(v.y), acc.y);
+          acc.z = fmaf(w, __uint_as_float(v.z), acc.z);
+          acc.w = fmaf(w, __uint_as_float(v.w), acc.w);
+        }
+      }
+      if (L > 0.f) {
+        const float inv = 1.f / L;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+      }
+      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G + g) * D + e4 * 4) = acc;
+    }
+    cluster_sync();  // the partial records stay readable until every CTA is done
+  } else if (need_select) {
+    cluster_sync();  // every CTA's list is final
+    if (flags & F_IDX_OUT) write_idx_out();
+    cluster_sync();  // keep the lists readable until CTA 0 is done
+  } else if (flags & F_IDX_OUT) {
+    write_idx_out();
   }
   if (bad) atomicOr(p.status, 1);
 }
 
-template <typename T, int D>
+// Opts the kernel into the largest dynamic shared memory the device allows
+// and into non-portable (up to 16 CTA) clusters; once per process.
+template <typename T, int D, int KIND>
 cudaError_t prepare_kernel() {
   static cudaError_t once = [] {
-    auto k = fasa_cluster_kernel<T, D>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    auto k = fasa_cluster_kernel<T, D, KIND>;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }();
   return once;
 }
 
-template <typename T, int D>
-cudaError_t launch_cluster_t(const Params& p, int C, cudaStream_t s) {
-  cudaError_t e = prepare_kernel<T, D>();
-  if (e != cudaSuccess) return e;
+inline int kind_of(int flags) {
+  if ((flags & (F_TIP | F_SELECT | F_FAC | F_ROPE)) == (F_TIP | F_SELECT | F_FAC | F_ROPE)) return KIND_STEP;
+  if (flags == F_DENSE) return KIND_DENSE;
+  return KIND_STAGE;
+}
+
+template <int KIND>
+inline cudaLaunchConfig_t cluster_config(int C, int units, int smem, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)C, (unsigned)(p.B * p.Hkv), 1);
+  cfg.gridDim = dim3((unsigned)C, (unsigned)units, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)p.smem_total;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fasa_cluster_kernel<T, D>, p);
+  return cfg;
+}
+
+template <typename T, int D, int KIND>
+cudaError_t launch_kind(const Params& p, int C, cudaStream_t s) {
+  cudaError_t e = prepare_kernel<T, D, KIND>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config<KIND>(C, p.B * p.Hkv, p.smem_total, s, attr);
+  return cudaLaunchKernelEx(&cfg, fasa_cluster_kernel<T, D, KIND>, p);
 }
 
 template <typename T, int D>
-int max_clusters_t(int C, int smem_bytes) {
-  if (prepare_kernel<T, D>() != cudaSuccess) return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)C, 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+cudaError_t launch_cluster_t(const Params& p, int C, cudaStream_t s) {
+  switch (kind_of(p.flags)) {
+    case KIND_STEP: return launch_kind<T, D, KIND_STEP>(p, C, s);
+    case KIND_DENSE: return launch_kind<T, D, KIND_DENSE>(p, C, s);
+    default: return launch_kind<T, D, KIND_STAGE>(p, C, s);
+  }
+}
+
+template <typename T, int D, int KIND>
+int max_clusters_kind(int C, int smem_bytes) {
+  if (prepare_kernel<T, D, KIND>() != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = cluster_config<KIND>(C, 1, smem_bytes, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fasa_cluster_kernel<T, D>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, fasa_cluster_kernel<T, D, KIND>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
+}
+
+template <typename T, int D>
+int max_clusters_t(int flags, int C, int smem_bytes) {
+  switch (kind_of(flags)) {
+    case KIND_STEP: return max_clusters_kind<T, D, KIND_STEP>(C, smem_bytes);
+    case KIND_DENSE: return max_clusters_kind<T, D, KIND_DENSE>(C, smem_bytes);
+    default: return max_clusters_kind<T, D, KIND_STAGE>(C, smem_bytes);
+  }
 }
 
 }  // namespace fasa

@@ -9,9 +9,9 @@ cudaError_t launch_cluster_f32(const Params& p, int head_dim, int C, cudaStream_
   return cudaErrorInvalidValue;
 }
 
-int max_active_clusters_f32(int head_dim, int C, int smem_bytes) {
-  if (head_dim == 128) return max_clusters_t<float, 128>(C, smem_bytes);
-  if (head_dim == 64) return max_clusters_t<float, 64>(C, smem_bytes);
+int max_active_clusters_f32(int flags, int head_dim, int C, int smem_bytes) {
+  if (head_dim == 128) return max_clusters_t<float, 128>(flags, C, smem_bytes);
+  if (head_dim == 64) return max_clusters_t<float, 64>(flags, C, smem_bytes);
   return 0;
 }
 

@@ -12,7 +12,11 @@ constexpr int RT = 32;           // FAC rows per pipeline tile
 constexpr int FAC_STAGES = 4;    // cp.async ring depth of the FAC gather
 constexpr int G_MAX = 8;         // largest GQA group
 constexpr int C_MAX = 16;        // largest cluster
-constexpr int MISC_BYTES = 4096; // broadcast / reduction scratch in shared memory
+constexpr int KDOM_BLOCK = 64;   // tokens per block of the dominant-key copy
+constexpr int MISC_BYTES = 2048; // broadcast / reduction scratch in shared memory
+// Radix digits of the 32-bit score keys: 12 + 10 + 10 bits.
+constexpr int HLOC_BINS = 4096;  // local histogram (largest digit)
+constexpr int HLEAD_BINS = 4096 + 1024 + 1024;  // cluster totals of the three digits
 
 // What one launch of the cluster kernel does.
 enum : int {
@@ -28,7 +32,9 @@ enum : int {
 
 struct Params {
   int B, Hq, Hkv, G, T_max, n_tip, budget, flags;
-  double rope_theta;
+  // RoPE frequencies as fixed-point turns: rope_turns[i] = theta_i / (2 pi) * 2^64
+  // (theta_i = B^(-2i/d)); pos * rope_turns[i] mod 2^64 is the angle in turns.
+  unsigned long long rope_turns[64];
   const void* q;            // pre-RoPE stored query (F_ROPE)
   const float* q_rot;       // rotated fp32 query (otherwise)
   const int* pos;
@@ -52,8 +58,9 @@ struct Params {
   int cand_cap;             // candidate entries per CTA
   int idx_cap;              // selected-index entries per CTA
   int hpc;                  // heads combined per CTA = ceil(G / C)
-  int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hist, off_sc, off_idx, off_part,
-      off_big, smem_total;
+  int fac_off;              // byte offset of the FAC staging ring inside the big region
+  int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hloc, off_hlead, off_sc, off_idx, off_own,
+      off_part, off_big, smem_total;
 };
 
 // Kernel launchers (one translation unit per storage type).
@@ -61,7 +68,7 @@ cudaError_t launch_cluster_bf16(const Params& p, int head_dim, int C, cudaStream
 cudaError_t launch_cluster_f32(const Params& p, int head_dim, int C, cudaStream_t s);
 // Prepares function attributes and returns the number of co-resident clusters
 // of size C for this configuration (0 if C cannot be launched).
-int max_active_clusters_bf16(int head_dim, int C, int smem_bytes);
-int max_active_clusters_f32(int head_dim, int C, int smem_bytes);
+int max_active_clusters_bf16(int flags, int head_dim, int C, int smem_bytes);
+int max_active_clusters_f32(int flags, int head_dim, int C, int smem_bytes);
 
 }  // namespace fasa

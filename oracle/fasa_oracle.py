@@ -241,19 +241,21 @@ def decode_step(q, pos, K, V, dom_fc, seq_lens, k, rope_theta):
     return out, idx, count, scores
 
 
-def build_kdom(K_stored: np.ndarray, dom_fc: np.ndarray) -> np.ndarray:
-    """Dominant key cache C_key^dom, FC-major: [B,Hkv,n,T,2] of stored values.
+def build_kdom(K_stored: np.ndarray, dom_fc: np.ndarray, block: int = 64) -> np.ndarray:
+    """Dominant key cache C_key^dom of stored values, FC-major within blocks of
+    `block` tokens: [B, Hkv, T/block, n, block, 2].
 
-    K_dom[b,h,j,tau,:] = K[b,h,tau, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2] (a copy;
-    the FC pair is never split).
+    K_dom[b,h,t//block,j,t%block,:] = K[b,h,t, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2]
+    (a copy; the FC pair is never split).
     """
     B, Hkv, T, _ = K_stored.shape
     n = dom_fc.shape[1]
-    out = np.empty((B, Hkv, n, T, 2), dtype=K_stored.dtype)
+    out = np.empty((B, Hkv, T // block, n, block, 2), dtype=K_stored.dtype)
     for h in range(Hkv):
         for j in range(n):
             i = int(dom_fc[h, j])
-            out[:, h, j, :, :] = K_stored[:, h, :, 2 * i:2 * i + 2]
+            cols = K_stored[:, h, :, 2 * i:2 * i + 2]           # [B, T, 2]
+            out[:, h, :, j, :, :] = cols.reshape(B, T // block, block, 2)
     return out
 
 

@@ -31,7 +31,7 @@ def build_kdom(layer, dims):
     import torch
     from kv_cache_token_tip_gb300 import fasa_build_kdom
     cfg = layer.cfg
-    kd = torch.empty((cfg.batch, cfg.n_kv_heads, dims.n_tip, cfg.context, 2),
+    kd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.context // 64, dims.n_tip, 64, 2),
                      dtype=layer.k.dtype, device=layer.k.device)
     fasa_build_kdom(layer.k, layer.dom_fc, None, kd, dims)
     return kd

@@ -306,20 +306,22 @@ def check_decode_stored(o):
 
 
 def check_build_kdom_layout(o):
-    """K_dom is FC-major: K_dom[b,h,j,tau,c] holds K[b,h,tau,2 dom[h,j] + c].
-    Keys that encode their own coordinates make the layout self-evident."""
-    B, H, T, d = 2, 3, 10, 16
+    """K_dom is FC-major within token blocks: K_dom[b,h,t//4,j,t%4,c] holds
+    K[b,h,t,2 dom[h,j] + c].  Keys that encode their own coordinates make the
+    layout self-evident."""
+    B, H, T, d = 2, 3, 12, 16
     K = np.zeros((B, H, T, d), dtype=np.float32)
     for b in range(B):
         for h in range(H):
             for t in range(T):
                 K[b, h, t] = b * 1e6 + h * 1e4 + t * 100 + np.arange(d)
     dom = np.array([[0, 5, 7], [1, 2, 3], [7, 6, 0]])
-    kd = o.build_kdom(K, dom)
-    assert kd.shape == (B, H, 3, T, 2)
-    assert kd[1, 2, 0, 4, 1] == 1e6 + 2e4 + 400 + 15      # FC 7 -> dims 14, 15
-    assert kd[0, 0, 1, 9, 0] == 900 + 10                  # FC 5 -> dim 10
-    assert kd[1, 1, 2, 0, 0] == 1e6 + 1e4 + 6             # FC 3 -> dim 6
+    kd = o.build_kdom(K, dom, block=4)
+    assert kd.shape == (B, H, 3, 3, 4, 2)
+    assert kd[1, 2, 1, 0, 0, 1] == 1e6 + 2e4 + 400 + 15   # t=4, FC 7 -> dims 14, 15
+    assert kd[0, 0, 2, 1, 1, 0] == 900 + 10               # t=9, FC 5 -> dim 10
+    assert kd[1, 1, 0, 2, 0, 0] == 1e6 + 1e4 + 6          # t=0, FC 3 -> dim 6
+    assert kd[0, 1, 2, 0, 3, 1] == 1e4 + 1100 + 3         # t=11, FC 1 -> dim 3
 
 
 def check_byte_model(o):

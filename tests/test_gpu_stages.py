@@ -76,11 +76,16 @@ def test_build_and_append_kdom_bit_exact(name, kw):
                        L.k.view(torch.int16).cpu().numpy(), L.dom_fc_host)
     got = kd.cpu().numpy() if cfg.dtype == "f32" else kd.view(torch.int16).cpu().numpy()
     assert np.array_equal(got, ref)
+
+    def fc_major(a):   # [B,H,T/64,n,64,2] -> [B,H,n,T,2]
+        B_, H_, nb, n_, kb, _ = a.shape
+        return a.transpose(0, 1, 3, 2, 4, 5).reshape(B_, H_, n_, nb * kb, 2)
+    ref = fc_major(ref)
     # ragged build touches only tau < len
     lens = np.array([max(1, cfg.context - 37 * (b + 1)) for b in range(cfg.batch)], dtype=np.int32)
     kd2 = torch.zeros_like(kd)
     fasa_build_kdom(L.k, L.dom_fc, torch.from_numpy(lens).cuda(), kd2, dims)
-    g2 = kd2.cpu().numpy() if cfg.dtype == "f32" else kd2.view(torch.int16).cpu().numpy()
+    g2 = fc_major(kd2.cpu().numpy() if cfg.dtype == "f32" else kd2.view(torch.int16).cpu().numpy())
     for b in range(cfg.batch):
         assert np.array_equal(g2[b, :, :, :lens[b]], ref[b, :, :, :lens[b]])
         assert not np.any(g2[b, :, :, lens[b]:])
@@ -88,7 +93,7 @@ def test_build_and_append_kdom_bit_exact(name, kw):
     k_new = torch.randn((cfg.batch, cfg.n_kv_heads, cfg.head_dim), device="cuda").to(L.k.dtype)
     slots = torch.from_numpy(np.minimum(lens, cfg.context - 1)).cuda()
     fasa_append_kdom(k_new, L.dom_fc, slots, kd2, dims)
-    g3 = kd2.cpu().numpy() if cfg.dtype == "f32" else kd2.view(torch.int16).cpu().numpy()
+    g3 = fc_major(kd2.cpu().numpy() if cfg.dtype == "f32" else kd2.view(torch.int16).cpu().numpy())
     kn = k_new.cpu().numpy() if cfg.dtype == "f32" else k_new.view(torch.int16).cpu().numpy()
     for b in range(cfg.batch):
         for h in range(cfg.n_kv_heads):

@@ -78,14 +78,14 @@ def _freq_half_exponent(rope_theta, d):
     return np.power(float(rope_theta), -1.0 * np.arange(d // 2) / d)
 
 
-def _kdom_wrong_pair(K_stored, dom_fc):
+def _kdom_wrong_pair(K_stored, dom_fc, block=64):
     B, H, T, _ = K_stored.shape
     n = dom_fc.shape[1]
-    out = np.empty((B, H, n, T, 2), dtype=K_stored.dtype)
+    out = np.empty((B, H, T // block, n, block, 2), dtype=K_stored.dtype)
     for h in range(H):
         for j in range(n):
             i = int(dom_fc[h, j])
-            out[:, h, j] = K_stored[:, h, :, i:i + 2]
+            out[:, h, :, j] = K_stored[:, h, :, i:i + 2].reshape(B, T // block, block, 2)
     return out
 
 
