@@ -375,72 +375,85 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const int tau_base = it * tt;
     const int ntok = min(tt, nloc - tau_base);
     const unsigned char* st = big + s * stage_bytes;
-    for (int tl = tid * 4; tl < ntok; tl += NT * 4) {
-      // two independent accumulator sets (even / odd FC) for latency hiding
+    // a pair of threads (lanes 2i, 2i+1) shares four consecutive tokens; each
+    // takes half of the FCs and one shuffle adds the halves
+    const int half = lane & 1;
+    const int jmid = (nfc + 1) >> 1;
+    const int j0 = half ? jmid : 0, j1 = half ? nfc : jmid;
+    for (int gbase = warp * 16; gbase * 4 < ntok; gbase += NT / 2) {  // warp-uniform
+      const int tl = (gbase + (lane >> 1)) * 4;
+      const bool act = tl < ntok;
       float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      const unsigned char* row = st + (tl / KB) * blk_bytes + (tl % KB) * 2 * ES;
-      int j = 0;
+      if (act) {
+        const unsigned char* row = st + (tl / KB) * blk_bytes + (tl % KB) * 2 * ES;
+        int j = j0;
 #pragma unroll 4
-      for (; j + 2 <= nfc; j += 2) {
-        const float4 qq = *reinterpret_cast<const float4*>(&qbar[2 * j]);
-        if constexpr (ES == 2) {
-          const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
-          const uint4 u = *reinterpret_cast<const uint4*>(row + (j + 1) * fc_row_bytes);
-          a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
-          a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
-          a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
-          a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
-          a1[0] = fmaf(qq.z, bf16_lo(u.x), fmaf(qq.w, bf16_hi(u.x), a1[0]));
-          a1[1] = fmaf(qq.z, bf16_lo(u.y), fmaf(qq.w, bf16_hi(u.y), a1[1]));
-          a1[2] = fmaf(qq.z, bf16_lo(u.z), fmaf(qq.w, bf16_hi(u.z), a1[2]));
-          a1[3] = fmaf(qq.z, bf16_lo(u.w), fmaf(qq.w, bf16_hi(u.w), a1[3]));
-        } else {
-          const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
-          const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
-          const float4 u0 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes);
-          const float4 u1 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes + 16);
-          a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
-          a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
-          a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
-          a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
-          a1[0] = fmaf(qq.z, u0.x, fmaf(qq.w, u0.y, a1[0]));
-          a1[1] = fmaf(qq.z, u0.z, fmaf(qq.w, u0.w, a1[1]));
-          a1[2] = fmaf(qq.z, u1.x, fmaf(qq.w, u1.y, a1[2]));
-          a1[3] = fmaf(qq.z, u1.z, fmaf(qq.w, u1.w, a1[3]));
+        for (; j + 2 <= j1; j += 2) {
+          const float4 qq = *reinterpret_cast<const float4*>(&qbar[2 * j]);
+          if constexpr (ES == 2) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
+            const uint4 u = *reinterpret_cast<const uint4*>(row + (j + 1) * fc_row_bytes);
+            a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
+            a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
+            a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
+            a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
+            a1[0] = fmaf(qq.z, bf16_lo(u.x), fmaf(qq.w, bf16_hi(u.x), a1[0]));
+            a1[1] = fmaf(qq.z, bf16_lo(u.y), fmaf(qq.w, bf16_hi(u.y), a1[1]));
+            a1[2] = fmaf(qq.z, bf16_lo(u.z), fmaf(qq.w, bf16_hi(u.z), a1[2]));
+            a1[3] = fmaf(qq.z, bf16_lo(u.w), fmaf(qq.w, bf16_hi(u.w), a1[3]));
+          } else {
+            const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
+            const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
+            const float4 u0 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes);
+            const float4 u1 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes + 16);
+            a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
+            a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
+            a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
+            a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
+            a1[0] = fmaf(qq.z, u0.x, fmaf(qq.w, u0.y, a1[0]));
+            a1[1] = fmaf(qq.z, u0.z, fmaf(qq.w, u0.w, a1[1]));
+            a1[2] = fmaf(qq.z, u1.x, fmaf(qq.w, u1.y, a1[2]));
+            a1[3] = fmaf(qq.z, u1.z, fmaf(qq.w, u1.w, a1[3]));
+          }
         }
-      }
-      if (j < nfc) {
-        const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
-        if constexpr (ES == 2) {
-          const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
-          a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
-          a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
-          a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
-          a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
-        } else {
-          const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
-          const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
-          a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
-          a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
-          a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
-          a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
+        if (j < j1) {
+          const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
+          if constexpr (ES == 2) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
+            a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
+            a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
+            a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
+            a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
+          } else {
+            const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
+            const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
+            a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
+            a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
+            a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
+            a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
+          }
         }
       }
       float acc[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) acc[t] = a0[t] + a1[t];
-      const int tloc = tau_base + tl;
-      if (tl + 4 <= ntok) {
-        *reinterpret_cast<float4*>(scw + tloc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          if (tl + t < ntok) scw[tloc + t] = acc[t];
+      for (int t = 0; t < 4; ++t) {
+        acc[t] = a0[t] + a1[t];
+        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 1);
       }
-      if (need_select) {
+      if (act && half == 0) {
+        const int tloc = tau_base + tl;
+        if (tl + 4 <= ntok) {
+          *reinterpret_cast<float4*>(scw + tloc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        } else {
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          if (tl + t < ntok) atomicAdd(&hloc[score_key(acc[t]) >> 20], 1u);
+          for (int t = 0; t < 4; ++t)
+            if (tl + t < ntok) scw[tloc + t] = acc[t];
+        }
+        if (need_select) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (tl + t < ntok) atomicAdd(&hloc[score_key(acc[t]) >> 20], 1u);
+        }
       }
     }
     const int anyfail = __syncthreads_or(fail);
@@ -490,14 +503,14 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       const int s = t % FAC_STAGES;
       const int rows_t = min(RT, fr_n - t * RT);
       const uint32_t st0 = smem_u32(fac_stage) + s * FAC_STAGE_B;
-      for (int c = tid; c < 2 * rows_t * CPR; c += NT) {
-        const int which = c / (rows_t * CPR);
-        const int rc = c - which * rows_t * CPR;
-        const int rr = rc / CPR;
-        const int ch = rc - rr * CPR;
-        const int tau = row_token(t * RT + rr);
-        const T* src = (which ? Vb : Kb) + (size_t)tau * D + ch * (16 / ES);
-        cp_async16(st0 + which * RT * ROWS + rr * ROWS + ch * 16, src);
+      // one warp per row: lanes take the 16-byte chunks of its K then V row
+      for (int rr = warp; rr < rows_t; rr += NW) {
+        const size_t row_off = (size_t)row_token(t * RT + rr) * D;
+        for (int c = lane; c < 2 * CPR; c += 32) {
+          const int which = c >= CPR;
+          const int ch = c - which * CPR;
+          cp_async16(st0 + which * RT * ROWS + rr * ROWS + ch * 16, (which ? Vb : Kb) + row_off + ch * (16 / ES));
+        }
       }
     }
     cp_async_commit();
