@@ -178,6 +178,35 @@ int fasa_decode_step(const void* q, const int32_t* pos,
                      const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
+ * Size of the fixed device scratch array used by fasa_decode_step_noalloc:
+ * 16 MiB, i.e. scores for B * Hkv * T_max <= 4194304 cached tokens.
+ */
+#define FASA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * fasa_decode_step for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is an interface convenience).  Same arguments as
+ * fasa_decode_step without the workspace: when the step needs a score
+ * workspace it uses a fixed array of FASA_NOALLOC_SCRATCH_BYTES inside the
+ * library image instead (reserved on every GPU that loads the library until
+ * the process exits).  Nothing is allocated or freed.
+ *  - Returns FASA_ERR_WORKSPACE when the step would need more scratch than
+ *    FASA_NOALLOC_SCRATCH_BYTES (B * Hkv * T_max * 4 bytes).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares that device's one array: calls that may
+ *    overlap on the GPU (for instance on two streams) race on it and must be
+ *    serialised by the caller.  The array needs no clearing: a call writes
+ *    every score it reads before reading it.
+ */
+int fasa_decode_step_noalloc(const void* q, const int32_t* pos,
+                             const void* k_cache, const void* v_cache, const void* k_dom,
+                             const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget,
+                             float* out, int32_t* idx_out, int32_t* count_out,
+                             const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
  * Synchronises `stream`, stores the device status word of the current device
  * in *status (FASA_DEV_* bits, 0 = clean) and clears it.
  */

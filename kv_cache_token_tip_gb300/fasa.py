@@ -19,7 +19,7 @@ EXPORTS = [
     "fasa_version", "fasa_status_string", "fasa_last_cuda_error", "fasa_max_budget",
     "fasa_workspace_size", "fasa_apply_rope_q", "fasa_build_kdom", "fasa_append_kdom",
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
-    "fasa_decode_step", "fasa_device_status", "fasa_cluster_size",
+    "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
 ]
 
 
@@ -84,6 +84,7 @@ def lib():
             "fasa_decode_step": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
                                  ctypes.c_int),
             "fasa_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+            "fasa_decode_step_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, dp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -218,6 +219,19 @@ def fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: 
         _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
         _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_decode_step_noalloc(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: int, out,
+                             idx_out=None, count_out=None, dims: FasaDims = None, stream=None):
+    """fasa_decode_step without a workspace argument: for callers that cannot
+    allocate device memory, the step uses the library's fixed scratch array."""
+    _check("fasa_decode_step_noalloc", lib().fasa_decode_step_noalloc(
+        _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"),
+        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
+        _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
+        ctypes.byref(dims), _stream(stream)))
 
 
 def fasa_device_status(stream=None) -> int:
