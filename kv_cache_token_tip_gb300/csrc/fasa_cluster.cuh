@@ -51,6 +51,7 @@ struct Misc {
   int tiesR[C_MAX];
   int scan[NW];
   int scan2[NW];
+  float hm[G_MAX], hl[G_MAX], hs[G_MAX];  // tensor-core FAC: per-head softmax state
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -503,13 +504,17 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       const int s = t % FAC_STAGES;
       const int rows_t = min(RT, fr_n - t * RT);
       const uint32_t st0 = smem_u32(fac_stage) + s * FAC_STAGE_B;
-      // one warp per row: lanes take the 16-byte chunks of its K then V row
-      for (int rr = warp; rr < rows_t; rr += NW) {
-        const size_t row_off = (size_t)row_token(t * RT + rr) * D;
+      // one warp per row: lanes take the 16-byte chunks of its K then V row;
+      // rows past the end of the tile are zero-filled (the tensor-core path
+      // multiplies them by zero weights, which must not meet stale NaNs)
+      for (int rr = warp; rr < RT; rr += NW) {
+        const bool real = rr < rows_t;
+        const size_t row_off = real ? (size_t)row_token(t * RT + rr) * D : 0;
         for (int c = lane; c < 2 * CPR; c += 32) {
           const int which = c >= CPR;
           const int ch = c - which * CPR;
-          cp_async16(st0 + which * RT * ROWS + rr * ROWS + ch * 16, (which ? Vb : Kb) + row_off + ch * (16 / ES));
+          cp_async16_zfill(st0 + which * RT * ROWS + rr * ROWS + ch * 16, (which ? Vb : Kb) + row_off + ch * (16 / ES),
+                           real ? 16u : 0u);
         }
       }
     }
@@ -795,6 +800,132 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       fac_start();
     }
 
+    constexpr int PSTRIDE = D + 4;
+    const int ntile = (fr_n + RT - 1) / RT;
+    if constexpr (ES == 2) {
+      // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+      //   QK as S^T = K Q^T  (16 rows x 8 heads per MMA; warps 0, 1 take the
+      //   two 16-row halves of a tile), PV as O^T = V^T P^T (16 head dims x 8
+      //   heads per MMA; warp w takes dims 16w..16w+15).  q and P are split
+      //   into bf16 hi + lo parts, so the products keep ~16 mantissa bits.
+      constexpr int KS = D / 16;
+      const float qs = 1.4426950408889634f * rsqrtf((float)D);
+      const int gq = lane >> 2, tq = lane & 3;
+      uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo]
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int d0 = ks * 16 + 2 * tq + hb * 8;
+          const float x0 = gq < G ? qrot[gq * D + d0] * qs : 0.f;
+          const float x1 = gq < G ? qrot[gq * D + d0 + 1] * qs : 0.f;
+          split_bf16(x0, x1, qb[ks][hb][0], qb[ks][hb][1]);
+        }
+      float* hm = ms->hm;  // running max (log2 units) per head
+      float* hl = ms->hl;  // running sum per head
+      float* hs = ms->hs;  // rescale of the current tile per head
+      if (tid < G_MAX) {
+        hm[tid] = -CUDART_INF_F;
+        hl[tid] = 0.f;
+      }
+      float oc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int t = 0; t < ntile; ++t) {
+        cp_async_wait<FAC_STAGES - 2>();
+        __syncthreads();
+        fac_issue(t + FAC_STAGES - 1);
+        const int s = t % FAC_STAGES;
+        const uint32_t Ks = smem_u32(fac_stage + s * FAC_STAGE_B);
+        const uint32_t Vs = Ks + RT * ROWS;
+        const int rows_t = min(RT, fr_n - t * RT);
+        if (warp < 2 && warp * 16 < rows_t) {
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          const int mi = lane >> 3;
+          const uint32_t arow = Ks + (warp * 16 + (lane & 7) + 8 * (mi & 1)) * ROWS + 16 * (mi >> 1);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(arow + ks * 32, a0, a1, a2, a3);
+            mma_bf16_16816(c, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
+            mma_bf16_16816(c, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
+          }
+          const int r0 = warp * 16 + gq, r1 = r0 + 8;
+          const bool v0 = r0 < rows_t && !row_masked(t * RT + r0);
+          const bool v1 = r1 < rows_t && !row_masked(t * RT + r1);
+          const int h0 = 2 * tq, h1 = 2 * tq + 1;
+          if (h0 < G) {
+            stile[h0 * RT + r0] = v0 ? c[0] : -CUDART_INF_F;
+            stile[h0 * RT + r1] = v1 ? c[2] : -CUDART_INF_F;
+          }
+          if (h1 < G) {
+            stile[h1 * RT + r0] = v0 ? c[1] : -CUDART_INF_F;
+            stile[h1 * RT + r1] = v1 ? c[3] : -CUDART_INF_F;
+          }
+        }
+        __syncthreads();
+        // online softmax: warp g owns head g; P overwrites the logits
+        {
+          const int g = warp;
+          float p = 0.f, scale = 1.f;
+          if (g < G) {
+            const float sv = lane < rows_t ? stile[g * RT + lane] : -CUDART_INF_F;
+            const float m_old = hm[g];
+            const float m_new = fmaxf(m_old, warp_max(sv));
+            if (m_new != -CUDART_INF_F) {
+              scale = exp2f(m_old - m_new);
+              p = lane < rows_t ? exp2f(sv - m_new) : 0.f;
+            }
+            const float lsum = warp_sum(p);
+            if (lane == 0) {
+              hm[g] = m_new;
+              hl[g] = hl[g] * scale + lsum;
+            }
+          }
+          stile[g * RT + lane] = p;  // heads >= G get zero weights
+          if (lane == 0) hs[g] = scale;
+        }
+        __syncthreads();
+        if (warp < KS) {
+          const float s0 = hs[2 * tq], s1 = hs[2 * tq + 1];
+          oc[0] *= s0;
+          oc[1] *= s1;
+          oc[2] *= s0;
+          oc[3] *= s1;
+          const int mi = lane >> 3;
+#pragma unroll
+          for (int kk = 0; kk < RT / 16; ++kk) {
+            if (kk * 16 < rows_t) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(Vs + (kk * 16 + (lane & 7) + 8 * (mi >> 1)) * ROWS + (warp * 16 + 8 * (mi & 1)) * 2, a0, a1,
+                        a2, a3);
+              const float* pr = stile + gq * RT + kk * 16 + 2 * tq;
+              uint32_t b0h, b0l, b1h, b1l;
+              split_bf16(pr[0], pr[1], b0h, b0l);
+              split_bf16(pr[8], pr[9], b1h, b1l);
+              mma_bf16_16816(oc, a0, a1, a2, a3, b0h, b1h);
+              mma_bf16_16816(oc, a0, a1, a2, a3, b0l, b1l);
+            }
+          }
+        }
+      }
+      cp_async_wait<0>();
+      __syncthreads();
+      // this CTA's partial record per head: o[0..D), m, l
+      if (warp < KS) {
+        const int dd = warp * 16 + gq;
+        if (2 * tq < G) {
+          part[(2 * tq) * PSTRIDE + dd] = oc[0];
+          part[(2 * tq) * PSTRIDE + dd + 8] = oc[2];
+        }
+        if (2 * tq + 1 < G) {
+          part[(2 * tq + 1) * PSTRIDE + dd] = oc[1];
+          part[(2 * tq + 1) * PSTRIDE + dd + 8] = oc[3];
+        }
+      }
+      if (tid < G) {
+        part[tid * PSTRIDE + D] = hm[tid];
+        part[tid * PSTRIDE + D + 1] = hl[tid];
+      }
+    } else {
     const float qs = 1.4426950408889634f * rsqrtf((float)D);
     float qreg[G_MAX][EPL];
 #pragma unroll
@@ -809,7 +940,6 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o_run[e] = 0.f;
 
-    const int ntile = (fr_n + RT - 1) / RT;
     for (int t = 0; t < ntile; ++t) {
       cp_async_wait<FAC_STAGES - 2>();
       __syncthreads();
@@ -864,7 +994,6 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
     // merge the row-parts of each head into this CTA's partial record
     // part[g] = (o[0..D), m, l) with m in log2 units; other CTAs pull it
-    constexpr int PSTRIDE = D + 4;
     float* mst = reinterpret_cast<float*>(fac_stage);
     if (pv_warp) {
       float* dst = mst + (my_g * nparts + my_part) * (D + 2);
@@ -890,6 +1019,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         val = acc;
       }
       part[g * PSTRIDE + e] = val;
+    }
     }
     cluster_sync();
 
