@@ -126,7 +126,7 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   p.off_qbar = off;
   off += align_up(2 * nfc * 4, 16);
   p.off_stile = off;
-  off += G_MAX * RT * 4;
+  off += (es == 2 ? NW * G_MAX * PTS : G_MAX * RT) * 4;
   p.off_hloc = off;
   off += select ? HLOC_BINS * 4 : 0;
   p.off_hlead = off;
@@ -134,7 +134,15 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   p.idx_cap = (flags & (F_SELECT | F_IDX_IN)) ? align_up(p.budget, 4) : 0;
   p.hpc = ceil_div(G, C);
   const int part_bytes = fac ? G * (D + 4) * 4 : 0;
-  const int fac_big = fac ? FAC_STAGES * 2 * RT * (D * es + 16) : 0;
+  // pushed partial records: [C][largest slice] float4 groups, then [C][G] (m, l)
+  const int ngrp4 = G * (D / 4);
+  const int recv_bytes = fac ? align_up(C * ceil_div(ngrp4, C) * 16 + C * G * 8, 128) : 0;
+  // FAC staging: fp32 -- a block-wide ring of FAC_STAGES tiles of RT rows;
+  // bf16 -- per warp, wst slots of one GR-row group (two if they fit)
+  auto fac_bytes = [&](int wst) {
+    if (!fac) return 0;
+    return es == 2 ? wst * NW * 2 * GR * (D * es + 16) : FAC_STAGES * 2 * RT * (D * es + 16);
+  };
 
   int s_cap = 0;
   *ws = 0;
@@ -142,7 +150,15 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
     const int chunk = align_up(ceil_div(d->t_max, C), KDOM_BLOCK);
     if (chunk <= S_CAP_MAX) s_cap = chunk;
   }
-  for (int attempt = 0; attempt < 2; ++attempt) {
+  // preference: scores in shared memory before two groups in flight per warp
+  const int s_cap0 = s_cap;
+  for (int attempt = 0; attempt < 4; ++attempt) {
+    const int wst = (es == 2 && attempt % 2 == 0) ? 2 : 1;
+    if (attempt % 2 == 1 && es != 2) continue;  // fp32 has no per-warp groups
+    if (attempt >= 2 && s_cap0 == 0) break;     // no second layout of the scores
+    s_cap = attempt < 2 ? s_cap0 : 0;
+    const int fac_big = fac_bytes(wst);
+    p.fac_wst = wst;
     int o = off;
     p.off_sc = o;
     o += s_cap * 4;
@@ -152,7 +168,7 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
     // next to the FAC ring
     int cap = 0;
     if (select) {
-      cap = (limit - (o + part_bytes + 256) - fac_big) / 8;
+      cap = (limit - (o + part_bytes + recv_bytes + 384) - fac_big) / 8;
       if (cap > p.budget + 4096) cap = p.budget + 4096;
       cap &= ~15;
     }
@@ -161,6 +177,9 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
     o += cap * 8;
     p.off_part = o;
     o += part_bytes;
+    o = align_up(o, 128);
+    p.off_recv = o;
+    o += recv_bytes;
     o = align_up(o, 128);
     p.off_big = o;
     p.fac_off = 0;
@@ -194,8 +213,6 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
       }
       return FASA_OK;
     }
-    if (s_cap == 0) break;
-    s_cap = 0;  // retry with the scores in the global workspace
   }
   return FASA_ERR_UNSUPPORTED;
 }

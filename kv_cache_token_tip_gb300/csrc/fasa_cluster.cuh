@@ -51,7 +51,6 @@ struct Misc {
   int tiesR[C_MAX];
   int scan[NW];
   int scan2[NW];
-  float hm[G_MAX], hl[G_MAX], hs[G_MAX];  // tensor-core FAC: per-head softmax state
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -210,6 +209,74 @@ __device__ __forceinline__ void radix_find(const uint32_t* hist, int k_rem, Misc
     run += ci;
   }
   __syncthreads();
+}
+
+// TIP scores of one staged k_dom tile (ntok tokens from the tile start, in
+// blocks of KDOM_BLOCK tokens, FC-major inside a block).  Thread t takes four
+// consecutive tokens at a time over all n FCs: one 16-byte (bf16) or two
+// (fp32) shared-memory loads per FC give the four tokens' (re, im) pairs.
+// NFC > 0 fixes n at compile time; NFC == 0 reads it from nfc_rt.  Scores go
+// to sc[0..ntok); with `hist`, each key's top 12 bits are counted in hloc.
+template <typename T, int NFC>
+__device__ __forceinline__ void tip_tile(const unsigned char* st, int ntok, int nfc_rt, const float* qbar, float* sc,
+                                         uint32_t* hloc, bool hist) {
+  constexpr int ES = sizeof(T);
+  const int nfc = NFC > 0 ? NFC : nfc_rt;
+  constexpr uint32_t fc_row_bytes = KDOM_BLOCK * 2 * ES;
+  const uint32_t blk_bytes = (uint32_t)nfc * fc_row_bytes;
+  for (int tl = threadIdx.x * 4; tl < ntok; tl += NT * 4) {
+    const unsigned char* row = st + (tl / KDOM_BLOCK) * blk_bytes + (tl % KDOM_BLOCK) * 2 * ES;
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    // adds FC j's term q_re * k_re + q_im * k_im of the four tokens into a
+    auto fc_add = [&](int j, float (&a)[4]) {
+      const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
+      if constexpr (ES == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
+        a[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a[0]));
+        a[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a[1]));
+        a[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a[2]));
+        a[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a[3]));
+      } else {
+        const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
+        const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
+        a[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a[0]));
+        a[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a[1]));
+        a[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a[2]));
+        a[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a[3]));
+      }
+    };
+    if constexpr (NFC > 0) {
+#pragma unroll
+      for (int j = 0; j + 2 <= NFC; j += 2) {
+        fc_add(j, a0);
+        fc_add(j + 1, a1);
+      }
+      if constexpr ((NFC & 1) != 0) fc_add(NFC - 1, a0);
+    } else {
+      int j = 0;
+#pragma unroll 2
+      for (; j + 2 <= nfc; j += 2) {
+        fc_add(j, a0);
+        fc_add(j + 1, a1);
+      }
+      if (j < nfc) fc_add(j, a0);
+    }
+    float acc[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[t] = a0[t] + a1[t];
+    if (tl + 4 <= ntok) {
+      *reinterpret_cast<float4*>(sc + tl) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (tl + t < ntok) sc[tl + t] = acc[t];
+    }
+    if (hist) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (tl + t < ntok) atomicAdd(&hloc[score_key(acc[t]) >> 20], 1u);
+    }
+  }
 }
 
 // KIND names the launch in profiles and lets the compiler drop unused phases:
@@ -376,86 +443,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const int tau_base = it * tt;
     const int ntok = min(tt, nloc - tau_base);
     const unsigned char* st = big + s * stage_bytes;
-    // a pair of threads (lanes 2i, 2i+1) shares four consecutive tokens; each
-    // takes half of the FCs and one shuffle adds the halves
-    const int half = lane & 1;
-    const int jmid = (nfc + 1) >> 1;
-    const int j0 = half ? jmid : 0, j1 = half ? nfc : jmid;
-    for (int gbase = warp * 16; gbase * 4 < ntok; gbase += NT / 2) {  // warp-uniform
-      const int tl = (gbase + (lane >> 1)) * 4;
-      const bool act = tl < ntok;
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      if (act) {
-        const unsigned char* row = st + (tl / KB) * blk_bytes + (tl % KB) * 2 * ES;
-        int j = j0;
-#pragma unroll 4
-        for (; j + 2 <= j1; j += 2) {
-          const float4 qq = *reinterpret_cast<const float4*>(&qbar[2 * j]);
-          if constexpr (ES == 2) {
-            const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
-            const uint4 u = *reinterpret_cast<const uint4*>(row + (j + 1) * fc_row_bytes);
-            a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
-            a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
-            a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
-            a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
-            a1[0] = fmaf(qq.z, bf16_lo(u.x), fmaf(qq.w, bf16_hi(u.x), a1[0]));
-            a1[1] = fmaf(qq.z, bf16_lo(u.y), fmaf(qq.w, bf16_hi(u.y), a1[1]));
-            a1[2] = fmaf(qq.z, bf16_lo(u.z), fmaf(qq.w, bf16_hi(u.z), a1[2]));
-            a1[3] = fmaf(qq.z, bf16_lo(u.w), fmaf(qq.w, bf16_hi(u.w), a1[3]));
-          } else {
-            const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
-            const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
-            const float4 u0 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes);
-            const float4 u1 = *reinterpret_cast<const float4*>(row + (j + 1) * fc_row_bytes + 16);
-            a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
-            a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
-            a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
-            a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
-            a1[0] = fmaf(qq.z, u0.x, fmaf(qq.w, u0.y, a1[0]));
-            a1[1] = fmaf(qq.z, u0.z, fmaf(qq.w, u0.w, a1[1]));
-            a1[2] = fmaf(qq.z, u1.x, fmaf(qq.w, u1.y, a1[2]));
-            a1[3] = fmaf(qq.z, u1.z, fmaf(qq.w, u1.w, a1[3]));
-          }
-        }
-        if (j < j1) {
-          const float2 qq = *reinterpret_cast<const float2*>(&qbar[2 * j]);
-          if constexpr (ES == 2) {
-            const uint4 w = *reinterpret_cast<const uint4*>(row + j * fc_row_bytes);
-            a0[0] = fmaf(qq.x, bf16_lo(w.x), fmaf(qq.y, bf16_hi(w.x), a0[0]));
-            a0[1] = fmaf(qq.x, bf16_lo(w.y), fmaf(qq.y, bf16_hi(w.y), a0[1]));
-            a0[2] = fmaf(qq.x, bf16_lo(w.z), fmaf(qq.y, bf16_hi(w.z), a0[2]));
-            a0[3] = fmaf(qq.x, bf16_lo(w.w), fmaf(qq.y, bf16_hi(w.w), a0[3]));
-          } else {
-            const float4 w0 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes);
-            const float4 w1 = *reinterpret_cast<const float4*>(row + j * fc_row_bytes + 16);
-            a0[0] = fmaf(qq.x, w0.x, fmaf(qq.y, w0.y, a0[0]));
-            a0[1] = fmaf(qq.x, w0.z, fmaf(qq.y, w0.w, a0[1]));
-            a0[2] = fmaf(qq.x, w1.x, fmaf(qq.y, w1.y, a0[2]));
-            a0[3] = fmaf(qq.x, w1.z, fmaf(qq.y, w1.w, a0[3]));
-          }
-        }
-      }
-      float acc[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        acc[t] = a0[t] + a1[t];
-        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 1);
-      }
-      if (act && half == 0) {
-        const int tloc = tau_base + tl;
-        if (tl + 4 <= ntok) {
-          *reinterpret_cast<float4*>(scw + tloc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (tl + t < ntok) scw[tloc + t] = acc[t];
-        }
-        if (need_select) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (tl + t < ntok) atomicAdd(&hloc[score_key(acc[t]) >> 20], 1u);
-        }
-      }
+    switch (nfc) {  // the common dominant-FC counts get fully unrolled loops
+      case 8: tip_tile<T, 8>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
+      case 12: tip_tile<T, 12>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
+      case 16: tip_tile<T, 16>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
+      default: tip_tile<T, 0>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
     }
     const int anyfail = __syncthreads_or(fail);
     if (anyfail) {
@@ -520,9 +512,32 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     }
     cp_async_commit();
   };
+  // bf16: warp w gathers and attends the GR-row groups w, w + NW, ...; slot
+  // s of its p.fac_wst private slots holds one group's K rows then V rows.
+  // Rows past fr_n are zero-filled.  Every call commits one cp.async group.
+  constexpr uint32_t GSLOT_B = 2u * GR * ROWS;
+  auto grp_issue = [&](int g, int s) {
+    if (g * GR < fr_n) {
+      const uint32_t st0 = smem_u32(big) + (uint32_t)(warp * p.fac_wst + s) * GSLOT_B;
+      for (int c = lane; c < GR * 2 * CPR; c += 32) {
+        const int rr = c / (2 * CPR), rem = c - rr * (2 * CPR);
+        const int which = rem >= CPR, ch = rem - which * CPR;
+        const int i = g * GR + rr;
+        const bool real = i < fr_n;
+        const size_t row_off = real ? (size_t)row_token(i) * D : 0;
+        cp_async16_zfill(st0 + which * GR * ROWS + rr * ROWS + ch * 16, (which ? Vb : Kb) + row_off + ch * (16 / ES),
+                         real ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
   auto fac_start = [&]() {
+    if constexpr (ES == 2) {
+      for (int s = 0; s < p.fac_wst; ++s) grp_issue(warp + s * NW, s);
+    } else {
 #pragma unroll
-    for (int s = 0; s < FAC_STAGES - 1; ++s) fac_issue(s);
+      for (int s = 0; s < FAC_STAGES - 1; ++s) fac_issue(s);
+    }
     fac_started = true;
   };
 
@@ -607,20 +622,67 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
       if (pass == 0) {
         // this CTA's candidates (top 12 bits >= prefix), token order, into
-        // own2 when they fit; each thread takes a contiguous run of tokens
-        // (odd length: conflict-free strides) and one block scan places them
-        const int seg = ((nloc + NT - 1) / NT) | 1;
-        const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
+        // own2 when they fit.  Warp w sweeps its contiguous share of the
+        // score vectors (float4 per lane, four in flight): the first sweep
+        // counts, the second writes at ballot-ranked positions.
+        const int nv = (nloc + 3) >> 2;
+        const int per_w = (nv + NW - 1) / NW;
+        const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
+        const uint32_t lt = (1u << lane) - 1u;
         int cnt = 0;
-        for (int i = s0; i < s1; ++i) cnt += (score_key(scr[i]) >> 20) >= prefix;
-        int total;
-        const int before = block_excl_scan(cnt, ms->scan, total);
+        for (int vb = v0; vb < v1; vb += 4 * 32) {
+          float x[4][4];
+          bool ok[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int v = vb + u * 32 + lane;
+            load4(scr, v * 4, v < v1 ? nloc : 0, x[u], ok[u]);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) cnt += ok[u][t] && (score_key(x[u][t]) >> 20) >= prefix;
+        }
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (lane == 0) ms->scan2[warp] = cnt;
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const int c = ms->scan2[w];
+          before += w < warp ? c : 0;
+          total += c;
+        }
         own_list = total <= p.cand_cap;
         if (own_list) {
           int pos = before;
-          for (int i = s0; i < s1 && pos < before + cnt; ++i) {
-            const uint32_t key = score_key(scr[i]);
-            if ((key >> 20) >= prefix) own2[pos++] = make_uint2(key, (uint32_t)(t0 + i));
+          for (int vb = v0; vb < v1; vb += 4 * 32) {
+            float x[4][4];
+            bool ok[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int v = vb + u * 32 + lane;
+              load4(scr, v * 4, v < v1 ? nloc : 0, x[u], ok[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t key[4], bal[4];
+              int excl = 0, wtot = 0;
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                key[t] = score_key(x[u][t]);
+                bal[t] = __ballot_sync(0xffffffffu, ok[u][t] && (key[t] >> 20) >= prefix);
+                excl += __popc(bal[t] & lt);
+                wtot += __popc(bal[t]);
+              }
+              if (wtot == 0) continue;  // warp-uniform
+              const int tok = t0 + (vb + u * 32 + lane) * 4;
+              int e = pos + excl;
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                if ((bal[t] >> lane) & 1u) own2[e++] = make_uint2(key[t], (uint32_t)(tok + t));
+              pos += wtot;
+            }
           }
           own_n = total;
           __syncthreads();
@@ -672,23 +734,50 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       return (key >> shift) >= prefix;
     };
     if (own_list) {
-      int run_t = 0, run_s = 0;
-      for (int e0 = 0; e0 < own_n; e0 += NT) {
-        const int e = e0 + tid;
-        const bool valid = e < own_n;
-        const uint32_t key = valid ? own2[e].x : 0u;
-        const bool tie = valid && ties_mode && key == prefix;
-        int tot_t = 0;
-        const int tr = ties_mode ? run_t + block_excl_scan((int)tie, ms->scan, tot_t) : 0;
-        const bool sel = valid && selected(key, tr);
-        int tot_s;
-        const int ps = run_s + block_excl_scan((int)sel, ms->scan, tot_s);
-        if (valid && !sel) own2[e].y |= 0x80000000u;
-        if (sel && ps < p.idx_cap) idx_s[ps] = (int)own2[e].y;
-        run_t += tot_t;
-        run_s += tot_s;
+      // warp w takes a contiguous share of the list; ranks within a warp
+      // come from ballots, across warps from per-warp totals
+      const uint32_t lt = (1u << lane) - 1u;
+      const int per_w = (own_n + NW - 1) / NW;
+      const int e0 = min(own_n, warp * per_w), e1 = min(own_n, e0 + per_w);
+      int tie_base = 0;
+      if (ties_mode) {
+        int c = 0;
+        for (int e = e0 + lane; e < e1; e += 32) c += own2[e].x == prefix;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) ms->scan2[warp] = c;
+        __syncthreads();
+        for (int w = 0; w < warp; ++w) tie_base += ms->scan2[w];
       }
-      if (tid == 0) ms->my_count = run_s;
+      int nsel = 0;
+      for (int eb = e0; eb < e1; eb += 32) {
+        const int e = eb + lane;
+        const bool valid = e < e1;
+        const uint32_t key = valid ? own2[e].x : 0u;
+        const uint32_t tb = __ballot_sync(0xffffffffu, valid && ties_mode && key == prefix);
+        const bool sel = valid && selected(key, tie_base + __popc(tb & lt));
+        if (valid && !sel) own2[e].y |= 0x80000000u;
+        nsel += __popc(__ballot_sync(0xffffffffu, sel));
+        tie_base += __popc(tb);
+      }
+      if (lane == 0) ms->scan[warp] = nsel;
+      __syncthreads();
+      int ps = 0, tot_s = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const int c = ms->scan[w];
+        ps += w < warp ? c : 0;
+        tot_s += c;
+      }
+      for (int eb = e0; eb < e1; eb += 32) {
+        const int e = eb + lane;
+        const uint32_t y = e < e1 ? own2[e].y : 0x80000000u;
+        const bool sel = (y >> 31) == 0u;
+        const uint32_t sb = __ballot_sync(0xffffffffu, sel);
+        const int at = ps + __popc(sb & lt);
+        if (sel && at < p.idx_cap) idx_s[at] = (int)y;
+        ps += __popc(sb);
+      }
+      if (tid == 0) ms->my_count = tot_s;
     } else {
       const int seg = ((nloc + NT - 1) / NT) | 1;
       const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
@@ -731,35 +820,32 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   }
 
   // idx_out / count_out: the selected tokens of every CTA, concatenated in
-  // cluster-rank (= token) order; CTA 0 pulls them once the lists are final.
+  // cluster-rank (= token) order.  Every CTA has pushed its count into every
+  // CTA's cntR (push_count) before a cluster barrier; each CTA then writes its
+  // own run at the offset the lower ranks' counts give.
+  auto push_count = [&]() {
+    if (tid < C) dsmem_st_u32(dsmem_map(smem_u32(&ms->cntR[crank]), (uint32_t)tid), (uint32_t)ms->my_count);
+  };
   auto write_idx_out = [&]() {
-    if (crank != 0) return;
-    if (p.count_out && tid == 0) p.count_out[unit] = k_eff;
+    if (crank == 0 && p.count_out && tid == 0) p.count_out[unit] = k_eff;
     if (!p.idx_out) return;
     int* io = p.idx_out + (size_t)unit * p.budget;
     if (!need_select) {
-      for (int i = tid; i < p.budget; i += NT) io[i] = (i < k_eff) ? i : -1;
+      if (crank == 0)
+        for (int i = tid; i < p.budget; i += NT) io[i] = (i < k_eff) ? i : -1;
       return;
     }
-    if (tid < C) ms->cntR[tid] = (int)dsmem_ld_u32(dsmem_map(smem_u32(&ms->my_count), (uint32_t)tid));
-    __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int r = 0; r < C; ++r) {
-        ms->offR[r] = run;
-        run += ms->cntR[r];
-      }
-      ms->ncand = run;
+    int off = 0, total = 0;
+    for (int r = 0; r < C; ++r) {
+      const int c = ms->cntR[r];
+      off += r < (int)crank ? c : 0;
+      total += c;
     }
-    __syncthreads();
-    const int total = min(ms->ncand, p.budget);
-    for (int e = tid; e < total; e += NT) {
-      int r = 0;
-      while (r + 1 < C && ms->offR[r + 1] <= e) ++r;
-      io[e] = (int)dsmem_ld_u32(dsmem_map(smem_u32(idx_s + (e - ms->offR[r])), (uint32_t)r));
-    }
-    for (int i = total + tid; i < p.budget; i += NT) io[i] = -1;
-    __syncthreads();
+    const int mine = min(ms->my_count, p.idx_cap);
+    for (int i = tid; i < mine; i += NT)
+      if (off + i < p.budget) io[off + i] = idx_s[i];
+    if (crank == (uint32_t)C - 1)
+      for (int i = total + tid; i < p.budget; i += NT) io[i] = -1;
   };
 
   // ---------------------------------------------------------------- FAC
@@ -802,12 +888,33 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
     constexpr int PSTRIDE = D + 4;
     const int ntile = (fr_n + RT - 1) / RT;
+    // Merges nrec partial records (o[0..D), m, l) per head, stored at
+    // mst[(g * nrec + r) * (D + 2)], into this CTA's record part[g].
+    auto merge_records = [&](const float* mst, int nrec) {
+      for (int x = tid; x < G * (D + 2); x += NT) {
+        const int g = x / (D + 2), e = x - g * (D + 2);
+        float M = -CUDART_INF_F;
+        for (int r = 0; r < nrec; ++r) M = fmaxf(M, mst[(g * nrec + r) * (D + 2) + D]);
+        float val = M;
+        if (e != D) {
+          float acc = 0.f;
+          for (int r = 0; r < nrec; ++r) {
+            const float* sp = mst + (g * nrec + r) * (D + 2);
+            if (sp[D] != -CUDART_INF_F) acc += exp2f(sp[D] - M) * sp[e];
+          }
+          val = acc;
+        }
+        part[g * PSTRIDE + e] = val;
+      }
+    };
     if constexpr (ES == 2) {
-      // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
-      //   QK as S^T = K Q^T  (16 rows x 8 heads per MMA; warps 0, 1 take the
-      //   two 16-row halves of a tile), PV as O^T = V^T P^T (16 head dims x 8
-      //   heads per MMA; warp w takes dims 16w..16w+15).  q and P are split
-      //   into bf16 hi + lo parts, so the products keep ~16 mantissa bits.
+      // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
+      // flash-decoding pass per warp over its own 16-row groups, no block
+      // barriers: QK as S^T = K Q^T (16 rows x 8 heads), PV as O^T = V^T P^T
+      // (16 head dims x 8 heads per MMA).  q and the softmax weights P are
+      // split into bf16 hi + lo parts, so the products keep ~16 mantissa bits.
+      // Lane (gq, tq) = (lane / 4, lane % 4) holds rows gq, gq + 8 of S^T and
+      // head dims gq, gq + 8 of O^T, for heads 2tq and 2tq + 1.
       constexpr int KS = D / 16;
       const float qs = 1.4426950408889634f * rsqrtf((float)D);
       const int gq = lane >> 2, tq = lane & 3;
@@ -821,110 +928,118 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
           const float x1 = gq < G ? qrot[gq * D + d0 + 1] * qs : 0.f;
           split_bf16(x0, x1, qb[ks][hb][0], qb[ks][hb][1]);
         }
-      float* hm = ms->hm;  // running max (log2 units) per head
-      float* hl = ms->hl;  // running sum per head
-      float* hs = ms->hs;  // rescale of the current tile per head
-      if (tid < G_MAX) {
-        hm[tid] = -CUDART_INF_F;
-        hl[tid] = 0.f;
-      }
-      float oc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int t = 0; t < ntile; ++t) {
-        cp_async_wait<FAC_STAGES - 2>();
-        __syncthreads();
-        fac_issue(t + FAC_STAGES - 1);
-        const int s = t % FAC_STAGES;
-        const uint32_t Ks = smem_u32(fac_stage + s * FAC_STAGE_B);
-        const uint32_t Vs = Ks + RT * ROWS;
-        const int rows_t = min(RT, fr_n - t * RT);
-        if (warp < 2 && warp * 16 < rows_t) {
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
-          const int mi = lane >> 3;
-          const uint32_t arow = Ks + (warp * 16 + (lane & 7) + 8 * (mi & 1)) * ROWS + 16 * (mi >> 1);
+      float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1
+      float l0 = 0.f, l1 = 0.f;                      // this lane's share of the running sums
+      float oc[KS][4];
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(arow + ks * 32, a0, a1, a2, a3);
-            mma_bf16_16816(c, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
-            mma_bf16_16816(c, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
-          }
-          const int r0 = warp * 16 + gq, r1 = r0 + 8;
-          const bool v0 = r0 < rows_t && !row_masked(t * RT + r0);
-          const bool v1 = r1 < rows_t && !row_masked(t * RT + r1);
-          const int h0 = 2 * tq, h1 = 2 * tq + 1;
-          if (h0 < G) {
-            stile[h0 * RT + r0] = v0 ? c[0] : -CUDART_INF_F;
-            stile[h0 * RT + r1] = v1 ? c[2] : -CUDART_INF_F;
-          }
-          if (h1 < G) {
-            stile[h1 * RT + r0] = v0 ? c[1] : -CUDART_INF_F;
-            stile[h1 * RT + r1] = v1 ? c[3] : -CUDART_INF_F;
-          }
-        }
-        __syncthreads();
-        // online softmax: warp g owns head g; P overwrites the logits
-        {
-          const int g = warp;
-          float p = 0.f, scale = 1.f;
-          if (g < G) {
-            const float sv = lane < rows_t ? stile[g * RT + lane] : -CUDART_INF_F;
-            const float m_old = hm[g];
-            const float m_new = fmaxf(m_old, warp_max(sv));
-            if (m_new != -CUDART_INF_F) {
-              scale = exp2f(m_old - m_new);
-              p = lane < rows_t ? exp2f(sv - m_new) : 0.f;
-            }
-            const float lsum = warp_sum(p);
-            if (lane == 0) {
-              hm[g] = m_new;
-              hl[g] = hl[g] * scale + lsum;
-            }
-          }
-          stile[g * RT + lane] = p;  // heads >= G get zero weights
-          if (lane == 0) hs[g] = scale;
-        }
-        __syncthreads();
-        if (warp < KS) {
-          const float s0 = hs[2 * tq], s1 = hs[2 * tq + 1];
-          oc[0] *= s0;
-          oc[1] *= s1;
-          oc[2] *= s0;
-          oc[3] *= s1;
-          const int mi = lane >> 3;
+      for (int mt = 0; mt < KS; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+      float* pt = stile + warp * (G_MAX * PTS);  // this warp's P tile [head][row]
+      const int mi = lane >> 3;
+      const uint32_t k_off = ((lane & 7) + 8 * (mi & 1)) * ROWS + 16 * (mi >> 1);
+      const uint32_t v_off = ((lane & 7) + 8 * (mi >> 1)) * ROWS + 16 * (mi & 1);
+      const int wst = p.fac_wst;
+      const int ngrp = (fr_n + GR - 1) / GR;
+      int it = 0;
+      for (int g = warp; g < ngrp; g += NW, ++it) {
+        const int s = wst == 2 ? (it & 1) : 0;
+        if (wst == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t Ks = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
+        const uint32_t Vs = Ks + GR * ROWS;
+        float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int kk = 0; kk < RT / 16; ++kk) {
-            if (kk * 16 < rows_t) {
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4_t(Vs + (kk * 16 + (lane & 7) + 8 * (mi >> 1)) * ROWS + (warp * 16 + 8 * (mi & 1)) * 2, a0, a1,
-                        a2, a3);
-              const float* pr = stile + gq * RT + kk * 16 + 2 * tq;
-              uint32_t b0h, b0l, b1h, b1l;
-              split_bf16(pr[0], pr[1], b0h, b0l);
-              split_bf16(pr[8], pr[9], b1h, b1l);
-              mma_bf16_16816(oc, a0, a1, a2, a3, b0h, b1h);
-              mma_bf16_16816(oc, a0, a1, a2, a3, b0l, b1l);
-            }
-          }
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(Ks + k_off + ks * 32, a0, a1, a2, a3);
+          mma_bf16_16816(sh, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
+          mma_bf16_16816(sl, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
         }
+        const int r0 = g * GR + gq, r1 = r0 + 8;
+        const bool v0 = r0 < fr_n && !row_masked(r0);
+        const bool v1 = r1 < fr_n && !row_masked(r1);
+        const float s0 = v0 ? sh[0] + sl[0] : -CUDART_INF_F, s1 = v0 ? sh[1] + sl[1] : -CUDART_INF_F;
+        const float s2 = v1 ? sh[2] + sl[2] : -CUDART_INF_F, s3 = v1 ? sh[3] + sl[3] : -CUDART_INF_F;
+        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+          x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+        }
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        // every row so far may be masked: then nothing is rescaled or added
+        const float c0 = n0 == -CUDART_INF_F ? 1.f : exp2f(m0 - n0);
+        const float c1 = n1 == -CUDART_INF_F ? 1.f : exp2f(m1 - n1);
+        const float p0 = n0 == -CUDART_INF_F ? 0.f : exp2f(s0 - n0);
+        const float p2 = n0 == -CUDART_INF_F ? 0.f : exp2f(s2 - n0);
+        const float p1 = n1 == -CUDART_INF_F ? 0.f : exp2f(s1 - n1);
+        const float p3 = n1 == -CUDART_INF_F ? 0.f : exp2f(s3 - n1);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          oc[mt][0] *= c0;
+          oc[mt][1] *= c1;
+          oc[mt][2] *= c0;
+          oc[mt][3] *= c1;
+        }
+        // P^T as the B operand: lane (gq, tq) needs head gq, rows 2tq.. --
+        // transposed through the warp's tile
+        pt[(2 * tq) * PTS + gq] = p0;
+        pt[(2 * tq + 1) * PTS + gq] = p1;
+        pt[(2 * tq) * PTS + gq + 8] = p2;
+        pt[(2 * tq + 1) * PTS + gq + 8] = p3;
+        __syncwarp();
+        const float2 pa = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq);
+        const float2 pb = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq + 8);
+        uint32_t b0h, b0l, b1h, b1l;
+        split_bf16(pa.x, pa.y, b0h, b0l);
+        split_bf16(pb.x, pb.y, b1h, b1l);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(Vs + v_off + mt * 32, a0, a1, a2, a3);
+          mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0h, b1h);
+          mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
+        }
+        __syncwarp();  // the slot and the P tile are free again
+        grp_issue(g + wst * NW, s);
       }
       cp_async_wait<0>();
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      __syncthreads();  // every warp is done with its slots: `big` takes the warp records
+      float* rec = reinterpret_cast<float*>(big);
+      const int h0 = 2 * tq, h1 = 2 * tq + 1;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int dd = mt * 16 + gq;
+        if (h0 < G) {
+          rec[(h0 * NW + warp) * (D + 2) + dd] = oc[mt][0];
+          rec[(h0 * NW + warp) * (D + 2) + dd + 8] = oc[mt][2];
+        }
+        if (h1 < G) {
+          rec[(h1 * NW + warp) * (D + 2) + dd] = oc[mt][1];
+          rec[(h1 * NW + warp) * (D + 2) + dd + 8] = oc[mt][3];
+        }
+      }
+      if (gq == 0) {
+        if (h0 < G) {
+          rec[(h0 * NW + warp) * (D + 2) + D] = m0;
+          rec[(h0 * NW + warp) * (D + 2) + D + 1] = l0;
+        }
+        if (h1 < G) {
+          rec[(h1 * NW + warp) * (D + 2) + D] = m1;
+          rec[(h1 * NW + warp) * (D + 2) + D + 1] = l1;
+        }
+      }
       __syncthreads();
-      // this CTA's partial record per head: o[0..D), m, l
-      if (warp < KS) {
-        const int dd = warp * 16 + gq;
-        if (2 * tq < G) {
-          part[(2 * tq) * PSTRIDE + dd] = oc[0];
-          part[(2 * tq) * PSTRIDE + dd + 8] = oc[2];
-        }
-        if (2 * tq + 1 < G) {
-          part[(2 * tq + 1) * PSTRIDE + dd] = oc[1];
-          part[(2 * tq + 1) * PSTRIDE + dd + 8] = oc[3];
-        }
-      }
-      if (tid < G) {
-        part[tid * PSTRIDE + D] = hm[tid];
-        part[tid * PSTRIDE + D + 1] = hl[tid];
-      }
+      merge_records(rec, NW);
     } else {
     const float qs = 1.4426950408889634f * rsqrtf((float)D);
     float qreg[G_MAX][EPL];
@@ -1005,58 +1120,53 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       }
     }
     __syncthreads();
-    for (int x = tid; x < G * (D + 2); x += NT) {
-      const int g = x / (D + 2), e = x - g * (D + 2);
-      float M = -CUDART_INF_F;
-      for (int pp = 0; pp < nparts; ++pp) M = fmaxf(M, mst[(g * nparts + pp) * (D + 2) + D]);
-      float val = M;
-      if (e != D) {
-        float acc = 0.f;
-        for (int pp = 0; pp < nparts; ++pp) {
-          const float* sp = mst + (g * nparts + pp) * (D + 2);
-          if (sp[D] != -CUDART_INF_F) acc += exp2f(sp[D] - M) * sp[e];
-        }
-        val = acc;
-      }
-      part[g * PSTRIDE + e] = val;
+    merge_records(mst, nparts);
     }
+    __syncthreads();  // part[] is complete
+
+    // Combine by push: each CTA cuts its record into the C output slices (runs
+    // of 4-element groups of the G*D outputs) and stores each slice, with
+    // (m, l) of every head and its selected count, into the shared memory of
+    // the CTA that finishes that slice.  One cluster barrier makes the stores
+    // visible; after it no CTA touches another's shared memory.
+    const int ngrp = G * (D / 4);
+    const int sl = (ngrp + C - 1) / C;
+    float4* recv_o = reinterpret_cast<float4*>(smem + p.off_recv);  // [C][sl]
+    float2* recv_ml = reinterpret_cast<float2*>(recv_o + C * sl);    // [C][G]
+    const uint32_t recv_o_l = smem_u32(recv_o), recv_ml_l = smem_u32(recv_ml);
+    for (int q = tid; q < ngrp; q += NT) {
+      const int r = ((q + 1) * C - 1) / ngrp;  // the CTA whose slice holds group q
+      const int q0r = (ngrp * r) / C;
+      const int g = q / (D / 4), e4 = q - g * (D / 4);
+      const float4 v = *reinterpret_cast<const float4*>(part + g * PSTRIDE + e4 * 4);
+      dsmem_st_v4f(dsmem_map(recv_o_l + ((int)crank * sl + q - q0r) * 16, (uint32_t)r), v.x, v.y, v.z, v.w);
     }
+    for (int x = tid; x < C * G; x += NT) {
+      const int r = x / G, g = x - r * G;
+      dsmem_st_v2f(dsmem_map(recv_ml_l + ((int)crank * G + g) * 8, (uint32_t)r), part[g * PSTRIDE + D],
+                   part[g * PSTRIDE + D + 1]);
+    }
+    if ((flags & F_IDX_OUT) && need_select) push_count();
     cluster_sync();
 
-    if (flags & F_IDX_OUT) write_idx_out();
-
-    // combine: the G*D outputs are split into C contiguous slices of
-    // 4-element groups; CTA r pulls every CTA's partial for its slice
-    const uint32_t part_l = smem_u32(part);
-    const int ngrp = G * (D / 4);
     const int q0 = (ngrp * (int)crank) / C, q1 = (ngrp * ((int)crank + 1)) / C;
-    const int g_lo = q0 / (D / 4), g_hi = q1 > q0 ? (q1 - 1) / (D / 4) : g_lo - 1;
-    // (m, l) of every CTA for the heads in the slice -> stile[(g - g_lo) * 2 * C_MAX + ...]
-    for (int x = tid; x < (g_hi - g_lo + 1) * C; x += NT) {
-      const int gg = x / C, r = x - gg * C;
-      const uint32_t a = dsmem_map(part_l + ((g_lo + gg) * PSTRIDE + D) * 4, (uint32_t)r);
-      const uint2 ml = dsmem_ld_v2(a);
-      stile[gg * 2 * C_MAX + r] = __uint_as_float(ml.x);
-      stile[gg * 2 * C_MAX + C_MAX + r] = __uint_as_float(ml.y);
-    }
-    __syncthreads();
     for (int q = q0 + tid; q < q1; q += NT) {
       const int g = q / (D / 4), e4 = q - g * (D / 4);
-      const float* ml = stile + (g - g_lo) * 2 * C_MAX;
       float M = -CUDART_INF_F;
-      for (int r = 0; r < C; ++r) M = fmaxf(M, ml[r]);
+      for (int r = 0; r < C; ++r) M = fmaxf(M, recv_ml[r * G + g].x);
       float L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -CUDART_INF_F) {
         for (int r = 0; r < C; ++r) {
-          if (ml[r] == -CUDART_INF_F) continue;
-          const float w = exp2f(ml[r] - M);
-          L += w * ml[C_MAX + r];
-          const uint4 v = dsmem_ld_v4(dsmem_map(part_l + (g * PSTRIDE + e4 * 4) * 4, (uint32_t)r));
-          acc.x = fmaf(w, __uint_as_float(v.x), acc.x);
-          acc.y = fmaf(w, __uint_as_float(v.y), acc.y);
-          acc.z = fmaf(w, __uint_as_float(v.z), acc.z);
-          acc.w = fmaf(w, __uint_as_float(v.w), acc.w);
+          const float2 ml = recv_ml[r * G + g];
+          if (ml.x == -CUDART_INF_F) continue;
+          const float w = exp2f(ml.x - M);
+          L += w * ml.y;
+          const float4 v = recv_o[r * sl + q - q0];
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
         }
       }
       if (L > 0.f) {
@@ -1068,11 +1178,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       }
       *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G + g) * D + e4 * 4) = acc;
     }
-    cluster_sync();  // the partial records stay readable until every CTA is done
-  } else if (need_select) {
-    cluster_sync();  // every CTA's list is final
     if (flags & F_IDX_OUT) write_idx_out();
-    cluster_sync();  // keep the lists readable until CTA 0 is done
+  } else if (need_select) {
+    if (flags & F_IDX_OUT) push_count();
+    cluster_sync();  // the counts are in; no CTA reads another's shared memory after this
+    if (flags & F_IDX_OUT) write_idx_out();
   } else if (flags & F_IDX_OUT) {
     write_idx_out();
   }

@@ -8,8 +8,10 @@ namespace fasa {
 
 constexpr int NT = 256;          // threads per CTA of the cluster kernel
 constexpr int NW = NT / 32;      // warps per CTA
-constexpr int RT = 32;           // FAC rows per pipeline tile
-constexpr int FAC_STAGES = 4;    // cp.async ring depth of the FAC gather
+constexpr int RT = 32;           // FAC rows per pipeline tile (fp32 path)
+constexpr int FAC_STAGES = 4;    // cp.async ring depth of the FAC gather (fp32 path)
+constexpr int GR = 16;           // FAC rows per warp group (bf16 tensor-core path)
+constexpr int PTS = 24;          // row stride (floats) of a warp's softmax-weight tile
 constexpr int G_MAX = 8;         // largest GQA group
 constexpr int C_MAX = 16;        // largest cluster
 constexpr int KDOM_BLOCK = 64;   // tokens per block of the dominant-key copy
@@ -59,8 +61,9 @@ struct Params {
   int idx_cap;              // selected-index entries per CTA
   int hpc;                  // heads combined per CTA = ceil(G / C)
   int fac_off;              // byte offset of the FAC staging ring inside the big region
+  int fac_wst;              // bf16 FAC: groups in flight per warp (1 or 2)
   int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hloc, off_hlead, off_sc, off_idx, off_own,
-      off_part, off_big, smem_total;
+      off_part, off_recv, off_big, smem_total;
 };
 
 // Kernel launchers (one translation unit per storage type).
