@@ -118,7 +118,7 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   const bool fac = (flags & (F_FAC | F_DENSE)) != 0;
   int off = 0;
   p.off_bar = off;
-  off += 64;
+  off += 64;  // mbarriers of the TIP ring
   p.off_misc = off;
   off += MISC_BYTES;
   p.off_qrot = off;
@@ -131,17 +131,19 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
   off += select ? HLOC_BINS * 4 : 0;
   p.off_hlead = off;
   off += select ? HLEAD_BINS * 4 : 0;
-  p.idx_cap = (flags & (F_SELECT | F_IDX_IN)) ? align_up(p.budget, 4) : 0;
+  // given indices (F_IDX_IN) are staged per CTA; selections live in the candidate list
+  p.idx_cap = (flags & F_IDX_IN) ? align_up(p.budget, 4) : 0;
   p.hpc = ceil_div(G, C);
   const int part_bytes = fac ? G * (D + 4) * 4 : 0;
   // pushed partial records: [C][largest slice] float4 groups, then [C][G] (m, l)
   const int ngrp4 = G * (D / 4);
   const int recv_bytes = fac ? align_up(C * ceil_div(ngrp4, C) * 16 + C * G * 8, 128) : 0;
-  // FAC staging: fp32 -- a block-wide ring of FAC_STAGES tiles of RT rows;
-  // bf16 -- per warp, wst slots of one GR-row group (two if they fit)
+  // FAC staging: fp32 -- a block-wide ring of FAC_STAGES tiles of RT padded
+  // rows; bf16 -- per warp, wst slots of one GR-row group of swizzled rows
+  // (two slots if they fit)
   auto fac_bytes = [&](int wst) {
     if (!fac) return 0;
-    return es == 2 ? wst * NW * 2 * GR * (D * es + 16) : FAC_STAGES * 2 * RT * (D * es + 16);
+    return es == 2 ? wst * NW * 2 * GR * (D * es) : FAC_STAGES * 2 * RT * (D * es + 16);
   };
 
   int s_cap = 0;
@@ -201,6 +203,10 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
       const int stage = nfc * tile * 2 * es;
       if (stages * stage > bigsz) bigsz = stages * stage;
     }
+    // the candidate list is staged in `big` (per-warp runs) before the FAC
+    // gather starts
+    if (select && bigsz < cap * 8) bigsz = align_up(cap * 8, 128);
+    p.stage_cap = bigsz / 8 / NW;
     p.tip_tile = tile;
     p.tip_stages = stages;
     p.smem_total = o + bigsz;

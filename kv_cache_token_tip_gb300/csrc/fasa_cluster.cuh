@@ -460,10 +460,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       __syncthreads();
       break;
     }
-    if (tid == 0 && it + ns < ntiles) {
-      fence_proxy_async();
-      tip_issue(it + ns);
-    }
+    // refill the stage: its generic reads all completed before the barrier
+    // above (their values are consumed), so the copy needs no proxy fence
+    if (tid == 0 && it + ns < ntiles) tip_issue(it + ns);
   }
 
   // ----------------------------------------------------- FAC row source
@@ -515,7 +514,12 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // bf16: warp w gathers and attends the GR-row groups w, w + NW, ...; slot
   // s of its p.fac_wst private slots holds one group's K rows then V rows.
   // Rows past fr_n are zero-filled.  Every call commits one cp.async group.
-  constexpr uint32_t GSLOT_B = 2u * GR * ROWS;
+  // Rows are ROWB bytes apart; 16-byte chunk c of row r sits at chunk
+  // position c ^ (r & 7), so the eight rows an ldmatrix reads fall in
+  // distinct banks.  Rows past fr_n are zero-filled (the tensor cores
+  // multiply them by zero weights, which must not meet stale NaNs).  Every
+  // call commits one cp.async group.
+  constexpr uint32_t GSLOT_B = 2u * GR * ROWB;
   auto grp_issue = [&](int g, int s) {
     if (g * GR < fr_n) {
       const uint32_t st0 = smem_u32(big) + (uint32_t)(warp * p.fac_wst + s) * GSLOT_B;
@@ -525,8 +529,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         const int i = g * GR + rr;
         const bool real = i < fr_n;
         const size_t row_off = real ? (size_t)row_token(i) * D : 0;
-        cp_async16_zfill(st0 + which * GR * ROWS + rr * ROWS + ch * 16, (which ? Vb : Kb) + row_off + ch * (16 / ES),
-                         real ? 16u : 0u);
+        cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
+                         (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
       }
     }
     cp_async_commit();
@@ -622,68 +626,64 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
       if (pass == 0) {
         // this CTA's candidates (top 12 bits >= prefix), token order, into
-        // own2 when they fit.  Warp w sweeps its contiguous share of the
-        // score vectors (float4 per lane, four in flight): the first sweep
-        // counts, the second writes at ballot-ranked positions.
+        // own2 when they fit.  One sweep: warp w scans its contiguous share
+        // of the score vectors (eight float4 loads per lane in flight; the
+        // score rows are padded to whole vectors) and appends its candidates,
+        // ranked by ballots, to its own run of a staging area in `big` (idle
+        // between the TIP ring and the FAC gather).  The runs are then copied
+        // to own2 at the offsets the warp counts give.
         const int nv = (nloc + 3) >> 2;
         const int per_w = (nv + NW - 1) / NW;
         const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
         const uint32_t lt = (1u << lane) - 1u;
+        const int stage_cap = p.stage_cap;
+        uint2* stg = reinterpret_cast<uint2*>(big) + warp * stage_cap;
         int cnt = 0;
-        for (int vb = v0; vb < v1; vb += 4 * 32) {
-          float x[4][4];
-          bool ok[4][4];
+        for (int vb = v0; vb < v1; vb += 8 * 32) {
+          float4 x[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int v = vb + u * 32 + lane;
-            load4(scr, v * 4, v < v1 ? nloc : 0, x[u], ok[u]);
+          for (int u = 0; u < 8; ++u) {
+            const int v = min(vb + u * 32 + lane, v1 - 1);
+            x[u] = *reinterpret_cast<const float4*>(scr + v * 4);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 8; ++u) {
+            const int v = vb + u * 32 + lane;
+            const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            uint32_t key[4], bal[4];
+            int excl = 0, wtot = 0;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) cnt += ok[u][t] && (score_key(x[u][t]) >> 20) >= prefix;
+            for (int t = 0; t < 4; ++t) {
+              key[t] = score_key(xs[t]);
+              bal[t] = __ballot_sync(0xffffffffu, v < v1 && v * 4 + t < nloc && (key[t] >> 20) >= prefix);
+              excl += __popc(bal[t] & lt);
+              wtot += __popc(bal[t]);
+            }
+            if (wtot == 0) continue;  // warp-uniform
+            int e = cnt + excl;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if ((bal[t] >> lane) & 1u) {
+                if (e < stage_cap) stg[e] = make_uint2(key[t], (uint32_t)(t0 + v * 4 + t));
+                ++e;
+              }
+            cnt += wtot;
+          }
         }
-        cnt = __reduce_add_sync(0xffffffffu, cnt);
         if (lane == 0) ms->scan2[warp] = cnt;
         __syncthreads();
         int before = 0, total = 0;
+        bool over = false;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const int c = ms->scan2[w];
           before += w < warp ? c : 0;
           total += c;
+          over |= c > stage_cap;
         }
-        own_list = total <= p.cand_cap;
+        own_list = !over && total <= p.cand_cap;
         if (own_list) {
-          int pos = before;
-          for (int vb = v0; vb < v1; vb += 4 * 32) {
-            float x[4][4];
-            bool ok[4][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int v = vb + u * 32 + lane;
-              load4(scr, v * 4, v < v1 ? nloc : 0, x[u], ok[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t key[4], bal[4];
-              int excl = 0, wtot = 0;
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                key[t] = score_key(x[u][t]);
-                bal[t] = __ballot_sync(0xffffffffu, ok[u][t] && (key[t] >> 20) >= prefix);
-                excl += __popc(bal[t] & lt);
-                wtot += __popc(bal[t]);
-              }
-              if (wtot == 0) continue;  // warp-uniform
-              const int tok = t0 + (vb + u * 32 + lane) * 4;
-              int e = pos + excl;
-#pragma unroll
-              for (int t = 0; t < 4; ++t)
-                if ((bal[t] >> lane) & 1u) own2[e++] = make_uint2(key[t], (uint32_t)(tok + t));
-              pos += wtot;
-            }
-          }
+          for (int i = lane; i < cnt; i += 32) own2[before + i] = stg[i];
           own_n = total;
           __syncthreads();
           if (flags & F_FAC) {
@@ -727,7 +727,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
     // Final selection of this CTA's tokens.  List mode: mask the candidates
     // that are not selected.  Scan mode: list the selected tokens now.
-    // Either way the selected tokens, in order, also go to idx_s.
+    // Either way each selected entry of own2 ends up holding its rank among
+    // this CTA's selections in .x (its key is not needed any more).
     const bool ties_mode = mode == MODE_TIES;
     auto selected = [&](uint32_t key, int tie_rank) -> bool {
       if (ties_mode) return key > prefix || (key == prefix && tie_rank < my_need);
@@ -768,13 +769,14 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         ps += w < warp ? c : 0;
         tot_s += c;
       }
+      // the rank of each selected entry among this CTA's selections replaces
+      // its key (no longer needed)
       for (int eb = e0; eb < e1; eb += 32) {
         const int e = eb + lane;
         const uint32_t y = e < e1 ? own2[e].y : 0x80000000u;
         const bool sel = (y >> 31) == 0u;
         const uint32_t sb = __ballot_sync(0xffffffffu, sel);
-        const int at = ps + __popc(sb & lt);
-        if (sel && at < p.idx_cap) idx_s[at] = (int)y;
+        if (sel) own2[e].x = (uint32_t)(ps + __popc(sb & lt));
         ps += __popc(sb);
       }
       if (tid == 0) ms->my_count = tot_s;
@@ -800,8 +802,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       for (int i = s0; i < s1; ++i) {
         const uint32_t key = score_key(scr[i]);
         if (selected(key, tr) && ps < p.cand_cap) {
-          own2[ps] = make_uint2(key, (uint32_t)(t0 + i));
-          if (ps < p.idx_cap) idx_s[ps] = t0 + i;
+          own2[ps] = make_uint2((uint32_t)ps, (uint32_t)(t0 + i));
           ++ps;
         }
         tr += ties_mode && key == prefix;
@@ -841,9 +842,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       off += r < (int)crank ? c : 0;
       total += c;
     }
-    const int mine = min(ms->my_count, p.idx_cap);
-    for (int i = tid; i < mine; i += NT)
-      if (off + i < p.budget) io[off + i] = idx_s[i];
+    for (int e = tid; e < own_n; e += NT) {
+      const uint2 en = own2[e];
+      const int at = off + (int)en.x;
+      if ((en.y >> 31) == 0u && at < p.budget) io[at] = (int)en.y;
+    }
     if (crank == (uint32_t)C - 1)
       for (int i = total + tid; i < p.budget; i += NT) io[i] = -1;
   };
@@ -934,9 +937,13 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
       float* pt = stile + warp * (G_MAX * PTS);  // this warp's P tile [head][row]
+      // ldmatrix row addresses (swizzled chunks): K as the A operand of QK --
+      // rows (lane & 7) + 8 (mi & 1), chunk 2 ks + (mi >> 1); V^T via .trans --
+      // rows (lane & 7) + 8 (mi >> 1), chunk 2 mt + (mi & 1)
       const int mi = lane >> 3;
-      const uint32_t k_off = ((lane & 7) + 8 * (mi & 1)) * ROWS + 16 * (mi >> 1);
-      const uint32_t v_off = ((lane & 7) + 8 * (mi >> 1)) * ROWS + 16 * (mi & 1);
+      const int kr = (lane & 7) + 8 * (mi & 1), vr = (lane & 7) + 8 * (mi >> 1);
+      const uint32_t k_row = kr * ROWB, v_row = vr * ROWB;
+      const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
       const int wst = p.fac_wst;
       const int ngrp = (fr_n + GR - 1) / GR;
       int it = 0;
@@ -946,12 +953,12 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         else cp_async_wait<0>();
         __syncwarp();
         const uint32_t Ks = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
-        const uint32_t Vs = Ks + GR * ROWS;
+        const uint32_t Vs = Ks + GR * ROWB;
         float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(Ks + k_off + ks * 32, a0, a1, a2, a3);
+          ldsm_x4(Ks + k_row + (((2 * ks + k_c) ^ sw) << 4), a0, a1, a2, a3);
           mma_bf16_16816(sh, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
           mma_bf16_16816(sl, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
         }
@@ -1000,7 +1007,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(Vs + v_off + mt * 32, a0, a1, a2, a3);
+          ldsm_x4_t(Vs + v_row + (((2 * mt + v_c) ^ sw) << 4), a0, a1, a2, a3);
           mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0h, b1h);
           mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
         }

@@ -15,7 +15,7 @@ constexpr int PTS = 24;          // row stride (floats) of a warp's softmax-weig
 constexpr int G_MAX = 8;         // largest GQA group
 constexpr int C_MAX = 16;        // largest cluster
 constexpr int KDOM_BLOCK = 64;   // tokens per block of the dominant-key copy
-constexpr int MISC_BYTES = 2048; // broadcast / reduction scratch in shared memory
+constexpr int MISC_BYTES = 512;  // broadcast / reduction scratch in shared memory
 // Radix digits of the 32-bit score keys: 12 + 10 + 10 bits.
 constexpr int HLOC_BINS = 4096;  // local histogram (largest digit)
 constexpr int HLEAD_BINS = 4096 + 1024 + 1024;  // cluster totals of the three digits
@@ -62,6 +62,7 @@ struct Params {
   int hpc;                  // heads combined per CTA = ceil(G / C)
   int fac_off;              // byte offset of the FAC staging ring inside the big region
   int fac_wst;              // bf16 FAC: groups in flight per warp (1 or 2)
+  int stage_cap;            // candidate-list staging entries per warp (in the big region)
   int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hloc, off_hlead, off_sc, off_idx, off_own,
       off_part, off_recv, off_big, smem_total;
 };
