@@ -203,10 +203,6 @@ int plan_smem(Params& p, const fasa_dims_t* d, int C, int flags, bool allow_ws, 
       const int stage = nfc * tile * 2 * es;
       if (stages * stage > bigsz) bigsz = stages * stage;
     }
-    // the candidate list is staged in `big` (per-warp runs) before the FAC
-    // gather starts
-    if (select && bigsz < cap * 8) bigsz = align_up(cap * 8, 128);
-    p.stage_cap = bigsz / 8 / NW;
     p.tip_tile = tile;
     p.tip_stages = stages;
     p.smem_total = o + bigsz;

@@ -51,6 +51,9 @@ struct Misc {
   int tiesR[C_MAX];
   int scan[NW];
   int scan2[NW];
+  int tip_fail;          // a TIP stage wait ran out
+  uint32_t tip_done[4];  // per TIP stage: warps done with it so far (monotonic)
+  int tip_last[4];       // per TIP stage: last tile issued into it (-1: none)
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -326,7 +329,13 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   const int nfc = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    if (flags & F_SELECT) mbar_init(smem_u32(&bars[7]), 1);  // score reload
     fence_mbar_init();
+    ms->tip_fail = 0;
+    for (int s = 0; s < 4; ++s) {
+      ms->tip_done[s] = 0u;
+      ms->tip_last[s] = -1;
+    }
   }
   if (flags & F_SELECT) {
     uint4* z = reinterpret_cast<uint4*>(hloc);
@@ -395,6 +404,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const uint32_t bar = smem_u32(&bars[s]);
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(smem_u32(big + s * stage_bytes), kd_unit + (size_t)(tau0 / KB) * nfc * KB * 2, bytes, bar);
+    ms->tip_last[s] = it;
   };
   if (tid == 0)
     for (int it = 0; it < min(ns, ntiles); ++it) tip_issue(it);
@@ -434,12 +444,24 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   cluster_wait();
 
   // ---------------------------------------------------------------- TIP scan
+  // No CTA barrier per tile: each warp counts itself done with a stage in
+  // ms->tip_done[s], and the warp whose count completes the stage refills it
+  // (every warp's reads of the stage completed before its count).  A wait
+  // that runs out stops the warp and, through ms->tip_fail, the others at
+  // their next tile.
   float* scw = (p.s_cap > 0) ? sc_s : (p.scores + (size_t)unit * p.T_max + t0);
+  int tip_fail = 0;
   for (int it = 0; it < ntiles; ++it) {
     const int s = it % ns;
     const uint32_t parity = (uint32_t)(it / ns) & 1u;
-    int fail = 0;
-    if (!mbar_wait_bounded(smem_u32(&bars[s]), parity, WAIT_LIMIT_NS)) fail = 1;
+    int stop = lane == 0 ? *reinterpret_cast<volatile int*>(&ms->tip_fail) : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) break;
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), parity, WAIT_LIMIT_NS);
+    if (!__all_sync(0xffffffffu, ok)) {
+      tip_fail = 1;
+      if (lane == 0) atomicOr(&ms->tip_fail, 1);
+      break;
+    }
     const int tau_base = it * tt;
     const int ntok = min(tt, nloc - tau_base);
     const unsigned char* st = big + s * stage_bytes;
@@ -449,20 +471,24 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       case 16: tip_tile<T, 16>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
       default: tip_tile<T, 0>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
     }
-    const int anyfail = __syncthreads_or(fail);
-    if (anyfail) {
-      if (tid == 0) {
-        atomicOr(p.status, 2);
-        // let copies still in flight land before the shared memory is released
-        for (int it2 = it + 1; it2 < min(ntiles, it + ns); ++it2)
-          mbar_wait_bounded(smem_u32(&bars[it2 % ns]), (uint32_t)(it2 / ns) & 1u, WAIT_LIMIT_NS);
-      }
-      __syncthreads();
-      break;
+    // every lane's reads of the stage have returned (their values fed the
+    // FMAs above), so no fence is needed before the count: a fence here would
+    // also wait for this warp's global score stores
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t prev = atomicAdd(&ms->tip_done[s], 1u);
+      if ((prev + 1u) % NW == 0u && it + ns < ntiles) tip_issue(it + ns);
     }
-    // refill the stage: its generic reads all completed before the barrier
-    // above (their values are consumed), so the copy needs no proxy fence
-    if (tid == 0 && it + ns < ntiles) tip_issue(it + ns);
+  }
+  if (__syncthreads_or(tip_fail | (ntiles > 0 ? ms->tip_fail : 0))) {
+    if (tid == 0) {
+      atomicOr(p.status, 2);
+      // let copies still in flight land before the shared memory is reused
+      for (int s = 0; s < ns; ++s)
+        if (ms->tip_last[s] >= 0)
+          mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, WAIT_LIMIT_NS);
+    }
+    __syncthreads();
   }
 
   // ----------------------------------------------------- FAC row source
@@ -555,8 +581,32 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   int own_n = 0;        // entries of own2
   bool own_list = false;  // own2 lists every candidate of this CTA (else: scan the scores)
   if (need_select) {
-    const float* scr = read_sc ? (p.scores_in + (size_t)unit * p.T_max + t0) : scw;
+    // Scores in global memory (the CTA's range did not fit in shared memory
+    // next to the TIP ring, or they are an input) are copied back into `big`
+    // when they fit there -- it is idle until the FAC gather -- so the list
+    // sweeps below read shared memory.  Warp w moves its own share.
+    const float* scr_g = read_sc ? (p.scores_in + (size_t)unit * p.T_max + t0) : scw;
+    const int nv = (nloc + 3) >> 2;  // score vectors (rows are padded to whole vectors)
+    const int per_w = (nv + NW - 1) / NW;
+    const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
+    const bool reload = (read_sc || p.s_cap == 0) && nv > 0 && nv * 16 <= p.smem_total - p.off_big;
+    const uint32_t rbar = smem_u32(&bars[7]);
+    if (reload) {
+      if (!read_sc) fence_proxy_async_global();  // this thread's score stores, before the copy reads them
+      __syncthreads();
+      if (lane == 0) {
+        if (warp == 0) mbar_arrive_expect_tx(rbar, (uint32_t)nv * 16u);
+        if (v1 > v0) bulk_g2s(smem_u32(big) + v0 * 16, scr_g + v0 * 4, (uint32_t)(v1 - v0) * 16u, rbar);
+      }
+    }
+    bool reload_wait = reload;
+    auto reload_done = [&]() {
+      if (reload_wait && !mbar_wait_bounded(rbar, 0u, WAIT_LIMIT_NS)) atomicOr(p.status, 2);
+      reload_wait = false;
+    };
+    const float* scr = reload ? reinterpret_cast<const float*>(big) : scr_g;
     if (read_sc) {
+      reload_done();
       for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
         float v[4];
         bool ok[4];
@@ -626,64 +676,37 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
       if (pass == 0) {
         // this CTA's candidates (top 12 bits >= prefix), token order, into
-        // own2 when they fit.  One sweep: warp w scans its contiguous share
-        // of the score vectors (eight float4 loads per lane in flight; the
-        // score rows are padded to whole vectors) and appends its candidates,
-        // ranked by ballots, to its own run of a staging area in `big` (idle
-        // between the TIP ring and the FAC gather).  The runs are then copied
-        // to own2 at the offsets the warp counts give.
-        const int nv = (nloc + 3) >> 2;
-        const int per_w = (nv + NW - 1) / NW;
-        const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
-        const uint32_t lt = (1u << lane) - 1u;
-        const int stage_cap = p.stage_cap;
-        uint2* stg = reinterpret_cast<uint2*>(big) + warp * stage_cap;
+        // own2 when they fit.  Thread t takes a contiguous run of tokens (odd
+        // length: the scalar shared-memory loads of a warp fall in distinct
+        // banks); it counts, one block scan places the runs, and it writes.
+        reload_done();
+        const int seg = ((nloc + NT - 1) / NT) | 1;
+        const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
+        const uint32_t kmin = prefix << 20;  // smallest key of the threshold bin
+        // eight loads ahead of the tests, both sweeps
+        auto keys8 = [&](int i0, uint32_t (&k)[8]) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) k[j] = i0 + j < s1 ? score_key(scr[i0 + j]) : 0u;
+        };
         int cnt = 0;
-        for (int vb = v0; vb < v1; vb += 8 * 32) {
-          float4 x[8];
+        for (int i0 = s0; i0 < s1; i0 += 8) {
+          uint32_t k[8];
+          keys8(i0, k);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int v = min(vb + u * 32 + lane, v1 - 1);
-            x[u] = *reinterpret_cast<const float4*>(scr + v * 4);
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int v = vb + u * 32 + lane;
-            const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-            uint32_t key[4], bal[4];
-            int excl = 0, wtot = 0;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              key[t] = score_key(xs[t]);
-              bal[t] = __ballot_sync(0xffffffffu, v < v1 && v * 4 + t < nloc && (key[t] >> 20) >= prefix);
-              excl += __popc(bal[t] & lt);
-              wtot += __popc(bal[t]);
-            }
-            if (wtot == 0) continue;  // warp-uniform
-            int e = cnt + excl;
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              if ((bal[t] >> lane) & 1u) {
-                if (e < stage_cap) stg[e] = make_uint2(key[t], (uint32_t)(t0 + v * 4 + t));
-                ++e;
-              }
-            cnt += wtot;
-          }
+          for (int j = 0; j < 8; ++j) cnt += (i0 + j < s1) && k[j] >= kmin;
         }
-        if (lane == 0) ms->scan2[warp] = cnt;
-        __syncthreads();
-        int before = 0, total = 0;
-        bool over = false;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const int c = ms->scan2[w];
-          before += w < warp ? c : 0;
-          total += c;
-          over |= c > stage_cap;
-        }
-        own_list = !over && total <= p.cand_cap;
+        int total;
+        const int before = block_excl_scan(cnt, ms->scan, total);
+        own_list = total <= p.cand_cap;
         if (own_list) {
-          for (int i = lane; i < cnt; i += 32) own2[before + i] = stg[i];
+          int pos = before;
+          for (int i0 = s0; i0 < s1 && pos < before + cnt; i0 += 8) {
+            uint32_t k[8];
+            keys8(i0, k);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if ((i0 + j < s1) && k[j] >= kmin) own2[pos++] = make_uint2(k[j], (uint32_t)(t0 + i0 + j));
+          }
           own_n = total;
           __syncthreads();
           if (flags & F_FAC) {

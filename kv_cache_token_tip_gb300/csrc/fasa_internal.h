@@ -62,7 +62,6 @@ struct Params {
   int hpc;                  // heads combined per CTA = ceil(G / C)
   int fac_off;              // byte offset of the FAC staging ring inside the big region
   int fac_wst;              // bf16 FAC: groups in flight per warp (1 or 2)
-  int stage_cap;            // candidate-list staging entries per warp (in the big region)
   int off_bar, off_misc, off_qrot, off_qbar, off_stile, off_hloc, off_hlead, off_sc, off_idx, off_own,
       off_part, off_recv, off_big, smem_total;
 };
