@@ -563,7 +563,21 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   };
   auto fac_start = [&]() {
     if constexpr (ES == 2) {
-      for (int s = 0; s < p.fac_wst; ++s) grp_issue(warp + s * NW, s);
+      // the first p.fac_wst groups of every warp are issued by the whole CTA
+      // (a few rows per thread instead of up to 32 per warp); the FAC loop
+      // waits for them once, CTA-wide, before it starts
+      const int nfirst = min((fr_n + GR - 1) / GR * GR, p.fac_wst * NW * GR);
+      for (int c = tid; c < nfirst * 2 * CPR; c += NT) {
+        const int i = c / (2 * CPR), rem = c - i * (2 * CPR);
+        const int which = rem >= CPR, ch = rem - which * CPR;
+        const int g = i / GR, rr = i - g * GR;  // group g: warp g % NW, slot g / NW
+        const uint32_t st0 = smem_u32(big) + (uint32_t)((g % NW) * p.fac_wst + g / NW) * GSLOT_B;
+        const bool real = i < fr_n;
+        const size_t row_off = real ? (size_t)row_token(i) * D : 0;
+        cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
+                         (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
+      }
+      cp_async_commit();
     } else {
 #pragma unroll
       for (int s = 0; s < FAC_STAGES - 1; ++s) fac_issue(s);
@@ -969,6 +983,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
       const int wst = p.fac_wst;
       const int ngrp = (fr_n + GR - 1) / GR;
+      cp_async_wait<0>();  // the CTA-wide first groups (fac_start)
+      __syncthreads();
       int it = 0;
       for (int g = warp; g < ngrp; g += NW, ++it) {
         const int s = wst == 2 ? (it & 1) : 0;
