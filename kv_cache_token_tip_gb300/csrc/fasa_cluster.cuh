@@ -41,7 +41,10 @@ namespace fasa {
 
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s for one bulk-copy wait
 
-enum : int { MODE_NONE = 0, MODE_FILL = 1, MODE_TIES = 2, MODE_CAND = 3 };
+enum : int { MODE_NONE = 0, MODE_FILL = 1, MODE_TIES = 2, MODE_CAND = 3, MODE_BX = 4 };
+// Largest threshold bucket resolved by exchanging its entries (see the
+// bucket exchange after the first radix digit).
+constexpr int BX_MAX = 512;
 
 struct Misc {
   int dstar, cnt_gt, bucket, my_count;
@@ -52,6 +55,10 @@ struct Misc {
   int scan[NW];
   int scan2[NW];
   int tip_fail;          // a TIP stage wait ran out
+  int bx_n;              // bucket entries received from the cluster (remote atomics)
+  int bx_fail;           // set remotely by a CTA without a candidate list
+  int bx_loc;            // this CTA's bucket entries
+  int bx_off[C_MAX];     // where this CTA's entries go in each CTA
   uint32_t tip_done[4];  // per TIP stage: warps done with it so far (monotonic)
   int tip_last[4];       // per TIP stage: last tile issued into it (-1: none)
 };
@@ -332,6 +339,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     if (flags & F_SELECT) mbar_init(smem_u32(&bars[7]), 1);  // score reload
     fence_mbar_init();
     ms->tip_fail = 0;
+    ms->bx_n = 0;
+    ms->bx_fail = 0;
+    ms->bx_loc = 0;
     for (int s = 0; s < 4; ++s) {
       ms->tip_done[s] = 0u;
       ms->tip_last[s] = -1;
@@ -731,6 +741,112 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
           }
         }
       }
+      if (pass == 0 && mode == MODE_NONE && bucket <= BX_MAX) {
+        // Bucket exchange: instead of more radix digits, every CTA sends the
+        // entries (key, token) of the threshold bucket to every CTA -- into
+        // hloc, idle until a later digit would zero it -- at offsets reserved
+        // with remote atomics.  After one cluster barrier each CTA ranks its
+        // own bucket entries in the whole bucket (key descending, token
+        // ascending: the stable order) and keeps those ranked below k_rem.
+        // A CTA without a candidate list vetoes it; the radix digits follow.
+        // entries travel as key << 32 | ~token: larger = earlier in the stable order
+        unsigned long long* bx_in = reinterpret_cast<unsigned long long*>(hloc);  // [bucket]
+        int* bx_own = reinterpret_cast<int*>(hloc) + 2 * BX_MAX;  // own2 indices of the own entries
+        uint32_t* bx_h = hloc + 3 * BX_MAX;                        // 1024-bin digit histogram
+        if (own_list)
+          for (int e = tid; e < own_n; e += NT)
+            if ((own2[e].x >> 20) == prefix) {
+              const int j = atomicAdd(&ms->bx_loc, 1);
+              if (j < BX_MAX) bx_own[j] = e;
+            }
+        __syncthreads();
+        const int nbo = min(ms->bx_loc, BX_MAX);
+        if (tid < C) {
+          if (!own_list) dsmem_st_u32(dsmem_map(smem_u32(&ms->bx_fail), (uint32_t)tid), 1u);
+          else if (nbo > 0)
+            ms->bx_off[tid] = (int)dsmem_atom_add_u32(dsmem_map(smem_u32(&ms->bx_n), (uint32_t)tid), (uint32_t)nbo);
+        }
+        __syncthreads();
+        if (own_list)
+          for (int x = tid; x < nbo * C; x += NT) {
+            const int j = x / C, r = x - j * C;
+            const int off = ms->bx_off[r] + j;
+            if (off < BX_MAX) {
+              const uint2 en = own2[bx_own[j]];
+              dsmem_st_v2u32(dsmem_map(smem_u32(bx_in + off), (uint32_t)r), ~en.y, en.x);
+            }
+          }
+        cluster_sync();
+        if (ms->bx_fail == 0 && ms->bx_n == bucket) {
+          auto packed = [&](int j) {
+            const uint2 en = own2[bx_own[j]];
+            return ((unsigned long long)en.x << 32) | (unsigned long long)(~en.y);
+          };
+          if (nbo * bucket <= 32 * NT) {
+            // few comparisons: rank each own entry in the bucket, one warp per
+            // entry, the lanes splitting the bucket
+            for (int j = warp; j < nbo; j += NW) {
+              const unsigned long long me = packed(j);
+              uint32_t rank = 0u;
+              for (int f0 = 0; f0 < bucket; f0 += 4 * 32) {
+                unsigned long long o[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int f = f0 + u * 32 + lane;
+                  o[u] = f < bucket ? bx_in[f] : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) rank += o[u] > me;
+              }
+              rank = __reduce_add_sync(0xffffffffu, rank);
+              if (lane == 0 && rank >= (uint32_t)k_rem) own2[bx_own[j]].y |= 0x80000000u;
+            }
+          } else {
+            // the k_rem-th largest key of the bucket from its two lower 10-bit
+            // digits (local histograms), then ties on that key by token
+            uint32_t kpre = prefix;  // key bits fixed so far (from the top)
+            int kr = k_rem, nfix = 12;
+            bool fill = false;
+            for (int dgt = 0; dgt < 2 && !fill; ++dgt) {
+              const int sh = 10 - 10 * dgt;
+              for (int i = tid; i < 1024; i += NT) bx_h[i] = 0u;
+              __syncthreads();
+              for (int f = tid; f < bucket; f += NT) {
+                const uint32_t key = (uint32_t)(bx_in[f] >> 32);
+                if ((key >> (32 - nfix)) == kpre) atomicAdd(&bx_h[(key >> sh) & 1023u], 1u);
+              }
+              __syncthreads();
+              radix_find<1024>(bx_h, kr, ms);
+              kr -= ms->cnt_gt;
+              kpre = (kpre << 10) | (uint32_t)ms->dstar;
+              nfix += 10;
+              fill = ms->bucket == kr;
+            }
+            // selected: key above the fixed bits, or equal on them and (when the
+            // last digit did not fill) among the first kr by token
+            for (int j = warp; j < nbo; j += NW) {
+              const unsigned long long me = packed(j);
+              const uint32_t kme = (uint32_t)(me >> 32) >> (32 - nfix);
+              bool keep = kme > kpre;
+              if (kme == kpre) {
+                if (fill) {
+                  keep = true;
+                } else {
+                  uint32_t before = 0u;  // entries with the same key, earlier tokens
+                  for (int f = lane; f < bucket; f += 32) {
+                    const unsigned long long o = bx_in[f];
+                    before += ((uint32_t)(o >> 32) == (uint32_t)(me >> 32)) && o > me;
+                  }
+                  keep = __reduce_add_sync(0xffffffffu, before) < (uint32_t)kr;
+                }
+              }
+              if (lane == 0 && !keep) own2[bx_own[j]].y |= 0x80000000u;
+            }
+          }
+          mode = MODE_BX;
+        }
+        __syncthreads();
+      }
       if (mode != MODE_NONE) break;
     }
 
@@ -767,7 +883,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     // Either way each selected entry of own2 ends up holding its rank among
     // this CTA's selections in .x (its key is not needed any more).
     const bool ties_mode = mode == MODE_TIES;
-    auto selected = [&](uint32_t key, int tie_rank) -> bool {
+    // (the bucket exchange already masked the list entries it drops)
+    auto selected = [&](uint32_t key, int tie_rank, uint32_t y) -> bool {
+      if (mode == MODE_BX) return (y >> 31) == 0u;
       if (ties_mode) return key > prefix || (key == prefix && tie_rank < my_need);
       return (key >> shift) >= prefix;
     };
@@ -792,7 +910,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         const bool valid = e < e1;
         const uint32_t key = valid ? own2[e].x : 0u;
         const uint32_t tb = __ballot_sync(0xffffffffu, valid && ties_mode && key == prefix);
-        const bool sel = valid && selected(key, tie_base + __popc(tb & lt));
+        const bool sel = valid && selected(key, tie_base + __popc(tb & lt), own2[e].y);
         if (valid && !sel) own2[e].y |= 0x80000000u;
         nsel += __popc(__ballot_sync(0xffffffffu, sel));
         tie_base += __popc(tb);
@@ -830,7 +948,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         int trr = tr;
         for (int i = s0; i < s1; ++i) {
           const uint32_t key = score_key(scr[i]);
-          cs += selected(key, trr);
+          cs += selected(key, trr, 0u);
           trr += ties_mode && key == prefix;
         }
       }
@@ -838,7 +956,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       int ps = block_excl_scan(cs, ms->scan, tot_s);
       for (int i = s0; i < s1; ++i) {
         const uint32_t key = score_key(scr[i]);
-        if (selected(key, tr) && ps < p.cand_cap) {
+        if (selected(key, tr, 0u) && ps < p.cand_cap) {
           own2[ps] = make_uint2((uint32_t)ps, (uint32_t)(t0 + i));
           ++ps;
         }
