@@ -301,6 +301,8 @@ def run_gpu(args):
     per_step = model["total"]
     R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
     R = min(R, 64)
+    if args.replicas > 0:  # profiling runs only: fewer replicas may fit in L2
+        R = args.replicas
     reps = make_replicas(cfg, R, dims)
     B, Hq, H, d, k = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.budget
     ws_bytes = fasa_workspace_size(dims, k)
@@ -437,7 +439,8 @@ def run_gpu(args):
             "config": {"workload": cfg.name, "batch": B, "q_heads": Hq, "kv_heads": H, "head_dim": d,
                        "context": cfg.context, "n_tip": cfg.n_tip, "budget": k, "rope_theta": cfg.rope_theta,
                        "cluster_ctas": C, "replicas": R,
-                       "l2": f"inputs larger than L2: {R} replicas x {per_step / 1e6:.2f} MB/step "
+                       "l2": f"{'inputs larger than L2' if R * per_step > L2_BYTES else 'NOT larger than L2 (profiling run)'}: "
+                             f"{R} replicas x {per_step / 1e6:.2f} MB/step "
                              f"rotate ({R * per_step / L2_BYTES:.1f}x L2)",
                        "launch": "CUDA graph of fasa_decode_step launches, one kernel per step",
                        "parallelism": f"replicas x{world}"},
@@ -502,6 +505,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="input replicas rotated through (0: enough to exceed 4x L2, as timing requires; "
+                         "a smaller count is for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
