@@ -889,7 +889,13 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       if (ties_mode) return key > prefix || (key == prefix && tie_rank < my_need);
       return (key >> shift) >= prefix;
     };
-    if (own_list) {
+    // After the bucket exchange the list is already masked, and after a
+    // bucket filled at the first digit every list entry is selected: the
+    // sweeps below then only rank the selections for idx_out.
+    const bool list_final = mode == MODE_BX || (mode == MODE_FILL && shift == dig_shift(0));
+    if (own_list && list_final && !(flags & F_IDX_OUT)) {
+      // nothing to do
+    } else if (own_list) {
       // warp w takes a contiguous share of the list; ranks within a warp
       // come from ballots, across warps from per-warp totals
       const uint32_t lt = (1u << lane) - 1u;

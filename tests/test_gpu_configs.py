@@ -106,3 +106,27 @@ def test_dense_full_size_sample():
         ref = oracle_unit(L, 0, h, cfg.budget)
         dense = O.focused_attention_unit(ref["q_rot"], ref["K"], ref["V"], np.arange(cfg.context))
         P.check_output(o[0, 4 * h:4 * h + 4], dense, "bf16")
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_ctx32k", "qwen25_7b_b8_ctx16k", "llama3_8b_b4_ctx128k"])
+def test_step_without_index_output(name):
+    """The step as the benchmark times it -- no idx_out / count_out -- gives
+    bit for bit the output of the step that also writes the indices (whose
+    selection and output the full-workload test checks against the oracle);
+    a sample of units is checked against the oracle directly."""
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for, fasa_decode_step, fasa_device_status, fasa_workspace_size
+    cfg = configs.CONFIGS[name]
+    L = gpu_gen.make_layer(cfg, 0)
+    dims = dims_for(cfg)
+    o_idx, ix, cn, _ = _run_step(L, cfg, dims)
+    kd = build_kdom(L, dims)
+    ws_bytes = fasa_workspace_size(dims, cfg.budget)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, ws, dims)
+    assert fasa_device_status() == 0
+    o = out.cpu().numpy()
+    assert np.array_equal(o, o_idx)
+    for (b, h) in [(0, 0), (cfg.batch - 1, cfg.n_kv_heads - 1)]:
+        _check_unit(L, cfg, o, ix, cn, b, h)
