@@ -706,30 +706,38 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         reload_done();
         const int seg = ((nloc + NT - 1) / NT) | 1;
         const int s0 = min(nloc, tid * seg), s1 = min(nloc, s0 + seg);
-        const uint32_t kmin = prefix << 20;  // smallest key of the threshold bin
+        // A score is a candidate iff its key is at least the smallest key of
+        // the threshold bin, i.e. iff the score is at least that key's float
+        // (keys order floats, with -0 = +0); bins below 8 start at -inf or
+        // at NaN patterns, where -inf is the bound.
+        const uint32_t kmin = prefix << 20;
+        const float fmin = prefix >= 8u ? __uint_as_float((kmin & 0x80000000u) ? (kmin & 0x7FFFFFFFu) : ~kmin)
+                                        : -CUDART_INF_F;
         // eight loads ahead of the tests, both sweeps
-        auto keys8 = [&](int i0, uint32_t (&k)[8]) {
+        auto scores8 = [&](int i0, float (&x)[8]) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) k[j] = i0 + j < s1 ? score_key(scr[i0 + j]) : 0u;
+          for (int j = 0; j < 8; ++j) x[j] = i0 + j < s1 ? scr[i0 + j] : -CUDART_INF_F;
         };
         int cnt = 0;
         for (int i0 = s0; i0 < s1; i0 += 8) {
-          uint32_t k[8];
-          keys8(i0, k);
+          float x[8];
+          scores8(i0, x);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) cnt += (i0 + j < s1) && k[j] >= kmin;
+          for (int j = 0; j < 8; ++j) cnt += (i0 + j < s1) && x[j] >= fmin;
         }
         int total;
         const int before = block_excl_scan(cnt, ms->scan, total);
         own_list = total <= p.cand_cap;
         if (own_list) {
+          // no early exit: the loads of a batch do not wait for the stores
+          // of the one before
           int pos = before;
-          for (int i0 = s0; i0 < s1 && pos < before + cnt; i0 += 8) {
-            uint32_t k[8];
-            keys8(i0, k);
+          for (int i0 = s0; i0 < s1; i0 += 8) {
+            float x[8];
+            scores8(i0, x);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              if ((i0 + j < s1) && k[j] >= kmin) own2[pos++] = make_uint2(k[j], (uint32_t)(t0 + i0 + j));
+              if ((i0 + j < s1) && x[j] >= fmin) own2[pos++] = make_uint2(score_key(x[j]), (uint32_t)(t0 + i0 + j));
           }
           own_n = total;
           __syncthreads();
