@@ -298,9 +298,13 @@ def run_gpu(args):
     dims = dims_for(cfg)
     lens = synth.seq_lens(cfg)
     model = algorithmic_bytes(cfg, lens)
-    per_step = model["total"]
-    R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
-    R = min(R, 64)
+    layers = cfg.layers          # a decode step runs every layer: one launch each
+    per_step = model["total"] * layers
+    if layers > 1:
+        R = layers               # one replica per layer, launched in order
+    else:
+        R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
+        R = min(R, 64)
     if args.replicas > 0:  # profiling runs only: fewer replicas may fit in L2
         R = args.replicas
     reps = make_replicas(cfg, R, dims)
@@ -331,10 +335,11 @@ def run_gpu(args):
     torch.cuda.synchronize()
     chunk = R * max(1, 512 // R)
     K, W = args.steps, args.warmup
+    KL = K * layers              # timed launches
     g_chunk = capture(step, chunk, stream)
-    rem = K % chunk
+    rem = KL % chunk
     g_rem = capture(step, rem, stream) if rem else None
-    g_warm = capture(step, W, stream) if W else None
+    g_warm = capture(step, W * layers, stream) if W else None
     torch.cuda.synchronize()
     if g_warm is not None:
         with torch.cuda.stream(stream):
@@ -350,7 +355,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):   # graphs replay on the current stream
             ev0.record(stream)
-            for _ in range(K // chunk):
+            for _ in range(KL // chunk):
                 g_chunk.replay()
             if g_rem is not None:
                 g_rem.replay()
@@ -373,7 +378,7 @@ def run_gpu(args):
         g_dense.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    dense_sec = e0.elapsed_time(e1) / 1e3 / Kd
+    dense_sec = e0.elapsed_time(e1) / 1e3 / Kd * layers   # per decode step
 
     # end to end through the public API: every step copies that step's q, pos
     # and lens from pinned host memory (one packed copy), runs
@@ -420,7 +425,8 @@ def run_gpu(args):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(E):
-            graphs[i % R].replay()
+            for l in range(layers):
+                graphs[(i * layers + l) % R].replay()
             stream.synchronize()
     e2e_sec = max_over_ranks(pg, time.perf_counter() - t0)
     e2e_per_step = e2e_sec / E
@@ -428,10 +434,12 @@ def run_gpu(args):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(E):
-            e2e_step(i % R)
+            for l in range(layers):
+                e2e_step((i * layers + l) % R)
             stream.synchronize()
     e2e_eager_per_step = max_over_ranks(pg, time.perf_counter() - t0) / E
-    if not torch.equal(h_out[(E - 1) % R], outs[(E - 1) % R].cpu()):
+    last = ((E - 1) * layers + layers - 1) % R
+    if not torch.equal(h_out[last], outs[last].cpu()):
         raise RuntimeError("end-to-end output copy does not match the device output")
     status = fasa_device_status(stream)
     if status:
@@ -447,12 +455,12 @@ def run_gpu(args):
         cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
                "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s "
                          f"(host-generated inputs, numpy fp64, 1 BLAS thread); "
-                         f"{cb['seconds'] / cb['steps'] * B * H * 1e6:.0f} us per whole decode step"}
+                         f"{cb['seconds'] / cb['steps'] * B * H * layers * 1e6:.0f} us per whole decode step"}
     else:
         cpu = None
     if rank == 0:
-        h2d = int(nbytes)
-        d2h = int(h_out[0].numel() * 4)
+        h2d = int(nbytes) * layers
+        d2h = int(h_out[0].numel() * 4) * layers
         line = {
             "metric": METRIC,
             "value": round(world * per_step / sec_per_step / 1e12, 4),
@@ -472,15 +480,19 @@ def run_gpu(args):
                        "l2": f"{'inputs larger than L2' if R * per_step > L2_BYTES else 'NOT larger than L2 (profiling run)'}: "
                              f"{R} replicas x {per_step / 1e6:.2f} MB/step "
                              f"rotate ({R * per_step / L2_BYTES:.1f}x L2)",
-                       "launch": "CUDA graph of fasa_decode_step launches, one kernel per step",
+                       "launch": ("CUDA graph of fasa_decode_step launches, one kernel per step"
+                                  if layers == 1 else
+                                  f"CUDA graph of fasa_decode_step launches, one kernel per layer, "
+                                  f"{layers} layers per step"),
+                       "layers": layers,
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": per_step,
-            "bytes_breakdown": {kk: model[kk] for kk in ("tip", "fac", "q", "out", "small")},
+            "bytes_breakdown": {kk: model[kk] * layers for kk in ("tip", "fac", "q", "out", "small")},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),
-                         "peak_kind": peak_kind, "kernel": "fasa_cluster_kernel<bf16,128>"},
+                         "peak_kind": peak_kind, "kernel": f"fasa_cluster_kernel<{cfg.dtype},{cfg.head_dim}>"},
             "dense": {"us_per_step": round(dense_sec * 1e6, 3),
-                      "achieved_gbs": round(model["dense_total"] / dense_sec / 1e9, 1),
+                      "achieved_gbs": round(model["dense_total"] * layers / dense_sec / 1e9, 1),
                       "sparse_vs_dense_speedup": round(dense_sec / sec_per_step, 3)},
             "e2e": {"value": round(world * per_step / e2e_per_step / 1e12, 4), "unit": "TB/s",
                     "us_per_step": round(e2e_per_step * 1e6, 3),
@@ -488,7 +500,7 @@ def run_gpu(args):
                     "mode": "CUDA graph per step: pinned H2D copy of q/pos/lens, fasa_decode_step, D2H copy of "
                             "out; host sync every step",
                     "eager_us_per_step": round(e2e_eager_per_step * 1e6, 3)},
-            "gpu_launches": K,
+            "gpu_launches": K * layers,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
