@@ -190,8 +190,11 @@ int fasa_decode_step(const void* q, const int32_t* pos,
  * workspace it uses a fixed array of FASA_NOALLOC_SCRATCH_BYTES inside the
  * library image instead (reserved on every GPU that loads the library until
  * the process exits).  Nothing is allocated or freed.
- *  - Returns FASA_ERR_WORKSPACE when the step would need more scratch than
- *    FASA_NOALLOC_SCRATCH_BYTES (B * Hkv * T_max * 4 bytes).
+ *  - When the automatic plan (dims->reserved == 0) needs more scratch than
+ *    FASA_NOALLOC_SCRATCH_BYTES, cluster sizes 2, 4, 8, 16 are tried in turn
+ *    (finer token ranges need less workspace) and the first that fits runs.
+ *  - Returns FASA_ERR_WORKSPACE when no plan fits the scratch (a plan that
+ *    needs a workspace needs B * Hkv * T_max * 4 bytes).
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.

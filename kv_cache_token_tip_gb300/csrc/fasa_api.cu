@@ -255,7 +255,8 @@ void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
 // Plans and launches the cluster kernel.  Cluster size: the explicit
 // override (dims->reserved), else the largest C (at most 16) for which every
 // unit's cluster is resident at once (one wave); when no C gives one wave,
-// the largest C <= 4 that can be launched.
+// the smallest C that can be launched for a step with a top-k, else the
+// largest C <= 4.
 int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t ws_bytes, bool launch,
                     size_t* ws_need, int* C_out, cudaStream_t stream) {
   DevInfo di;
@@ -276,7 +277,13 @@ int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t
       if (plan_smem(p, d, c, flags, true, &need, di.smem_optin) != FASA_OK) continue;
       if (cluster_capacity(flags, d->dtype, d->head_dim, c, p.smem_total) >= units) C = c;
     }
-    for (int c = 4; c >= 1 && !C; --c) {
+    // Several waves either way.  With a top-k: the fewest CTAs per unit (a
+    // larger cluster only repeats the per-CTA fixed costs of the selection).
+    // Without (dense or given indices: pure streaming): the largest C <= 4,
+    // whose finer work units balance the waves.
+    const bool sel = (flags & F_SELECT) != 0;
+    for (int i = 0; i < 4 && !C; ++i) {
+      const int c = sel ? 1 + i : 4 - i;
       if (plan_smem(p, d, c, flags, true, &need, di.smem_optin) != FASA_OK) continue;
       if (cluster_capacity(flags, d->dtype, d->head_dim, c, p.smem_total) >= 1) C = c;
     }

@@ -55,6 +55,23 @@ extern "C" int fasa_decode_step_noalloc(const void* q, const int32_t* pos, const
   size_t need = 0;
   int st = fasa_workspace_size(dims, budget, &need);
   if (st != FASA_OK) return st;
+  // When the automatic plan's workspace exceeds the scratch array, larger
+  // clusters split each unit's tokens finer and need less (none once every
+  // CTA's scores fit in shared memory); the first that fits is used.
+  fasa_dims_t forced;
+  if (need > FASA_NOALLOC_SCRATCH_BYTES && dims->reserved == 0) {
+    forced = *dims;
+    const int sizes[4] = {2, 4, 8, 16};
+    for (int i = 0; i < 4; ++i) {
+      forced.reserved = sizes[i];
+      size_t n2 = 0;
+      if (fasa_workspace_size(&forced, budget, &n2) == FASA_OK && n2 <= FASA_NOALLOC_SCRATCH_BYTES) {
+        dims = &forced;
+        need = n2;
+        break;
+      }
+    }
+  }
   if (need == 0)  // everything fits in shared memory: no scratch at all
     return fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget, out, idx_out, count_out,
                             nullptr, 0, dims, stream);

@@ -64,3 +64,31 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     st = lib().fasa_decode_step_noalloc(P_, P_, P_, P_, P_, P_, P_, cfg.budget, P_, None, None,
                                         ctypes.byref(dims), None)
     assert st == 3   # FASA_ERR_WORKSPACE, before any launch
+
+
+def test_noalloc_falls_back_to_a_cluster_size_that_fits():
+    """One layer of the 32-sequence ragged batch: the automatic plan (one CTA
+    per unit, 32K-token ranges) needs a 32 MiB score workspace, more than the
+    scratch; the no-alloc entry point runs a larger cluster instead, with the
+    result of the workspace entry point forced to that cluster size."""
+    import torch
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_cluster_size, fasa_decode_step, fasa_decode_step_noalloc,
+                                          fasa_device_status, fasa_workspace_size)
+    cfg = configs.CONFIGS["mistral_7b_l32_b32_ragged"]
+    auto = dims_for(cfg)
+    assert fasa_workspace_size(auto, cfg.budget) > (16 << 20)
+    sizes = [c for c in (2, 4, 8, 16) if fasa_workspace_size(dims_for(cfg, cluster_ctas=c), cfg.budget) <= (16 << 20)]
+    assert sizes
+    forced = dims_for(cfg, cluster_ctas=sizes[0])
+    assert fasa_cluster_size(forced) == sizes[0]
+    L = gpu_gen.make_layer(cfg, 0)
+    kd = build_kdom(L, forced)
+    shape_o = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    ws_bytes = fasa_workspace_size(forced, cfg.budget)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    out_ref = torch.empty(shape_o, dtype=torch.float32, device="cuda")
+    fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out_ref, None, None, ws, forced)
+    out = torch.full(shape_o, float("nan"), dtype=torch.float32, device="cuda")
+    fasa_decode_step_noalloc(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, auto)
+    assert fasa_device_status() == 0
+    assert np.array_equal(out.cpu().numpy(), out_ref.cpu().numpy())
