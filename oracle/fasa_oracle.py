@@ -43,7 +43,8 @@ __all__ = [
     "decode_stored", "fc_frequencies", "rope_rotate", "apply_rope_q",
     "fc_score", "tip_scores_unit", "topk_select_unit", "focused_attention_unit",
     "tip_score", "topk_select", "focused_attention", "dense_attention",
-    "decode_step", "build_kdom", "bytes_fraction", "theoretical_speedup",
+    "decode_step", "append_token", "decode_step_append", "build_kdom", "bytes_fraction",
+    "theoretical_speedup",
 ]
 
 
@@ -239,6 +240,30 @@ def decode_step(q, pos, K, V, dom_fc, seq_lens, k, rope_theta):
     idx, count = topk_select(scores, seq_lens, k)
     out = focused_attention(q_rot, K, V, idx, count)
     return out, idx, count, scores
+
+
+def append_token(K, V, k_new, v_new, seq_lens, rope_theta):
+    """The new token of a decode step enters the cache: its key, rotated by
+    its own position len_b (keys are cached post-RoPE), and its value go to
+    index len_b.  K/V [B,Hkv,T,d] fp64 (copied), k_new/v_new [B,Hkv,d] fp64
+    (k_new pre-RoPE).  Returns (K', V', seq_lens + 1)."""
+    K = np.array(K, dtype=np.float64, copy=True)
+    V = np.array(V, dtype=np.float64, copy=True)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    for b in range(K.shape[0]):
+        t = int(lens[b])
+        K[b, :, t, :] = rope_rotate(np.asarray(k_new[b], dtype=np.float64), t, rope_theta)
+        V[b, :, t, :] = np.asarray(v_new[b], dtype=np.float64)
+    return K, V, lens + 1
+
+
+def decode_step_append(q, k_new, v_new, K, V, dom_fc, seq_lens, k, rope_theta):
+    """A decode step that first appends the new token (``append_token``) and
+    then attends over len_b + 1 tokens with the query at position len_b, the
+    new token's own position.  Returns decode_step's tuple plus (K', V')."""
+    K2, V2, lens2 = append_token(K, V, k_new, v_new, seq_lens, rope_theta)
+    res = decode_step(q, np.asarray(seq_lens), K2, V2, dom_fc, lens2, k, rope_theta)
+    return res + (K2, V2)
 
 
 def build_kdom(K_stored: np.ndarray, dom_fc: np.ndarray, block: int = 64) -> np.ndarray:

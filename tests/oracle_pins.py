@@ -339,4 +339,76 @@ def check_byte_model(o):
     assert abs(c["t"] / c["budget"] - c["fac_ratio_approx"]) / c["fac_ratio_approx"] <= c["rel_tol"]
 
 
+# --- NEXT-1: appending the step's own token ---------------------------------
+def check_append_same_position_dot(o):
+    """The new key is rotated by its own position, which is also the query's
+    position: R_m^T R_m = I makes every FC's rotated dot q'.k' equal the
+    pre-RoPE dot q.k."""
+    rng = _rng(41)
+    B, Hkv, T, d = 2, 2, 12, 8
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = rng.standard_normal((B, Hkv, T, d))
+    k_new = rng.standard_normal((B, Hkv, d))
+    v_new = rng.standard_normal((B, Hkv, d))
+    q = rng.standard_normal((B, Hkv, d))          # one query head per KV head
+    lens = np.array([5, 11])
+    K2, V2, lens2 = o.append_token(K, V, k_new, v_new, lens, 1e4)
+    assert np.array_equal(lens2, lens + 1)
+    qr = o.apply_rope_q(q, lens, 1e4)
+    for b in range(B):
+        t = lens[b]
+        for h in range(Hkv):
+            for i in range(d // 2):
+                lhs = qr[b, h, 2 * i] * K2[b, h, t, 2 * i] + qr[b, h, 2 * i + 1] * K2[b, h, t, 2 * i + 1]
+                rhs = q[b, h, 2 * i] * k_new[b, h, 2 * i] + q[b, h, 2 * i + 1] * k_new[b, h, 2 * i + 1]
+                assert abs(lhs - rhs) <= 1e-12 * (1 + abs(rhs))
+        assert np.array_equal(V2[b, :, t], v_new[b])
+        keep = np.ones(T, dtype=bool)
+        keep[t] = False
+        assert np.array_equal(K2[b][:, keep], K[b][:, keep]) and np.array_equal(V2[b][:, keep], V[b][:, keep])
+
+
+def check_append_empty_cache(o):
+    """With an empty cache the step attends over its own token only: every
+    query head's output is its KV head's new value."""
+    rng = _rng(42)
+    B, Hkv, G, T, d = 2, 2, 3, 4, 8
+    K = np.zeros((B, Hkv, T, d))
+    V = np.zeros((B, Hkv, T, d))
+    q = rng.standard_normal((B, Hkv * G, d))
+    k_new = rng.standard_normal((B, Hkv, d))
+    v_new = rng.standard_normal((B, Hkv, d))
+    dom = np.array([[0, 2], [1, 3]])
+    out, idx, cnt, _, _, _ = o.decode_step_append(q, k_new, v_new, K, V, dom, np.array([0, 0]), 4, 1e4)
+    assert np.all(cnt == 1) and np.all(idx[:, :, 0] == 0)
+    for b in range(B):
+        for hq in range(Hkv * G):
+            assert np.allclose(out[b, hq], v_new[b, hq // G], atol=1e-14)
+
+
+def check_append_equals_cached_token(o):
+    """Appending equals a plain step over a cache that already holds the
+    token, its key rotated here by the complex-exponential closed form
+    (x0 + i x1) e^{i t theta_j}."""
+    rng = _rng(43)
+    B, Hkv, G, T, d, theta = 1, 2, 2, 20, 8, 1e4
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = rng.standard_normal((B, Hkv, T, d))
+    q = rng.standard_normal((B, Hkv * G, d))
+    k_new = rng.standard_normal((B, Hkv, d))
+    v_new = rng.standard_normal((B, Hkv, d))
+    dom = np.array([[0, 3], [1, 2]])
+    lens = np.array([13])
+    out, idx, cnt, sc, _, _ = o.decode_step_append(q, k_new, v_new, K, V, dom, lens, 6, theta)
+    Kc, Vc = K.copy(), V.copy()
+    t = int(lens[0])
+    for h in range(Hkv):
+        z = (k_new[0, h, 0::2] + 1j * k_new[0, h, 1::2]) * np.exp(1j * t * theta ** (-np.arange(d // 2) * 2.0 / d))
+        Kc[0, h, t, 0::2], Kc[0, h, t, 1::2] = z.real, z.imag
+        Vc[0, h, t] = v_new[0, h]
+    out2, idx2, cnt2, _ = o.decode_step(q, lens, Kc, Vc, dom, lens + 1, 6, theta)
+    assert np.array_equal(idx, idx2) and np.array_equal(cnt, cnt2)
+    assert np.allclose(out, out2, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -101,6 +101,17 @@ def _focused_attention_wrong_group(q_rot, K, V, idx, count):
     return out
 
 
+def _append_one_position_late(K, V, k_new, v_new, seq_lens, rope_theta):
+    K = np.array(K, dtype=np.float64, copy=True)
+    V = np.array(V, dtype=np.float64, copy=True)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    for b in range(K.shape[0]):
+        t = int(lens[b])
+        K[b, :, t, :] = O.rope_rotate(np.asarray(k_new[b], dtype=np.float64), t + 1, rope_theta)
+        V[b, :, t, :] = np.asarray(v_new[b], dtype=np.float64)
+    return K, V, lens + 1
+
+
 MUTATIONS = {
     "rope_row_vector_sign": ("rope_rotate", _rope_row_convention),
     "rope_rotate_half_pairing": ("rope_rotate", _rope_rotate_half),
@@ -110,6 +121,7 @@ MUTATIONS = {
     "theta_exponent_halved": ("fc_frequencies", _freq_half_exponent),
     "kdom_splits_fc_pair": ("build_kdom", _kdom_wrong_pair),
     "gqa_modulo_mapping": ("focused_attention", _focused_attention_wrong_group),
+    "append_rotates_one_position_late": ("append_token", _append_one_position_late),
 }
 
 
