@@ -178,6 +178,29 @@ int fasa_decode_step(const void* q, const int32_t* pos,
                      const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
+ * fasa_decode_step with the new token's cache maintenance fused in (the
+ * FASA pages, "Hardware-Aware Variants": FASA-C keeps the dominant key cache
+ * alongside the KV cache, so each decode step adds its own token to both).
+ * For every sequence b, with t = seq_lens[b] (lengths BEFORE the step,
+ * t < T_max):
+ *  - k_new [B,Hkv,d] (pre-RoPE, stored dtype) is rotated by position t and
+ *    written to k_cache[b,h,t,:]; v_new [B,Hkv,d] to v_cache[b,h,t,:]; the
+ *    rotated key's dominant FCs to k_dom (the layout of fasa_build_kdom);
+ *  - then the step runs over the t + 1 tokens 0..t with the query q at
+ *    position t (the new token's own position).
+ * seq_lens is read, not written: the caller advances it after the step.
+ * Device-side errors (t >= T_max: nothing appended) set FASA_DEV_BAD_INPUT.
+ * Same workspace and output conventions as fasa_decode_step; k_new / v_new
+ * need only their element alignment.
+ */
+int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
+                            const int32_t* seq_lens, void* k_cache, void* v_cache, void* k_dom,
+                            const int32_t* dom_fc, int32_t budget,
+                            float* out, int32_t* idx_out, int32_t* count_out,
+                            void* workspace, size_t workspace_bytes,
+                            const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
  * Size of the fixed device scratch array used by fasa_decode_step_noalloc:
  * 16 MiB, i.e. scores for B * Hkv * T_max <= 4194304 cached tokens.
  */

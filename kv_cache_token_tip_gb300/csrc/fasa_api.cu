@@ -636,6 +636,35 @@ int fasa_decode_step(const void* q, const int32_t* pos, const void* k_cache, con
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new, const int32_t* seq_lens,
+                            void* k_cache, void* v_cache, void* k_dom, const int32_t* dom_fc, int32_t budget,
+                            float* out, int32_t* idx_out, int32_t* count_out, void* workspace,
+                            size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
+    return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.q = q;
+  p.pos = seq_lens;  // the query sits at the new token's position, len
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_dom = k_dom;
+  p.dom_fc = dom_fc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.idx_out = idx_out;
+  p.count_out = count_out;
+  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC | F_APPEND;
+  if (idx_out || count_out) flags |= F_IDX_OUT;
+  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 int fasa_device_status(fasa_stream_t stream, int32_t* status) {
   if (!status) return FASA_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

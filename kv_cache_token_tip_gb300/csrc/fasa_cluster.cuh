@@ -295,7 +295,7 @@ __device__ __forceinline__ void tip_tile(const unsigned char* st, int ntok, int 
 enum : int { KIND_STEP = 0, KIND_DENSE = 1, KIND_STAGE = 2 };
 
 __host__ __device__ constexpr int kind_flags(int kind, int flags) {
-  return kind == KIND_STEP ? (flags & (F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT))
+  return kind == KIND_STEP ? (flags & (F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT | F_APPEND))
          : kind == KIND_DENSE ? F_DENSE
                               : flags;
 }
@@ -362,7 +362,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // (and go out before the bulk TIP traffic)
   bool bad = false;
   int len = p.seq_lens[b];
-  const int m_pos = (flags & F_ROPE) ? p.pos[b] : 0;
+  // with F_APPEND the query sits at the new token's position, len
+  const int m_pos = (flags & F_ROPE) ? ((flags & F_APPEND) ? len : p.pos[b]) : 0;
   const int dom_i = (tid < p.n_tip && (flags & F_TIP)) ? p.dom_fc[h * p.n_tip + tid] : 0;
   constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;  // query pairs per thread
   float2 qv[QPAIRS];
@@ -386,6 +387,18 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     len = min(max(len, 0), p.T_max);
   }
 
+  // F_APPEND: the step's own token goes to index t_new = len and is attended
+  // with the others (a full cache cannot take it: reported, not appended)
+  int t_new = -1;
+  if (flags & F_APPEND) {
+    if (len < p.T_max) {
+      t_new = len;
+      len += 1;
+    } else {
+      bad = true;
+    }
+  }
+
   const int k_eff = min(p.budget, len);
   const bool sel_flag = (flags & F_SELECT) != 0;
   const bool need_select = sel_flag && len > p.budget;
@@ -397,9 +410,14 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   const int t0 = min(len, (int)crank * chunk);
   const int t1 = min(len, t0 + chunk);
   const int nloc = t1 - t0;
+  // K_dom is streamed up to the new token, which this CTA (if it owns it)
+  // scores from registers
+  const bool own_new = t_new >= t0 && t_new < t1;
+  const int t1s = own_new ? t_new : t1;
+  const int nloc_s = t1s - t0;
 
   // ---------------------------------------------------------------- TIP loads
-  const int ntiles = do_tip ? (nloc + tt - 1) / tt : 0;
+  const int ntiles = do_tip ? (nloc_s + tt - 1) / tt : 0;
   // k_dom is [.., T_max/KB, n_tip, KB, 2]: a tile of whole blocks is one
   // contiguous range, moved by a single bulk copy
   const uint32_t fc_row_bytes = (uint32_t)KB * 2 * ES;
@@ -409,7 +427,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   auto tip_issue = [&](int it) {  // one thread
     const int s = it % ns;
     const int tau0 = t0 + it * tt;
-    const int nblk = (min(tt, t1 - tau0) + KB - 1) / KB;
+    const int nblk = (min(tt, t1s - tau0) + KB - 1) / KB;
     const uint32_t bytes = (uint32_t)nblk * blk_bytes;
     const uint32_t bar = smem_u32(&bars[s]);
     mbar_arrive_expect_tx(bar, bytes);
@@ -451,6 +469,52 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     }
   }
   __syncthreads();
+
+  // F_APPEND, in the CTA that owns the new token: rotate its key by its
+  // position, store key and value at index t_new of the cache and the key's
+  // dominant FCs in K_dom, and score it exactly as the TIP loop scores a
+  // streamed token (same FC order, same accumulation; stored precision).
+  float s_new = 0.f;
+  if (own_new) {
+    float2* knew = reinterpret_cast<float2*>(stile);  // rotated key pairs, as stored
+    const T* kn = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D;
+    const T* vn = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D;
+    T* Kw = const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D;
+    T* Vw = const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D;
+    for (int i = tid; i < D / 2; i += NT) {
+      const float x0 = to_f32<T>(kn[2 * i]), x1 = to_f32<T>(kn[2 * i + 1]);
+      const float2 c = rope_cos_sin(p.rope_turns[i], t_new);
+      const T r0 = from_f32<T>(x0 * c.x - x1 * c.y), r1 = from_f32<T>(x0 * c.y + x1 * c.x);
+      Kw[2 * i] = r0;
+      Kw[2 * i + 1] = r1;
+      Vw[2 * i] = vn[2 * i];
+      Vw[2 * i + 1] = vn[2 * i + 1];
+      knew[i] = make_float2(to_f32<T>(r0), to_f32<T>(r1));
+    }
+    __syncthreads();
+    T* kdw = const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc * KB + (t_new % KB)) * 2;
+    auto dom_at = [&](int j) { return min(max(p.dom_fc[h * nfc + j], 0), D / 2 - 1); };
+    for (int j = tid; j < nfc; j += NT) {
+      const float2 kp = knew[dom_at(j)];
+      kdw[(size_t)j * KB * 2] = from_f32<T>(kp.x);
+      kdw[(size_t)j * KB * 2 + 1] = from_f32<T>(kp.y);
+    }
+    if (tid == 0 && do_tip) {
+      float a0 = 0.f, a1 = 0.f;
+      auto fc_add = [&](int j, float& a) {
+        const float2 kp = knew[dom_at(j)];
+        a = fmaf(qbar[2 * j], kp.x, fmaf(qbar[2 * j + 1], kp.y, a));
+      };
+      int j = 0;
+      for (; j + 2 <= nfc; j += 2) {
+        fc_add(j, a0);
+        fc_add(j + 1, a1);
+      }
+      if (j < nfc) fc_add(j, a0);
+      s_new = a0 + a1;
+    }
+    __syncthreads();
+  }
   cluster_wait();
 
   // ---------------------------------------------------------------- TIP scan
@@ -460,6 +524,10 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // that runs out stops the warp and, through ms->tip_fail, the others at
   // their next tile.
   float* scw = (p.s_cap > 0) ? sc_s : (p.scores + (size_t)unit * p.T_max + t0);
+  if (own_new && do_tip && tid == 0) {  // the appended token's score, as TIP would
+    scw[t_new - t0] = s_new;
+    if (need_select) atomicAdd(&hloc[score_key(s_new) >> 20], 1u);
+  }
   int tip_fail = 0;
   for (int it = 0; it < ntiles; ++it) {
     const int s = it % ns;
@@ -473,7 +541,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       break;
     }
     const int tau_base = it * tt;
-    const int ntok = min(tt, nloc - tau_base);
+    const int ntok = min(tt, nloc_s - tau_base);
     const unsigned char* st = big + s * stage_bytes;
     switch (nfc) {  // the common dominant-FC counts get fully unrolled loops
       case 8: tip_tile<T, 8>(st, ntok, nfc, qbar, scw + tau_base, hloc, need_select); break;
@@ -1023,6 +1091,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // ---------------------------------------------------------------- FAC
   if (flags & (F_FAC | F_DENSE)) {
     if (!fac_started) {
+      // an appended row may be gathered by another CTA of the cluster: the
+      // barrier orders its owner's stores before the gathers
+      if (t_new >= 0) cluster_sync();
       int n_total;
       if (flags & F_DENSE) {
         n_total = len;

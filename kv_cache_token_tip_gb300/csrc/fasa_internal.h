@@ -30,6 +30,7 @@ enum : int {
   F_FAC = 1 << 5,      // attention over the selected rows
   F_IDX_IN = 1 << 6,   // selected rows come from p.idx_in / p.count_in
   F_DENSE = 1 << 7,    // attention over every cached row
+  F_APPEND = 1 << 8,   // step: first append the new token (k_new, v_new) at index len
 };
 
 struct Params {
@@ -47,6 +48,8 @@ struct Params {
   const int* seq_lens;
   const float* scores_in;   // F_SC_IN
   float* scores;            // TIP output (s_cap == 0) -- global [B,Hkv,T_max]
+  const void* k_new;        // F_APPEND: the new token's pre-RoPE key [B,Hkv,d]
+  const void* v_new;        //           and value [B,Hkv,d]
   const int* idx_in;        // F_IDX_IN
   const int* count_in;
   int* idx_out;             // F_IDX_OUT

@@ -20,6 +20,7 @@ EXPORTS = [
     "fasa_workspace_size", "fasa_apply_rope_q", "fasa_build_kdom", "fasa_append_kdom",
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
+    "fasa_decode_step_append",
 ]
 
 
@@ -85,6 +86,8 @@ def lib():
                                  ctypes.c_int),
             "fasa_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "fasa_decode_step_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_decode_step_append": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
+                                        ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -218,6 +221,24 @@ def fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: 
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
         _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
         _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
+        _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_decode_step_append(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, dom_fc, budget: int, out,
+                            idx_out=None, count_out=None, workspace=None, dims: FasaDims = None, stream=None):
+    """The decode step with the new token appended first: k_new (pre-RoPE)
+    and v_new [B,Hkv,d] go to index seq_lens[b] of the caches (and K_dom),
+    and the step attends over seq_lens[b] + 1 tokens with the query at
+    position seq_lens[b].  seq_lens is not advanced."""
+    ws_bytes = 0
+    if workspace is not None and not isinstance(workspace, int):
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fasa_decode_step_append", lib().fasa_decode_step_append(
+        _ptr(q, _store_dtypes(), "q"), _ptr(k_new, _store_dtypes(), "k_new"),
+        _ptr(v_new, _store_dtypes(), "v_new"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"), int(budget),
+        _ptr(out, _f32(), "out"), _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
 
 
