@@ -298,6 +298,9 @@ def run_gpu(args):
     dims = dims_for(cfg)
     lens = synth.seq_lens(cfg)
     model = algorithmic_bytes(cfg, lens)
+    if args.append:  # the new token's K and V rows and K_dom entries are written
+        model["append"] = cfg.batch * cfg.n_kv_heads * (2 * cfg.head_dim + 2 * cfg.n_tip) * cfg.elem_bytes
+        model["total"] += model["append"]
     layers = cfg.layers          # a decode step runs every layer: one launch each
     per_step = model["total"] * layers
     if layers > 1:
@@ -314,10 +317,28 @@ def run_gpu(args):
     outs = [torch.empty((B, Hq, d), dtype=torch.float32, device="cuda") for _ in range(R)]
     stream = torch.cuda.Stream()
 
+    if args.append:
+        # fasa_decode_step_append with lengths one short of the cache: each
+        # step stores its token at index len - 1 (the same slot on every
+        # replay) and attends over the same len tokens as the plain step
+        from kv_cache_token_tip_gb300 import fasa_decode_step_append
+        gen = torch.Generator(device="cuda").manual_seed(1)
+        app = []
+        for L, _ in reps:
+            shape = (B, H, cfg.head_dim)
+            kn = torch.randn(shape, generator=gen, device="cuda").to(L.k.dtype)
+            vn = torch.randn(shape, generator=gen, device="cuda").to(L.v.dtype)
+            app.append((kn, vn, (L.seq_lens - 1).contiguous()))
+
     def step(i):
         L, kd = reps[i % R]
-        fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, k, outs[i % R],
-                         None, None, ws, dims, stream=stream)
+        if args.append:
+            kn, vn, lens_m1 = app[i % R]
+            fasa_decode_step_append(L.q, kn, vn, lens_m1, L.k, L.v, kd, L.dom_fc, k, outs[i % R],
+                                    None, None, ws, dims, stream=stream)
+        else:
+            fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, k, outs[i % R],
+                             None, None, ws, dims, stream=stream)
 
     # dense comparison: the same kernels over every cached row
     q_rots = []
@@ -485,9 +506,12 @@ def run_gpu(args):
                                   f"CUDA graph of fasa_decode_step launches, one kernel per layer, "
                                   f"{layers} layers per step"),
                        "layers": layers,
+                       "entry": "fasa_decode_step_append (each step stores its own token)" if args.append
+                                else "fasa_decode_step",
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": per_step,
-            "bytes_breakdown": {kk: model[kk] * layers for kk in ("tip", "fac", "q", "out", "small")},
+            "bytes_breakdown": {kk: model[kk] * layers for kk in ("tip", "fac", "q", "out", "small", "append")
+                                if kk in model},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),
                          "peak_kind": peak_kind, "kernel": f"fasa_cluster_kernel<{cfg.dtype},{cfg.head_dim}>"},
@@ -550,6 +574,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--append", action="store_true",
+                    help="time fasa_decode_step_append (the step stores its own token first) instead of "
+                         "fasa_decode_step")
     ap.add_argument("--replicas", type=int, default=0,
                     help="input replicas rotated through (0: enough to exceed 4x L2, as timing requires; "
                          "a smaller count is for profiler captures)")

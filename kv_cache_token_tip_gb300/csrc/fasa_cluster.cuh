@@ -365,6 +365,17 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // with F_APPEND the query sits at the new token's position, len
   const int m_pos = (flags & F_ROPE) ? ((flags & F_APPEND) ? len : p.pos[b]) : 0;
   const int dom_i = (tid < p.n_tip && (flags & F_TIP)) ? p.dom_fc[h * p.n_tip + tid] : 0;
+  // F_APPEND: the new token's key and value pairs (thread i < D/2: pair i),
+  // loaded here with the other small inputs whichever CTA turns out to own it
+  T kn0 = T(0.f), kn1 = T(0.f), vn0 = T(0.f), vn1 = T(0.f);
+  if ((flags & F_APPEND) && tid < D / 2) {
+    const T* kn = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D;
+    const T* vn = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D;
+    kn0 = kn[2 * tid];
+    kn1 = kn[2 * tid + 1];
+    vn0 = vn[2 * tid];
+    vn1 = vn[2 * tid + 1];
+  }
   constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;  // query pairs per thread
   float2 qv[QPAIRS];
 #pragma unroll
@@ -477,18 +488,17 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   float s_new = 0.f;
   if (own_new) {
     float2* knew = reinterpret_cast<float2*>(stile);  // rotated key pairs, as stored
-    const T* kn = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D;
-    const T* vn = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D;
     T* Kw = const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D;
     T* Vw = const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D;
-    for (int i = tid; i < D / 2; i += NT) {
-      const float x0 = to_f32<T>(kn[2 * i]), x1 = to_f32<T>(kn[2 * i + 1]);
+    if (tid < D / 2) {  // D / 2 <= NT
+      const int i = tid;
+      const float x0 = to_f32<T>(kn0), x1 = to_f32<T>(kn1);
       const float2 c = rope_cos_sin(p.rope_turns[i], t_new);
       const T r0 = from_f32<T>(x0 * c.x - x1 * c.y), r1 = from_f32<T>(x0 * c.y + x1 * c.x);
       Kw[2 * i] = r0;
       Kw[2 * i + 1] = r1;
-      Vw[2 * i] = vn[2 * i];
-      Vw[2 * i + 1] = vn[2 * i + 1];
+      Vw[2 * i] = vn0;
+      Vw[2 * i + 1] = vn1;
       knew[i] = make_float2(to_f32<T>(r0), to_f32<T>(r1));
     }
     __syncthreads();
