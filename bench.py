@@ -311,6 +311,13 @@ def run_gpu(args):
     if args.replicas > 0:  # profiling runs only: fewer replicas may fit in L2
         R = args.replicas
     reps = make_replicas(cfg, R, dims)
+    if args.fasa_m:
+        # FASA-M placement: the K/V caches move to page-locked host memory
+        # (read in place by the row gather over the host link); K_dom stays
+        for L, _ in reps:
+            L.k = L.k.cpu().pin_memory()
+            L.v = L.v.cpu().pin_memory()
+        torch.cuda.empty_cache()
     B, Hq, H, d, k = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.budget
     ws_bytes = fasa_workspace_size(dims, k)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
@@ -508,8 +515,15 @@ def run_gpu(args):
                        "layers": layers,
                        "entry": "fasa_decode_step_append (each step stores its own token)" if args.append
                                 else "fasa_decode_step",
+                       "kv_placement": "pinned host memory (FASA-M): selected rows cross the host link"
+                                       if args.fasa_m else "device memory",
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": per_step,
+            **({"fasa_m": {"link_bytes_per_step": model["fac"] * layers,
+                           "link_gbs": round(model["fac"] * layers / sec_per_step / 1e9, 1),
+                           "hbm_bytes_not_held_per_replica": int(2 * reps[0][0].k.numel()
+                                                                 * reps[0][0].k.element_size())}}
+               if args.fasa_m else {}),
             "bytes_breakdown": {kk: model[kk] * layers for kk in ("tip", "fac", "q", "out", "small", "append")
                                 if kk in model},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
@@ -574,6 +588,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--fasa-m", dest="fasa_m", action="store_true",
+                    help="FASA-M placement: K/V caches in pinned host memory, K_dom on the GPU")
     ap.add_argument("--append", action="store_true",
                     help="time fasa_decode_step_append (the step stores its own token first) instead of "
                          "fasa_decode_step")

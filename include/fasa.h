@@ -12,6 +12,16 @@
  *  - Every tensor pointer is a DEVICE pointer owned by the caller.  Nothing
  *    is allocated or freed by the library.  Calls are asynchronous on
  *    `stream` (NULL = the legacy default stream).
+ *  - FASA-M placement (the FASA pages, "Hardware-Aware Variants": keep the
+ *    dominant key cache on the GPU, offload the rest of the KV cache to host
+ *    memory and move only the selected tokens): k_cache and v_cache of
+ *    fasa_decode_step, fasa_decode_step_append, fasa_decode_step_noalloc,
+ *    fasa_focused_attention and fasa_dense_attention may instead point to
+ *    page-locked host memory that the device can address (cudaHostAlloc /
+ *    cudaHostRegister, same pointer on the device).  Those entry points read
+ *    the caches only row by row in the attention gather (and the append step
+ *    writes its one row), so a step then moves just the selected K/V rows
+ *    over the host link; TIP reads k_dom, which stays in device memory.
  *  - Return value: FASA_OK, or an error code.  Arguments are validated on
  *    the host before any launch; on an error nothing is launched and nothing
  *    is written.  Values that live in device memory (sequence lengths,

@@ -98,14 +98,17 @@ def lib():
 
 
 # ---------------------------------------------------------------- marshalling
-def _ptr(x, dtype=None, name="tensor"):
+def _ptr(x, dtype=None, name="tensor", host_ok=False):
+    """Device pointer of a contiguous tensor.  With host_ok, a tensor in pinned
+    host memory is accepted too (the GPU reads it in place over the
+    host link: the FASA-M placement of the K/V caches)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     import torch
-    if not x.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_cuda and not (host_ok and x.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not x.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and x.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
@@ -197,16 +200,16 @@ def fasa_topk_select(scores, seq_lens, budget: int, idx, count, dims: FasaDims, 
 def fasa_focused_attention(q_rot, k_cache, v_cache, seq_lens, idx, count, budget: int, out,
                            dims: FasaDims, stream=None):
     _check("fasa_focused_attention", lib().fasa_focused_attention(
-        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
-        _ptr(v_cache, _store_dtypes(), "v_cache"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache", True),
+        _ptr(v_cache, _store_dtypes(), "v_cache", True), _ptr(seq_lens, _i32(), "seq_lens"),
         _ptr(idx, _i32(), "idx"), _ptr(count, _i32(), "count"), int(budget),
         _ptr(out, _f32(), "out"), ctypes.byref(dims), _stream(stream)))
 
 
 def fasa_dense_attention(q_rot, k_cache, v_cache, seq_lens, out, dims: FasaDims, stream=None):
     _check("fasa_dense_attention", lib().fasa_dense_attention(
-        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
-        _ptr(v_cache, _store_dtypes(), "v_cache"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache", True),
+        _ptr(v_cache, _store_dtypes(), "v_cache", True), _ptr(seq_lens, _i32(), "seq_lens"),
         _ptr(out, _f32(), "out"), ctypes.byref(dims), _stream(stream)))
 
 
@@ -217,7 +220,7 @@ def fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: 
         ws_bytes = workspace.numel() * workspace.element_size()
     _check("fasa_decode_step", lib().fasa_decode_step(
         _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"),
-        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
         _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
         _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
@@ -236,7 +239,7 @@ def fasa_decode_step_append(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, 
     _check("fasa_decode_step_append", lib().fasa_decode_step_append(
         _ptr(q, _store_dtypes(), "q"), _ptr(k_new, _store_dtypes(), "k_new"),
         _ptr(v_new, _store_dtypes(), "v_new"), _ptr(seq_lens, _i32(), "seq_lens"),
-        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"), int(budget),
         _ptr(out, _f32(), "out"), _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
@@ -248,7 +251,7 @@ def fasa_decode_step_noalloc(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, 
     allocate device memory, the step uses the library's fixed scratch array."""
     _check("fasa_decode_step_noalloc", lib().fasa_decode_step_noalloc(
         _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"),
-        _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(v_cache, _store_dtypes(), "v_cache"),
+        _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
         _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
         _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),

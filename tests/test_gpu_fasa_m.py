@@ -1,0 +1,81 @@
+"""FASA-M placement (GPU): the K/V caches in page-locked host memory, the
+dominant key cache in device memory ("Hardware-Aware Variants" on the FASA
+pages).  The step reads the caches only in the row gather, so the results
+must equal the all-device run bit for bit; the append step must also land
+its row in host memory."""
+
+import numpy as np
+import pytest
+
+from tests.gpu_util import build_kdom, ensure_built
+from workload import configs, gpu_gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    ensure_built()
+
+
+def _ws(dims, budget):
+    import torch
+    from kv_cache_token_tip_gb300 import fasa_workspace_size
+    n = fasa_workspace_size(dims, budget)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device="cuda") if n else None
+
+
+@pytest.mark.parametrize("name,over", [("llama3_8b_ctx32k", dict(context=8192, batch=2)),
+                                       ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2))])
+def test_step_and_dense_with_host_caches(name, over):
+    import torch
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_apply_rope_q, fasa_decode_step, fasa_dense_attention,
+                                          fasa_device_status)
+    cfg = configs.CONFIGS[name].with_(**over)
+    L = gpu_gen.make_layer(cfg, 0)
+    dims = dims_for(cfg)
+    kd = build_kdom(L, dims)
+    ws = _ws(dims, cfg.budget)
+    Kh, Vh = L.k.cpu().pin_memory(), L.v.cpu().pin_memory()
+    res = []
+    for K, V in ((L.k, L.v), (Kh, Vh)):
+        out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+        idx = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.budget), dtype=torch.int32, device="cuda")
+        fasa_decode_step(L.q, L.pos, K, V, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, None, ws, dims)
+        q_rot = torch.empty_like(out)
+        fasa_apply_rope_q(L.q, L.pos, q_rot, dims)
+        dense = torch.empty_like(out)
+        fasa_dense_attention(q_rot, K, V, L.seq_lens, dense, dims)
+        assert fasa_device_status() == 0
+        res.append((out.cpu(), idx.cpu(), dense.cpu()))
+    assert torch.equal(res[0][1], res[1][1])
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][2], res[1][2])
+    assert np.all(np.isfinite(res[1][0].numpy()))
+
+
+def test_append_step_with_host_caches():
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for, fasa_decode_step_append, fasa_device_status
+    cfg = configs.CONFIGS["llama3_8b_ctx32k"].with_(context=4096, batch=2)
+    L = gpu_gen.make_layer(cfg, 0)
+    L.seq_lens = torch.tensor([3000, 77], dtype=torch.int32, device="cuda")
+    dims = dims_for(cfg)
+    kd_dev = build_kdom(L, dims)
+    kd_host_run = kd_dev.clone()
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    shape = (cfg.batch, cfg.n_kv_heads, cfg.head_dim)
+    kn = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    vn = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    ws = _ws(dims, cfg.budget)
+    Kd, Vd = L.k.clone(), L.v.clone()
+    Kh, Vh = L.k.cpu().pin_memory(), L.v.cpu().pin_memory()
+    outs = []
+    for K, V, kd in ((Kd, Vd, kd_dev), (Kh, Vh, kd_host_run)):
+        out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+        fasa_decode_step_append(L.q, kn, vn, L.seq_lens, K, V, kd, L.dom_fc, cfg.budget, out, None, None, ws, dims)
+        assert fasa_device_status() == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(kd_dev, kd_host_run)
+    assert torch.equal(Kd.cpu(), Kh) and torch.equal(Vd.cpu(), Vh)
