@@ -44,7 +44,8 @@ __all__ = [
     "fc_score", "tip_scores_unit", "topk_select_unit", "focused_attention_unit",
     "tip_score", "topk_select", "focused_attention", "dense_attention",
     "decode_step", "append_token", "decode_step_append", "build_kdom", "bytes_fraction",
-    "theoretical_speedup",
+    "theoretical_speedup", "fc_scores_unit", "ca_from_scores", "contextual_agreement_unit",
+    "calibrate_dominant_fcs",
 ]
 
 
@@ -281,6 +282,55 @@ def build_kdom(K_stored: np.ndarray, dom_fc: np.ndarray, block: int = 64) -> np.
             i = int(dom_fc[h, j])
             cols = K_stored[:, h, :, 2 * i:2 * i + 2]           # [B, T, 2]
             out[:, h, :, j, :, :] = cols.reshape(B, T // block, block, 2)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Contextual Agreement and the offline calibration, [P5] "The Functional
+# Sparsity Hypothesis and the Contextual Agreement (CA) Metric" (Eq. 4) and
+# the calibration objective with its procedure (Algorithm 1)
+# ----------------------------------------------------------------------------
+def fc_scores_unit(q_rot_group: np.ndarray, k_rows: np.ndarray) -> np.ndarray:
+    """Single-FC scores of every FC i for one (batch, KV head):
+    alpha_i[tau] = sum over the group's query heads of q'^[i] . k_tau^[i]
+    (post-RoPE, the same group sum as TIP).  Returns [d/2, t]."""
+    q = np.asarray(q_rot_group, dtype=np.float64)
+    K = np.asarray(k_rows, dtype=np.float64)
+    F = K.shape[1] // 2
+    return np.stack([fc_score(q[g], K, i) for i in range(F) for g in range(q.shape[0])]
+                    ).reshape(F, q.shape[0], -1).sum(axis=1)
+
+
+def ca_from_scores(full: np.ndarray, alpha_i: np.ndarray, K: int) -> float:
+    """Eq. 4: |TopK-I(full, K) & TopK-I(alpha_i, K)| / K, with K' = min(K, t)
+    in place of K (both sets hold every token when t <= K)."""
+    t = len(full)
+    kk = min(K, t)
+    if kk == 0:
+        return 1.0
+    a = set(topk_select_unit(full, kk).tolist())
+    b = set(topk_select_unit(alpha_i, kk).tolist())
+    return len(a & b) / kk
+
+
+def contextual_agreement_unit(q_rot_group, k_rows, K: int) -> np.ndarray:
+    """CA of every FC for one (batch, KV head) and one query group: the full
+    head's scores are the sum of the single-FC scores (the FC decomposition
+    of q R k^T).  Returns [d/2]."""
+    A = fc_scores_unit(q_rot_group, k_rows)
+    full = A.sum(axis=0)
+    return np.array([ca_from_scores(full, A[i], K) for i in range(A.shape[0])])
+
+
+def calibrate_dominant_fcs(ca_mean: np.ndarray, n_tip: int) -> np.ndarray:
+    """Algorithm 1, last step: per head, the n_tip FCs with the highest mean
+    CA (equal means: smaller FC index first), returned in ascending order.
+    ca_mean [Hkv, d/2] -> [Hkv, n_tip] int32."""
+    ca_mean = np.asarray(ca_mean, dtype=np.float64)
+    out = np.empty((ca_mean.shape[0], n_tip), dtype=np.int32)
+    for h in range(ca_mean.shape[0]):
+        order = np.argsort(-ca_mean[h], kind="stable")[:n_tip]
+        out[h] = np.sort(order)
     return out
 
 

@@ -411,4 +411,62 @@ def check_append_equals_cached_token(o):
     assert np.allclose(out, out2, rtol=1e-12, atol=1e-12)
 
 
+# --- NEXT-4: Contextual Agreement (Eq. 4) and calibration (Algorithm 1) -----
+def check_ca_hand_examples(o):
+    """Overlaps worked out by hand (TopK-I: larger first, ties to the smaller
+    token index)."""
+    full = np.array([6.0, 5, 4, 3, 2, 1])                  # top-3: {0, 1, 2}
+    assert o.ca_from_scores(full, np.array([1.0, 2, 3, 6, 5, 4]), 3) == 0.0       # {3, 4, 5}
+    assert abs(o.ca_from_scores(full, np.array([6.0, 1, 5, 2, 4, 3]), 3) - 2 / 3) < 1e-15  # {0, 2, 4}
+    assert o.ca_from_scores(full, full * 7.0, 3) == 1.0     # same ranking
+    ties_full = np.array([1.0, 1, 1, 0])                    # top-2: {0, 1}
+    assert o.ca_from_scores(ties_full, np.array([0.0, 1, 1, 1]), 2) == 0.5  # {1, 2}
+    assert o.ca_from_scores(full, -full, 6) == 1.0          # K = t: every token in both
+
+
+def check_ca_bounds_and_short_contexts(o):
+    rng = _rng(51)
+    q = rng.standard_normal((3, 8))
+    K = rng.standard_normal((40, 8))
+    ca = o.contextual_agreement_unit(q, K, 7)
+    assert ca.shape == (4,) and np.all((ca >= 0) & (ca <= 1))
+    assert np.all(np.abs(ca * 7 - np.round(ca * 7)) < 1e-12)  # multiples of 1/K
+    assert np.all(o.contextual_agreement_unit(q, K[:5], 7) == 1.0)  # t <= K
+
+
+def check_ca_single_carrying_fc(o):
+    """A query whose only non-zero FC is j: FC j's scores are the full scores
+    (CA 1); every other FC scores all tokens 0, so its top-K is the first K
+    tokens and its CA is the share of the full top-K below index K."""
+    rng = _rng(52)
+    t, K, j = 50, 6, 2
+    q = np.zeros((2, 8))
+    q[:, 2 * j:2 * j + 2] = rng.standard_normal((2, 2))
+    Kr = rng.standard_normal((t, 8))
+    ca = o.contextual_agreement_unit(q, Kr, K)
+    full = Kr @ q.sum(axis=0)
+    top = sorted(range(t), key=lambda tau: (-full[tau], tau))[:K]
+    share = sum(1 for tau in top if tau < K) / K
+    assert ca[j] == 1.0
+    for i in range(4):
+        if i != j:
+            assert ca[i] == share
+
+
+def check_fc_scores_sum_to_logits(o):
+    rng = _rng(53)
+    q = rng.standard_normal((4, 16))
+    K = rng.standard_normal((30, 16))
+    A = o.fc_scores_unit(q, K)
+    assert A.shape == (8, 30)
+    assert np.allclose(A.sum(axis=0), K @ q.sum(axis=0), rtol=1e-12, atol=1e-12)
+    assert np.allclose(A[3], K[:, 6:8] @ q[:, 6:8].sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def check_calibration_selection(o):
+    ca = np.array([[0.1, 0.5, 0.5, 0.2], [0.9, 0.1, 0.3, 0.3], [0.3, 0.3, 0.3, 0.3]])
+    assert np.array_equal(o.calibrate_dominant_fcs(ca, 2), [[1, 2], [0, 2], [0, 1]])
+    assert np.array_equal(o.calibrate_dominant_fcs(ca, 3), [[1, 2, 3], [0, 2, 3], [0, 1, 2]])
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

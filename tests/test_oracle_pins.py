@@ -112,6 +112,23 @@ def _append_one_position_late(K, V, k_new, v_new, seq_lens, rope_theta):
     return K, V, lens + 1
 
 
+def _ca_over_t(full, alpha_i, K):
+    t = len(full)
+    kk = min(K, t)
+    a = set(O.topk_select_unit(full, kk).tolist())
+    b = set(O.topk_select_unit(alpha_i, kk).tolist())
+    return len(a & b) / t
+
+
+def _calibrate_lowest(ca_mean, n_tip):
+    return np.sort(np.argsort(np.asarray(ca_mean), axis=1, kind="stable")[:, :n_tip], axis=1).astype(np.int32)
+
+
+def _ca_fc_vs_itself(q_rot_group, k_rows, K):
+    A = O.fc_scores_unit(q_rot_group, k_rows)
+    return np.array([O.ca_from_scores(A[i], A[i], K) for i in range(A.shape[0])])
+
+
 MUTATIONS = {
     "rope_row_vector_sign": ("rope_rotate", _rope_row_convention),
     "rope_rotate_half_pairing": ("rope_rotate", _rope_rotate_half),
@@ -122,6 +139,9 @@ MUTATIONS = {
     "kdom_splits_fc_pair": ("build_kdom", _kdom_wrong_pair),
     "gqa_modulo_mapping": ("focused_attention", _focused_attention_wrong_group),
     "append_rotates_one_position_late": ("append_token", _append_one_position_late),
+    "ca_normalised_by_t": ("ca_from_scores", _ca_over_t),
+    "calibration_keeps_lowest_ca": ("calibrate_dominant_fcs", _calibrate_lowest),
+    "ca_compares_fc_with_itself": ("contextual_agreement_unit", _ca_fc_vs_itself),
 }
 
 
