@@ -211,6 +211,39 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
+ * Offline calibration of the dominant FCs (the FASA pages: "The Functional
+ * Sparsity Hypothesis and the Contextual Agreement (CA) Metric", Eq. 4, and
+ * the calibration procedure, Algorithm 1).
+ *
+ * fasa_fc_agreement: for every sequence b and KV head h, the Contextual
+ * Agreement of every FC i over the cached tokens tau < len_b:
+ *   alpha_i[tau] = sum over the group's query heads g of q_rot_g^[i] . k_tau^[i]
+ *   full[tau]    = sum_i alpha_i[tau]        (the head's logits, group-summed
+ *                                             as TIP sums them)
+ *   ca[b,h,i]    = |TopK-I(full, K') & TopK-I(alpha_i, K')| / K',
+ *                  K' = min(topk, len_b); 1 when len_b = 0.
+ * TopK-I keeps the K' largest scores, equal scores to the smaller tau.
+ *   q_rot fp32 [B,Hq,d] (rotated queries at the calibration step), k_cache as
+ *   for the other entry points (16-byte aligned), ca fp32 [B,Hkv,d/2] (out).
+ * dims->n_tip is not used.  One CTA per (FC, b, h) keeps one key per cached
+ * token in shared memory: FASA_ERR_UNSUPPORTED when T_max exceeds what fits
+ * (about 52K tokens on GB300).  Lengths out of range are clamped and set
+ * FASA_DEV_BAD_INPUT.  A calibration averages ca over its samples (queries,
+ * sequences) and passes the mean to fasa_select_dominant_fcs.
+ */
+int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* seq_lens, int32_t topk,
+                      float* ca, const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
+ * Algorithm 1, last step: dom_fc[h, 0..n_tip) = the n_tip FCs of highest
+ * ca_mean[h, :] (equal values: the smaller FC index first), in ascending
+ * order.  ca_mean fp32 [Hkv, d/2], dom_fc int32 [Hkv, n_tip] (out), both in
+ * device memory; 1 <= n_tip <= d/2.
+ */
+int fasa_select_dominant_fcs(const float* ca_mean, int32_t n_tip, int32_t* dom_fc,
+                             const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
  * Size of the fixed device scratch array used by fasa_decode_step_noalloc:
  * 16 MiB, i.e. scores for B * Hkv * T_max <= 4194304 cached tokens.
  */

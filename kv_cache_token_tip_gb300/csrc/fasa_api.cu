@@ -665,6 +665,32 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* seq_lens, int32_t topk, float* ca,
+                      const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q_rot || !k_cache || !seq_lens || !ca || topk < 1) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(q_rot)) return FASA_ERR_INVALID_ARG;
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  if (fc_agreement_smem(dims->head_dim, dims->t_max) > (size_t)di.smem_optin) return FASA_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_fc_agreement(q_rot, k_cache, seq_lens, topk, ca, dims->batch, dims->n_q_heads,
+                                            dims->n_kv_heads, dims->head_dim, dims->t_max, dims->dtype == FASA_BF16,
+                                            di.status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+int fasa_select_dominant_fcs(const float* ca_mean, int32_t n_tip, int32_t* dom_fc, const fasa_dims_t* dims,
+                             fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!ca_mean || !dom_fc || n_tip < 1 || n_tip > dims->head_dim / 2) return FASA_ERR_INVALID_ARG;
+  const cudaError_t e = launch_select_dominant(ca_mean, dims->n_kv_heads, dims->head_dim / 2, n_tip, dom_fc,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
 int fasa_device_status(fasa_stream_t stream, int32_t* status) {
   if (!status) return FASA_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

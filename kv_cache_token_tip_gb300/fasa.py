@@ -20,7 +20,7 @@ EXPORTS = [
     "fasa_workspace_size", "fasa_apply_rope_q", "fasa_build_kdom", "fasa_append_kdom",
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
-    "fasa_decode_step_append",
+    "fasa_decode_step_append", "fasa_fc_agreement", "fasa_select_dominant_fcs",
 ]
 
 
@@ -88,6 +88,8 @@ def lib():
             "fasa_decode_step_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_decode_step_append": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
                                         ctypes.c_int),
+            "fasa_fc_agreement": ([vp, vp, vp, i32, vp, dp, vp], ctypes.c_int),
+            "fasa_select_dominant_fcs": ([vp, i32, vp, dp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -243,6 +245,22 @@ def fasa_decode_step_append(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, 
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"), int(budget),
         _ptr(out, _f32(), "out"), _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_fc_agreement(q_rot, k_cache, seq_lens, topk: int, ca, dims: FasaDims, stream=None):
+    """Contextual Agreement of every FC for every (batch, KV head):
+    ca [B, Hkv, d/2] fp32."""
+    _check("fasa_fc_agreement", lib().fasa_fc_agreement(
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
+        _ptr(seq_lens, _i32(), "seq_lens"), int(topk), _ptr(ca, _f32(), "ca"), ctypes.byref(dims),
+        _stream(stream)))
+
+
+def fasa_select_dominant_fcs(ca_mean, n_tip: int, dom_fc, dims: FasaDims, stream=None):
+    """dom_fc [Hkv, n_tip] int32 <- the n_tip FCs of highest mean CA per head."""
+    _check("fasa_select_dominant_fcs", lib().fasa_select_dominant_fcs(
+        _ptr(ca_mean, _f32(), "ca_mean"), int(n_tip), _ptr(dom_fc, _i32(), "dom_fc"), ctypes.byref(dims),
+        _stream(stream)))
 
 
 def fasa_decode_step_noalloc(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: int, out,
