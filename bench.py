@@ -40,6 +40,9 @@ KERNEL_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_cluster.cuh",
                   "kv_cache_token_tip_gb300/csrc/fasa_ptx.cuh",
                   "kv_cache_token_tip_gb300/csrc/fasa_internal.h",
                   "kv_cache_token_tip_gb300/csrc/fasa_api.cu"]
+CA_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_ca.cu",
+              "kv_cache_token_tip_gb300/csrc/fasa_ptx.cuh"]
+CA_METRIC = "FC calibration (Contextual Agreement of every FC): achieved HBM TB/s of the K cache read once"
 
 
 # ----------------------------------------------------------------------------
@@ -62,9 +65,9 @@ def algorithmic_bytes(cfg, lens) -> dict:
                 total=tip + sel + q + out + small, dense_total=dense)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -80,13 +83,14 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"fasa_step_{workload}.md")
+def ncu_traffic(workload: str, prefix: str = "fasa_step", sources=None):
+    """DRAM bytes per launch (per call, for a call of several launches) from
+    the committed ncu summary, if it was taken on the current kernel sources
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(sources)
     vals = {}
     with open(path) as f:
         for line in f:
@@ -243,14 +247,49 @@ def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: 
     return time.perf_counter() - t0, steps, nbytes
 
 
-def run_oracle_leg(cfg, seconds: float, max_steps: int = 10 ** 9, warmup: int = 0):
-    """Runs oracle_sample in a child process with BLAS limited to one thread so
-    the reported core count is exact."""
+def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 1):
+    """Times the fp64 oracle's calibration on a bounded sample: each step is one
+    (batch, KV head) unit -- RoPE of its query group at position len, then the
+    Contextual Agreement (Eq. 4) of every FC over its cached tokens with K = the
+    workload's budget.  Returns (seconds, steps, bytes of K read once)."""
+    import oracle as O
+    lens = synth.seq_lens(cfg)
+    G = cfg.group
+    q_all = O.decode_stored(synth.store(synth.gen_q(cfg, 0), cfg.dtype), cfg.dtype)
+    units = []
+    for u in range(min(n_units, cfg.batch * cfg.n_kv_heads)):
+        b, h = divmod(u, cfg.n_kv_heads)
+        L = int(lens[b])
+        kk, _ = synth.gen_kv_head(cfg, 0, b, h, t_count=L)
+        K = O.decode_stored(synth.store(kk, cfg.dtype), cfg.dtype)
+        units.append((q_all[b, h * G:(h + 1) * G], L, K, L * cfg.head_dim * cfg.elem_bytes))
+
+    def one(i):
+        q, pos, K, nb = units[i % len(units)]
+        q_rot = O.apply_rope_q(q[None], np.array([pos]), cfg.rope_theta)[0]
+        O.contextual_agreement_unit(q_rot, K, cfg.budget)
+        return nb
+
+    for i in range(warmup):
+        one(i)
+    steps, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while steps < max_steps:
+        nbytes += one(steps)
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return time.perf_counter() - t0, steps, nbytes
+
+
+def run_oracle_leg(cfg, seconds: float, max_steps: int = 10 ** 9, warmup: int = 0, fn: str = "oracle_sample"):
+    """Runs oracle_sample (or `fn`) in a child process with BLAS limited to one
+    thread so the reported core count is exact."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; from workload import configs; "
-            "cfg = configs.CONFIGS[%r]; t, n, b = bench.oracle_sample(cfg, %r, %r, %r); "
+            "cfg = configs.CONFIGS[%r]; t, n, b = bench.%s(cfg, %r, %r, %r); "
             "print(json.dumps({'seconds': t, 'steps': n, 'bytes': b}))"
-            % (ROOT, cfg.name, seconds, max_steps, warmup))
+            % (ROOT, cfg.name, fn, seconds, max_steps, warmup))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
@@ -548,6 +587,154 @@ def run_gpu(args):
     return line
 
 
+def run_calibrate(args):
+    """The offline calibration (fasa_fc_agreement: the Contextual Agreement of
+    every FC for every (batch, KV head) of the workload, K = its budget), timed
+    like the decode step: CUDA graphs of calls rotating over input replicas
+    that together exceed L2, W warm-up calls, then exactly K timed calls."""
+    import torch
+    from kv_cache_token_tip_gb300 import build as kbuild
+    kbuild.build()
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_apply_rope_q, fasa_device_status, fasa_fc_agreement,
+                                          fasa_fc_agreement_workspace_size)
+    from workload import gpu_gen
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    cfg = configs.CONFIGS[args.workload]
+    dims = dims_for(cfg)
+    lens = synth.seq_lens(cfg)
+    B, Hq, H, d = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    k_bytes = int(np.sum(lens)) * H * d * cfg.elem_bytes          # the K cache, read once
+    io_bytes = B * Hq * d * 4 + B * 4 + B * H * (d // 2) * 4       # q_rot, lengths, ca
+    per_call = k_bytes + io_bytes
+    R = args.replicas if args.replicas > 0 else min(16, max(2, int(np.ceil(4 * L2_BYTES / k_bytes))))
+    reps = []
+    for r in range(R):
+        L = gpu_gen.make_layer(cfg, layer=r)
+        L.v = None
+        qr = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        fasa_apply_rope_q(L.q, L.pos, qr, dims)
+        reps.append((L, qr, torch.empty((B, H, d // 2), dtype=torch.float32, device="cuda")))
+    torch.cuda.empty_cache()
+    ws = torch.empty(fasa_fc_agreement_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call(i):
+        L, qr, ca = reps[i % R]
+        fasa_fc_agreement(qr, L.k, L.seq_lens, cfg.budget, ca, dims, workspace=ws, stream=stream)
+
+    call(0)
+    torch.cuda.synchronize()
+    K, W = args.steps, args.warmup
+    chunk = R * max(1, 64 // R)
+    g_chunk = capture(call, chunk, stream)
+    rem = K % chunk
+    g_rem = capture(call, rem, stream) if rem else None
+    g_warm = capture(call, W, stream)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    torch.cuda.synchronize()
+    if fasa_device_status(stream):
+        raise RuntimeError("device status set after warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(K // chunk):
+                g_chunk.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    sec = max_over_ranks(pg, ev0.elapsed_time(ev1)) / 1e3 / K
+
+    # end to end through the public API: per call, a pinned H2D copy of the
+    # rotated queries and lengths (the K cache is resident model state), the
+    # call, a D2H copy of ca, a host sync
+    E = max(20, min(500, K))
+    qb = reps[0][1].numel() * 4
+    h_in = torch.empty(qb + 4 * B, dtype=torch.uint8).pin_memory()
+    h_in[:qb].copy_(reps[0][1].cpu().view(torch.uint8).reshape(-1))
+    h_in[qb:].copy_(torch.from_numpy(np.asarray(lens, dtype=np.int32)).view(torch.uint8))
+    d_in = torch.empty_like(h_in, device="cuda")
+    d_q = d_in[:qb].view(torch.float32).view(B, Hq, d)
+    d_len = d_in[qb:].view(torch.int32)
+    h_out = torch.empty((B, H, d // 2), dtype=torch.float32).pin_memory()
+    L0, _, ca0 = reps[0]
+
+    def e2e():
+        d_in.copy_(h_in, non_blocking=True)
+        fasa_fc_agreement(d_q, L0.k, d_len, cfg.budget, ca0, dims, workspace=ws, stream=stream)
+        h_out.copy_(ca0, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            e2e()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(E):
+            g.replay()
+            stream.synchronize()
+    e2e_sec = max_over_ranks(pg, time.perf_counter() - t0) / E
+    if not torch.equal(h_out, ca0.cpu()):
+        raise RuntimeError("end-to-end output copy does not match the device output")
+    if fasa_device_status(stream):
+        raise RuntimeError("device status set after the timed region")
+
+    peak, peak_kind = measured_peak()
+    achieved = per_call / sec / 1e9
+    line = None
+    cpu = None
+    if args.cpu_baseline and rank == 0 and world == 1:
+        cb = run_oracle_leg(cfg, args.cpu_seconds, fn="oracle_ca_sample")
+        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s "
+                         f"(host-generated inputs, numpy fp64, 1 BLAS thread); "
+                         f"{cb['seconds'] / cb['steps'] * B * H * 1e3:.0f} ms per whole call"}
+    if rank == 0:
+        line = {
+            "metric": CA_METRIC,
+            "value": round(world * per_call / sec / 1e12, 4), "unit": "TB/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(sec * 1e3, 6), "us_per_step": round(sec * 1e6, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded; pre-RoPE q/k ~ N(0,1) with x8 outlier FCs)",
+            "config": {"workload": cfg.name, "batch": B, "q_heads": Hq, "kv_heads": H, "head_dim": d,
+                       "context": cfg.context, "topk": cfg.budget, "replicas": R,
+                       "l2": f"{'inputs larger than L2' if R * k_bytes > L2_BYTES else 'NOT larger than L2'}: "
+                             f"{R} replicas x {k_bytes / 1e6:.1f} MB of K rotate",
+                       "entry": "fasa_fc_agreement (3 launches: scores, per-row TopK-I masks, per-FC counts)",
+                       "parallelism": f"replicas x{world}"},
+            "bytes_per_step": per_call,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(cfg.name, "fasa_ca", CA_SOURCES),
+                         "peak_kind": peak_kind, "kernel": "fasa_fc_agreement (all 3 launches of one call)"},
+            "e2e": {"value": round(world * per_call / e2e_sec / 1e12, 4), "unit": "TB/s",
+                    "us_per_step": round(e2e_sec * 1e6, 3), "h2d_bytes_per_step": int(h_in.numel()),
+                    "d2h_bytes_per_step": int(h_out.numel() * 4),
+                    "mode": "CUDA graph per call: pinned H2D of q_rot/lens, fasa_fc_agreement, D2H of ca"},
+            "gpu_launches": 3 * K,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return line
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle timed on the host cores.  Each step is
     one (batch, KV head) unit of the workload (a bounded sample); W untimed
@@ -557,19 +744,22 @@ def run_reference(args):
     if rank != 0:
         return None
     cfg = configs.CONFIGS[args.workload]
-    cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps, args.warmup)
+    cal = args.calibrate
+    cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps, args.warmup,
+                        fn="oracle_ca_sample" if cal else "oracle_sample")
     val = cb["bytes"] / cb["seconds"] / 1e12
     per_unit = cb["seconds"] / cb["steps"]
     line = {
         "impl": "reference",
-        "metric": METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
+        "metric": CA_METRIC if cal else METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
         "steps": cb["steps"], "warmup": args.warmup,
         "ms_per_step": per_unit * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, host-generated)",
         "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.n_q_heads,
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "context": cfg.context,
                    "n_tip": cfg.n_tip, "budget": cfg.budget,
-                   "step": "one (batch, KV head) unit of the decode step"},
+                   "step": "one (batch, KV head) unit of the "
+                           + ("calibration (CA of every FC, topk = budget)" if cal else "decode step")},
         "cpu_baseline": {"value": val, "unit": "TB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{cb['steps']} units in {cb['seconds']:.1f} s, bounded to "
                                    f"~{args.cpu_seconds:.0f} s (numpy fp64, 1 BLAS thread)"},
@@ -593,6 +783,8 @@ def main(argv=None):
     ap.add_argument("--append", action="store_true",
                     help="time fasa_decode_step_append (the step stores its own token first) instead of "
                          "fasa_decode_step")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="time the offline calibration (fasa_fc_agreement) instead of the decode step")
     ap.add_argument("--replicas", type=int, default=0,
                     help="input replicas rotated through (0: enough to exceed 4x L2, as timing requires; "
                          "a smaller count is for profiler captures)")
@@ -601,6 +793,8 @@ def main(argv=None):
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.calibrate:
+        return run_calibrate(args)
     return run_gpu(args)
 
 

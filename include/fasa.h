@@ -225,14 +225,21 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
  * TopK-I keeps the K' largest scores, equal scores to the smaller tau.
  *   q_rot fp32 [B,Hq,d] (rotated queries at the calibration step), k_cache as
  *   for the other entry points (16-byte aligned), ca fp32 [B,Hkv,d/2] (out).
- * dims->n_tip is not used.  One CTA per (FC, b, h) keeps one key per cached
- * token in shared memory: FASA_ERR_UNSUPPORTED when T_max exceeds what fits
- * (about 52K tokens on GB300).  Lengths out of range are clamped and set
- * FASA_DEV_BAD_INPUT.  A calibration averages ca over its samples (queries,
- * sequences) and passes the mean to fasa_select_dominant_fcs.
+ * dims->n_tip is not used.  The call streams K once: it writes every token's
+ * full and single-FC scores into the workspace as order-preserving 32-bit
+ * keys (FC-major), then each score row's TopK-I set as a token bitmask, and
+ * counts the intersections from the masks (workspace:
+ * B*Hkv*(d/2+1)*(T_max + T_max/32)*4 bytes).  workspace: device memory of
+ * at least fasa_fc_agreement_workspace_size bytes, 16-byte aligned, owned by
+ * the caller, contents not kept (FASA_ERR_WORKSPACE when missing or short).
+ * Lengths out of range are clamped and set FASA_DEV_BAD_INPUT.  A calibration
+ * averages ca over its samples (queries, sequences) and passes the mean to
+ * fasa_select_dominant_fcs.
  */
+int fasa_fc_agreement_workspace_size(const fasa_dims_t* dims, size_t* bytes);
 int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* seq_lens, int32_t topk,
-                      float* ca, const fasa_dims_t* dims, fasa_stream_t stream);
+                      float* ca, void* workspace, size_t workspace_bytes, const fasa_dims_t* dims,
+                      fasa_stream_t stream);
 
 /*
  * Algorithm 1, last step: dom_fc[h, 0..n_tip) = the n_tip FCs of highest

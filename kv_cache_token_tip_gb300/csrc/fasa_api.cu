@@ -665,19 +665,29 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fasa_fc_agreement_workspace_size(const fasa_dims_t* dims, size_t* bytes) {
+  if (!bytes) return FASA_ERR_INVALID_ARG;
+  *bytes = 0;
+  const int st = check_dims(dims);
+  if (st) return st;
+  *bytes = fc_agreement_workspace(dims->batch * dims->n_kv_heads, dims->head_dim, dims->t_max);
+  return FASA_OK;
+}
+
 int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* seq_lens, int32_t topk, float* ca,
-                      const fasa_dims_t* dims, fasa_stream_t stream) {
+                      void* workspace, size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream) {
   int st = check_dims(dims);
   if (st) return st;
   if (!q_rot || !k_cache || !seq_lens || !ca || topk < 1) return FASA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(q_rot)) return FASA_ERR_INVALID_ARG;
+  const size_t need = fc_agreement_workspace(dims->batch * dims->n_kv_heads, dims->head_dim, dims->t_max);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASA_ERR_WORKSPACE;
   DevInfo di;
   st = device_info(&di);
   if (st) return st;
-  if (fc_agreement_smem(dims->head_dim, dims->t_max) > (size_t)di.smem_optin) return FASA_ERR_UNSUPPORTED;
   const cudaError_t e = launch_fc_agreement(q_rot, k_cache, seq_lens, topk, ca, dims->batch, dims->n_q_heads,
                                             dims->n_kv_heads, dims->head_dim, dims->t_max, dims->dtype == FASA_BF16,
-                                            di.status, reinterpret_cast<cudaStream_t>(stream));
+                                            workspace, di.status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);
 }
 

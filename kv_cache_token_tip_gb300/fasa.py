@@ -20,7 +20,8 @@ EXPORTS = [
     "fasa_workspace_size", "fasa_apply_rope_q", "fasa_build_kdom", "fasa_append_kdom",
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
-    "fasa_decode_step_append", "fasa_fc_agreement", "fasa_select_dominant_fcs",
+    "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
+    "fasa_select_dominant_fcs",
 ]
 
 
@@ -88,7 +89,8 @@ def lib():
             "fasa_decode_step_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_decode_step_append": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
                                         ctypes.c_int),
-            "fasa_fc_agreement": ([vp, vp, vp, i32, vp, dp, vp], ctypes.c_int),
+            "fasa_fc_agreement_workspace_size": ([dp, ctypes.POINTER(sz)], ctypes.c_int),
+            "fasa_fc_agreement": ([vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_select_dominant_fcs": ([vp, i32, vp, dp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -247,12 +249,23 @@ def fasa_decode_step_append(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, 
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
 
 
-def fasa_fc_agreement(q_rot, k_cache, seq_lens, topk: int, ca, dims: FasaDims, stream=None):
+def fasa_fc_agreement_workspace_size(dims: FasaDims) -> int:
+    out = ctypes.c_size_t(0)
+    _check("fasa_fc_agreement_workspace_size",
+           lib().fasa_fc_agreement_workspace_size(ctypes.byref(dims), ctypes.byref(out)))
+    return out.value
+
+
+def fasa_fc_agreement(q_rot, k_cache, seq_lens, topk: int, ca, dims: FasaDims, workspace=None, stream=None):
     """Contextual Agreement of every FC for every (batch, KV head):
-    ca [B, Hkv, d/2] fp32."""
+    ca [B, Hkv, d/2] fp32.  Without a workspace one is allocated here."""
+    if workspace is None:
+        import torch
+        workspace = torch.empty(fasa_fc_agreement_workspace_size(dims), dtype=torch.uint8, device=ca.device)
     _check("fasa_fc_agreement", lib().fasa_fc_agreement(
         _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
-        _ptr(seq_lens, _i32(), "seq_lens"), int(topk), _ptr(ca, _f32(), "ca"), ctypes.byref(dims),
+        _ptr(seq_lens, _i32(), "seq_lens"), int(topk), _ptr(ca, _f32(), "ca"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), ctypes.byref(dims),
         _stream(stream)))
 
 

@@ -132,6 +132,32 @@ def test_fc_agreement_exact_on_integer_inputs():
                             k[b, h, :lens[b]].astype(np.float64), K, exact=True)
 
 
+@pytest.mark.parametrize("case", ["large_k", "sample_misses"])
+def test_fc_agreement_threshold_fallbacks(case):
+    """The threshold search falls back to a select over whole rows when the
+    candidate list overflows (a large K') or holds fewer than K' keys (every
+    16th token scores far above the rest, so the sample overestimates the
+    K'-th score).  Integer inputs: the result equals the oracle's exactly."""
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for
+    cfg = configs.CONFIGS["llama3_8b_ctx32k"].with_(context=8192, batch=1, n_q_heads=4, n_kv_heads=1)
+    rng = np.random.default_rng(5)
+    T, d = cfg.context, cfg.head_dim
+    if case == "large_k":
+        k = rng.integers(-4, 5, size=(1, 1, T, d)).astype(np.float32)
+        q = rng.integers(-3, 4, size=(1, 4, d)).astype(np.float32)
+        K = 3000
+    else:
+        k = rng.integers(-1, 2, size=(1, 1, T, d)).astype(np.float32)
+        k[0, 0, ::16] = 4.0
+        q = np.ones((1, 4, d), dtype=np.float32)
+        K = 2000
+    k_d = torch.from_numpy(k).cuda().to(torch.bfloat16)
+    lens_d = torch.tensor([T], dtype=torch.int32, device="cuda")
+    ca = _gpu_ca(torch.from_numpy(q).cuda(), k_d, lens_d, K, dims_for(cfg)).cpu().numpy()
+    _check_unit(ca[0, 0], q[0].astype(np.float64), k[0, 0].astype(np.float64), K, exact=True)
+
+
 def test_select_dominant_equals_oracle_with_ties():
     import torch
     from kv_cache_token_tip_gb300 import dims_for, fasa_select_dominant_fcs
@@ -187,11 +213,14 @@ def test_fc_agreement_rejects_bad_arguments():
     with pytest.raises(FasaError) as e:
         fasa_fc_agreement(q_rot, L.k, L.seq_lens, 0, ca, dims_for(cfg))
     assert e.value.status == 1
-    # a context longer than one CTA's shared memory holds (the call returns
-    # before any launch)
+    # a workspace smaller than the size query asks for
+    from kv_cache_token_tip_gb300 import fasa_fc_agreement_workspace_size
+    n = fasa_fc_agreement_workspace_size(dims_for(cfg))
+    assert n == cfg.batch * cfg.n_kv_heads * (cfg.head_dim // 2 + 1) * (cfg.context + cfg.context // 32) * 4
+    short = torch.empty(n - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(FasaError) as e:
-        fasa_fc_agreement(q_rot, L.k, L.seq_lens, 64, ca, dims_for(cfg.with_(context=131072)))
-    assert e.value.status == 2
+        fasa_fc_agreement(q_rot, L.k, L.seq_lens, 64, ca, dims_for(cfg), workspace=short)
+    assert e.value.status == 3
     dom = torch.empty((cfg.n_kv_heads, 65), dtype=torch.int32, device="cuda")
     with pytest.raises(FasaError) as e:
         fasa_select_dominant_fcs(ca[0], 65, dom, dims_for(cfg))
