@@ -4,7 +4,7 @@
 // calibration procedure, Algorithm 1).
 //
 // Three launches per call, so that K is read once:
-//   ca_scores_kernel   one CTA per (64-token tile, batch b, KV head h): streams
+//   ca_scores_kernel   one CTA per (128-token tile, batch b, KV head h): streams
 //                      the tile's key rows once and writes, per token, the
 //                      full (group-summed) score and the d/2 single-FC scores
 //                      as order-preserving keys, FC-major, into the workspace;
@@ -40,7 +40,7 @@ namespace {
 constexpr int CA_NT = 256;            // threads of a select CTA
 constexpr int CA_NW = CA_NT / 32;
 constexpr int SC_NT = 256;            // threads of a scoring CTA
-constexpr int SC_TT = 64;             // tokens per scoring CTA (T_max is a multiple of 64)
+constexpr int SC_TT = 128;            // tokens per scoring CTA
 constexpr int CA_CAP = 2048;          // candidate keys per row held in shared memory
 constexpr int CA_STRIDE = 16;         // the threshold sample takes every 16th token
 constexpr int CN_NT = 128;            // threads of a counting CTA
@@ -81,18 +81,24 @@ __device__ int ca_excl_scan(int x, CaScratch* sc, int& total) {
 __device__ void find_bin(const uint32_t* hist, int nb, int kr, CaScratch* sc) {
   const int m = nb / CA_NT;  // thread j owns the m bins counted from the top
   const int base = nb - ((int)threadIdx.x + 1) * m;
+  // the sum starts at a lane-dependent bin so that a warp's reads spread
+  // over the banks (the bins of neighbouring threads are m words apart)
+  const int lane = threadIdx.x & 31;
   int sum = 0;
-  for (int i = 0; i < m; ++i) sum += (int)hist[base + i];
+  for (int i = 0; i < m; ++i) sum += (int)hist[base + ((i + lane) & (m - 1))];
   int total;
   int run = ca_excl_scan(sum, sc, total);
-  for (int i = m - 1; i >= 0; --i) {
-    const int c = (int)hist[base + i];
-    if (run < kr && kr <= run + c) {
-      sc->dstar = base + i;
-      sc->cnt_gt = run;
-      sc->n_eq = c;
+  if (run < kr && kr <= run + sum) {  // the one thread whose bins hold it
+    for (int i = m - 1; i >= 0; --i) {
+      const int c = (int)hist[base + i];
+      if (kr <= run + c) {
+        sc->dstar = base + i;
+        sc->cnt_gt = run;
+        sc->n_eq = c;
+        break;
+      }
+      run += c;
     }
-    run += c;
   }
   __syncthreads();
 }
@@ -207,25 +213,27 @@ __device__ void row_topk_mask(const uint32_t* __restrict__ row, int len, int kk,
     for (int u = 0; u < 4; ++u) {
       const int v = vw + lane + u * CA_NT;
       const uint32_t kx[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
-      int cnt = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) cnt += (4 * v + c < len) && kx[c] >= t0;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int base = 0;
-      if (lane == 31 && incl) base = atomicAdd(&sc->n_cand, incl);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int pos = base + incl - cnt;
+      // one ballot per key slot: slot c of the warp's lanes lands after the
+      // earlier slots, lanes in order (the list order is free)
+      uint32_t bal[4];
+      int tot = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if ((4 * v + c < len) && kx[c] >= t0) {
+        bal[c] = __ballot_sync(0xffffffffu, (4 * v + c < len) && kx[c] >= t0);
+        tot += __popc(bal[c]);
+      }
+      if (tot == 0) continue;  // warp-uniform
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sc->n_cand, tot);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if ((bal[c] >> lane) & 1u) {
+          const int pos = base + __popc(bal[c] & lt);
           if (pos < CA_CAP) list[pos] = make_uint2(kx[c], (uint32_t)(4 * v + c));
-          ++pos;
         }
+        base += __popc(bal[c]);
       }
     }
   }
@@ -379,7 +387,8 @@ __global__ void __launch_bounds__(SC_NT) ca_scores_kernel(const float* __restric
   uint32_t* out = keys + (size_t)unit * (F + 1) * T_max + t0;
   for (int r = warp; r <= F; r += SC_NT / 32) {
 #pragma unroll
-    for (int c = lane; c < SC_TT; c += 32) out[(size_t)r * T_max + c] = ks[r * S + c];
+    for (int c = lane; c < SC_TT; c += 32)
+      if (t0 + c < len) out[(size_t)r * T_max + c] = ks[r * S + c];
   }
 }
 
@@ -458,7 +467,7 @@ cudaError_t launch_fc_agreement(const float* q_rot, const void* k, const int* le
                                 cudaStream_t s) {
   const int units = B * Hkv, F = D / 2;
   uint32_t* keys = static_cast<uint32_t*>(ws);
-  const dim3 grid(T_max / SC_TT, units);
+  const dim3 grid((T_max + SC_TT - 1) / SC_TT, units);
   if (bf16) {
     if (D == 128)
       ca_scores_kernel<__nv_bfloat16, 128><<<grid, SC_NT, 0, s>>>(
