@@ -316,10 +316,26 @@ def ca_from_scores(full: np.ndarray, alpha_i: np.ndarray, K: int) -> float:
 def contextual_agreement_unit(q_rot_group, k_rows, K: int) -> np.ndarray:
     """CA of every FC for one (batch, KV head) and one query group: the full
     head's scores are the sum of the single-FC scores (the FC decomposition
-    of q R k^T).  Returns [d/2]."""
+    of q R k^T).  Returns [d/2]; all ones when no token is cached."""
+    if np.asarray(k_rows).shape[0] == 0:
+        return np.ones(np.asarray(k_rows).shape[1] // 2)
     A = fc_scores_unit(q_rot_group, k_rows)
     full = A.sum(axis=0)
     return np.array([ca_from_scores(full, A[i], K) for i in range(A.shape[0])])
+
+
+def compound_agreement_unit(q_rot_group, k_rows, dom_fc, K: int) -> float:
+    """Compound CA of a chosen FC set I_dom for one (batch, KV head): Eq. 4
+    with alpha_i replaced by the summed scores of the chosen FCs -- the
+    statistic the CA page reports for the dominant sets (its Table 1), and
+    the TIP score S of the same set -- against the full head's scores.
+    1 when no token is cached."""
+    if np.asarray(k_rows).shape[0] == 0:
+        return 1.0
+    A = fc_scores_unit(q_rot_group, k_rows)
+    full = A.sum(axis=0)
+    chosen = A[np.asarray(dom_fc, dtype=np.int64)].sum(axis=0)
+    return ca_from_scores(full, chosen, K)
 
 
 def calibrate_dominant_fcs(ca_mean: np.ndarray, n_tip: int) -> np.ndarray:

@@ -469,4 +469,53 @@ def check_calibration_selection(o):
     assert np.array_equal(o.calibrate_dominant_fcs(ca, 3), [[1, 2, 3], [0, 2, 3], [0, 1, 2]])
 
 
+def check_ca_without_tokens(o):
+    """Nothing cached: both TopK-I sets are empty, read as full agreement."""
+    q = _rng(59).standard_normal((2, 8))
+    K = np.zeros((0, 8))
+    assert np.array_equal(o.contextual_agreement_unit(q, K, 4), np.ones(4))
+    assert o.compound_agreement_unit(q, K, [1, 2], 4) == 1.0
+
+
+def check_compound_all_fcs_is_one(o):
+    """Choosing every FC sums to the full logits: the two sets coincide."""
+    rng = _rng(61)
+    q = rng.standard_normal((3, 16))
+    K = rng.standard_normal((40, 16))
+    for k in (1, 5, 40, 100):
+        assert o.compound_agreement_unit(q, K, range(8), k) == 1.0
+
+
+def check_compound_single_fc_is_ca(o):
+    """A one-FC set is Eq. 4 itself; a set missing the FC that carries the
+    logits agrees less than the set holding it."""
+    rng = _rng(67)
+    q = rng.standard_normal((3, 16))
+    K = rng.standard_normal((40, 16))
+    ca = o.contextual_agreement_unit(q, K, 5)
+    for i in range(8):
+        assert o.compound_agreement_unit(q, K, [i], 5) == ca[i]
+    assert len(set(ca.tolist())) > 1   # the pin distinguishes the FCs
+    # FC 3 carries the logits (x20): every set holding it reaches 1 here
+    K2 = K.copy()
+    K2[:, 6:8] *= 20.0
+    q2 = q.copy()
+    q2[:, 6:8] *= 20.0
+    assert o.compound_agreement_unit(q2, K2, [1, 3, 5], 5) == 1.0
+    assert o.compound_agreement_unit(q2, K2, [0, 1, 2, 4, 5, 6, 7], 5) < 1.0
+
+
+def check_compound_scores_are_tip_scores(o):
+    """The chosen set's summed scores are the TIP scores of that set."""
+    rng = _rng(71)
+    q = rng.standard_normal((4, 16))
+    K = rng.standard_normal((50, 16))
+    dom = [0, 3, 6]
+    full = K @ q.sum(axis=0)
+    S = o.tip_scores_unit(q, K, dom)
+    for k in (3, 10):
+        expect = len(set(o.topk_select_unit(full, k).tolist()) & set(o.topk_select_unit(S, k).tolist())) / k
+        assert o.compound_agreement_unit(q, K, dom, k) == expect
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -129,6 +129,21 @@ def _ca_fc_vs_itself(q_rot_group, k_rows, K):
     return np.array([O.ca_from_scores(A[i], A[i], K) for i in range(A.shape[0])])
 
 
+def _compound_drops_last(q_rot_group, k_rows, dom_fc, K):
+    if np.asarray(k_rows).shape[0] == 0:
+        return 1.0
+    A = O.fc_scores_unit(q_rot_group, k_rows)
+    dom = list(dom_fc)
+    dom = dom[:-1] if len(dom) > 1 else dom
+    return O.ca_from_scores(A.sum(axis=0), A[np.asarray(dom, dtype=np.int64)].sum(axis=0), K)
+
+
+def _compound_vs_itself(q_rot_group, k_rows, dom_fc, K):
+    A = O.fc_scores_unit(q_rot_group, k_rows)
+    s = A[np.asarray(list(dom_fc), dtype=np.int64)].sum(axis=0)
+    return O.ca_from_scores(s, s, K)
+
+
 MUTATIONS = {
     "rope_row_vector_sign": ("rope_rotate", _rope_row_convention),
     "rope_rotate_half_pairing": ("rope_rotate", _rope_rotate_half),
@@ -142,6 +157,8 @@ MUTATIONS = {
     "ca_normalised_by_t": ("ca_from_scores", _ca_over_t),
     "calibration_keeps_lowest_ca": ("calibrate_dominant_fcs", _calibrate_lowest),
     "ca_compares_fc_with_itself": ("contextual_agreement_unit", _ca_fc_vs_itself),
+    "compound_drops_last_fc": ("compound_agreement_unit", _compound_drops_last),
+    "compound_compares_set_with_itself": ("compound_agreement_unit", _compound_vs_itself),
 }
 
 
