@@ -45,7 +45,7 @@ __all__ = [
     "tip_score", "topk_select", "focused_attention", "dense_attention",
     "decode_step", "append_token", "decode_step_append", "build_kdom", "bytes_fraction",
     "theoretical_speedup", "fc_scores_unit", "ca_from_scores", "contextual_agreement_unit",
-    "calibrate_dominant_fcs",
+    "calibrate_dominant_fcs", "compound_agreement_unit", "dominant_set",
 ]
 
 
@@ -174,9 +174,24 @@ def _group(n_q_heads: int, n_kv_heads: int) -> int:
     return n_q_heads // n_kv_heads
 
 
+def dominant_set(dom_row) -> list:
+    """I_dom of one KV head from its row of the dominant-FC table: the entries
+    before the first negative one.  A negative entry marks an unused slot, so
+    the heads of one layer may keep different numbers of FCs (the per-head
+    N_tip the FASA pages propose under "Layer-wise and head-wise N_tip
+    optimization"); a row without negative entries is used whole."""
+    out = []
+    for i in dom_row:
+        if int(i) < 0:
+            break
+        out.append(int(i))
+    return out
+
+
 def tip_score(q_rot, K, dom_fc, seq_lens) -> np.ndarray:
-    """q_rot [B,Hq,d], K [B,Hkv,T,d] fp64, dom_fc [Hkv,n], seq_lens [B]
-    -> scores [B,Hkv,T] (NaN at tau >= len_b)."""
+    """q_rot [B,Hq,d], K [B,Hkv,T,d] fp64, dom_fc [Hkv,n] (per-head sets as
+    dominant_set reads them), seq_lens [B] -> scores [B,Hkv,T] (NaN at
+    tau >= len_b)."""
     B, Hq, d = q_rot.shape
     Hkv, T = K.shape[1], K.shape[2]
     G = _group(Hq, Hkv)
@@ -184,7 +199,7 @@ def tip_score(q_rot, K, dom_fc, seq_lens) -> np.ndarray:
     for b in range(B):
         L = int(seq_lens[b])
         for h in range(Hkv):
-            out[b, h, :L] = tip_scores_unit(q_rot[b, h * G:(h + 1) * G], K[b, h, :L], dom_fc[h])
+            out[b, h, :L] = tip_scores_unit(q_rot[b, h * G:(h + 1) * G], K[b, h, :L], dominant_set(dom_fc[h]))
     return out
 
 
@@ -272,14 +287,17 @@ def build_kdom(K_stored: np.ndarray, dom_fc: np.ndarray, block: int = 64) -> np.
     `block` tokens: [B, Hkv, T/block, n, block, 2].
 
     K_dom[b,h,t//block,j,t%block,:] = K[b,h,t, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2]
-    (a copy; the FC pair is never split).
+    (a copy; the FC pair is never split).  Unused slots (negative entries)
+    hold zeros here; the library leaves them untouched.
     """
     B, Hkv, T, _ = K_stored.shape
     n = dom_fc.shape[1]
-    out = np.empty((B, Hkv, T // block, n, block, 2), dtype=K_stored.dtype)
+    out = np.zeros((B, Hkv, T // block, n, block, 2), dtype=K_stored.dtype)
     for h in range(Hkv):
         for j in range(n):
             i = int(dom_fc[h, j])
+            if i < 0:
+                continue
             cols = K_stored[:, h, :, 2 * i:2 * i + 2]           # [B, T, 2]
             out[:, h, :, j, :, :] = cols.reshape(B, T // block, block, 2)
     return out
@@ -334,7 +352,7 @@ def compound_agreement_unit(q_rot_group, k_rows, dom_fc, K: int) -> float:
         return 1.0
     A = fc_scores_unit(q_rot_group, k_rows)
     full = A.sum(axis=0)
-    chosen = A[np.asarray(dom_fc, dtype=np.int64)].sum(axis=0)
+    chosen = A[np.asarray(dominant_set(dom_fc), dtype=np.int64)].sum(axis=0)
     return ca_from_scores(full, chosen, K)
 
 

@@ -518,4 +518,35 @@ def check_compound_scores_are_tip_scores(o):
         assert o.compound_agreement_unit(q, K, dom, k) == expect
 
 
+# --- per-head ragged N_tip ---------------------------------------------------
+def check_dominant_set_reading(o):
+    assert o.dominant_set([3, 5, -1, -1]) == [3, 5]
+    assert o.dominant_set([1, -1, 2]) == [1]
+    assert o.dominant_set([-1, 2]) == []
+    assert o.dominant_set(np.array([4, 0, 7], dtype=np.int32)) == [4, 0, 7]
+
+
+def check_ragged_tip_closed_form(o):
+    """Heads keeping 1 and 3 FCs: each head's scores are its own FCs' query
+    columns (group-summed) times the key columns -- a matrix product."""
+    rng = _rng(73)
+    B, Hq, Hkv, T, d = 1, 4, 2, 20, 16
+    q = rng.standard_normal((B, Hq, d))
+    K = rng.standard_normal((B, Hkv, T, d))
+    dom = np.array([[5, -1, -1], [0, 2, 7]], dtype=np.int32)
+    s = o.tip_score(q, K, dom, np.array([T]))
+    for h, fcs in ((0, [5]), (1, [0, 2, 7])):
+        cols = np.concatenate([[2 * i, 2 * i + 1] for i in fcs])
+        qbar = q[0, 2 * h:2 * h + 2].sum(axis=0)
+        assert np.allclose(s[0, h], K[0, h][:, cols] @ qbar[cols], rtol=1e-12, atol=1e-12)
+
+
+def check_ragged_kdom_slots(o):
+    K = _rng(79).standard_normal((1, 2, 64, 8))
+    kd = o.build_kdom(K, np.array([[3, -1], [1, 2]], dtype=np.int32))
+    assert np.array_equal(kd[0, 0, 0, 0], K[0, 0, :, 6:8])
+    assert np.all(kd[0, 0, 0, 1] == 0)
+    assert np.array_equal(kd[0, 1, 0, 1], K[0, 1, :, 4:6])
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

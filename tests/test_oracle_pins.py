@@ -81,10 +81,12 @@ def _freq_half_exponent(rope_theta, d):
 def _kdom_wrong_pair(K_stored, dom_fc, block=64):
     B, H, T, _ = K_stored.shape
     n = dom_fc.shape[1]
-    out = np.empty((B, H, T // block, n, block, 2), dtype=K_stored.dtype)
+    out = np.zeros((B, H, T // block, n, block, 2), dtype=K_stored.dtype)
     for h in range(H):
         for j in range(n):
             i = int(dom_fc[h, j])
+            if i < 0:
+                continue
             out[:, h, :, j] = K_stored[:, h, :, i:i + 2].reshape(B, T // block, block, 2)
     return out
 
@@ -144,6 +146,14 @@ def _compound_vs_itself(q_rot_group, k_rows, dom_fc, K):
     return O.ca_from_scores(s, s, K)
 
 
+def _dominant_set_skips_gaps(dom_row):
+    return [int(i) for i in dom_row if int(i) >= 0]
+
+
+def _dominant_set_sentinel_as_fc0(dom_row):
+    return [max(int(i), 0) for i in dom_row]
+
+
 MUTATIONS = {
     "rope_row_vector_sign": ("rope_rotate", _rope_row_convention),
     "rope_rotate_half_pairing": ("rope_rotate", _rope_rotate_half),
@@ -159,6 +169,8 @@ MUTATIONS = {
     "ca_compares_fc_with_itself": ("contextual_agreement_unit", _ca_fc_vs_itself),
     "compound_drops_last_fc": ("compound_agreement_unit", _compound_drops_last),
     "compound_compares_set_with_itself": ("compound_agreement_unit", _compound_vs_itself),
+    "ragged_set_reads_past_the_sentinel": ("dominant_set", _dominant_set_skips_gaps),
+    "ragged_sentinel_taken_as_fc0": ("dominant_set", _dominant_set_sentinel_as_fc0),
 }
 
 
