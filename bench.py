@@ -48,18 +48,21 @@ CA_METRIC = "FC calibration (Contextual Agreement of every FC): achieved HBM TB/
 # ----------------------------------------------------------------------------
 # Byte model (FASA-C memory movement, per step)
 # ----------------------------------------------------------------------------
-def algorithmic_bytes(cfg, lens) -> dict:
-    """Bytes one decode step must move: every cached token's dominant-FC key
-    columns (TIP), the selected K and V rows (FAC), the query, the fp32 output
-    and the small index tables."""
+def algorithmic_bytes(cfg, lens, budget=None) -> dict:
+    """Bytes one layer's decode step must move: every cached token's
+    dominant-FC key columns (TIP; each head its own count of FCs), the
+    selected K and V rows (FAC), the query, the fp32 output and the small
+    index tables."""
     es = cfg.elem_bytes
-    H, d, n = cfg.n_kv_heads, cfg.head_dim, cfg.n_tip
+    H, d = cfg.n_kv_heads, cfg.head_dim
+    n_sum = sum(cfg.head_n_tip(h) for h in range(H))
+    budget = cfg.budget if budget is None else budget
     lens = np.asarray(lens, dtype=np.int64)
-    tip = int(np.sum(lens) * H * n * 2 * es)
-    sel = int(np.sum(np.minimum(lens, cfg.budget)) * H * 2 * d * es)
+    tip = int(np.sum(lens) * n_sum * 2 * es)
+    sel = int(np.sum(np.minimum(lens, budget)) * H * 2 * d * es)
     q = cfg.batch * cfg.n_q_heads * d * es
     out = cfg.batch * cfg.n_q_heads * d * 4
-    small = H * n * 4 + 2 * cfg.batch * 4
+    small = H * cfg.n_tip * 4 + 2 * cfg.batch * 4   # the dominant-FC table and the lengths
     dense = int(np.sum(lens) * H * 2 * d * es) + q + out + 2 * cfg.batch * 4
     return dict(tip=tip, fac=sel, q=q, out=out, small=small,
                 total=tip + sel + q + out + small, dense_total=dense)
@@ -200,10 +203,10 @@ def max_over_ranks(pg, x: float) -> float:
 # ----------------------------------------------------------------------------
 # CPU oracle leg (bounded sample)
 # ----------------------------------------------------------------------------
-def unit_bytes(cfg, L: int) -> int:
-    """Algorithmic bytes of one (batch, KV head) unit of length L."""
+def unit_bytes(cfg, L: int, h: int = 0) -> int:
+    """Algorithmic bytes of one (batch, KV head h) unit of length L."""
     es, G, d = cfg.elem_bytes, cfg.group, cfg.head_dim
-    return L * cfg.n_tip * 2 * es + min(L, cfg.budget) * 2 * d * es + G * d * es + G * d * 4
+    return L * cfg.head_n_tip(h) * 2 * es + min(L, cfg.budget) * 2 * d * es + G * d * es + G * d * 4
 
 
 def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 2):
@@ -225,7 +228,8 @@ def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: 
         kk, vv = synth.gen_kv_head(cfg, 0, b, h, t_count=L)
         K = O.decode_stored(synth.store(kk, cfg.dtype), cfg.dtype)
         V = O.decode_stored(synth.store(vv, cfg.dtype), cfg.dtype)
-        units.append((q_all[b, h * G:(h + 1) * G], int(lens[b]), K, V, dom[h], unit_bytes(cfg, L)))
+        units.append((q_all[b, h * G:(h + 1) * G], int(lens[b]), K, V, O.dominant_set(dom[h]),
+                      unit_bytes(cfg, L, h)))
 
     def one(i):
         q, pos, K, V, dfc, nb = units[i % len(units)]
@@ -336,12 +340,15 @@ def run_gpu(args):
     cfg = configs.CONFIGS[args.workload]
     dims = dims_for(cfg)
     lens = synth.seq_lens(cfg)
-    model = algorithmic_bytes(cfg, lens)
-    if args.append:  # the new token's K and V rows and K_dom entries are written
-        model["append"] = cfg.batch * cfg.n_kv_heads * (2 * cfg.head_dim + 2 * cfg.n_tip) * cfg.elem_bytes
-        model["total"] += model["append"]
     layers = cfg.layers          # a decode step runs every layer: one launch each
-    per_step = model["total"] * layers
+    # the byte model summed over the layers (each layer its own budget)
+    per_layer = [algorithmic_bytes(cfg, lens, cfg.layer_budget(l)) for l in range(layers)]
+    model = {kk: sum(m[kk] for m in per_layer) / layers for kk in per_layer[0]}
+    if args.append:  # the new token's K and V rows and K_dom entries are written
+        model["append"] = cfg.batch * sum(2 * cfg.head_dim + 2 * cfg.head_n_tip(h)
+                                          for h in range(cfg.n_kv_heads)) * cfg.elem_bytes
+        model["total"] += model["append"]
+    per_step = int(round(model["total"] * layers))
     if layers > 1:
         R = layers               # one replica per layer, launched in order
     else:
@@ -378,12 +385,13 @@ def run_gpu(args):
 
     def step(i):
         L, kd = reps[i % R]
+        kl = cfg.layer_budget(i % layers)
         if args.append:
             kn, vn, lens_m1 = app[i % R]
-            fasa_decode_step_append(L.q, kn, vn, lens_m1, L.k, L.v, kd, L.dom_fc, k, outs[i % R],
+            fasa_decode_step_append(L.q, kn, vn, lens_m1, L.k, L.v, kd, L.dom_fc, kl, outs[i % R],
                                     None, None, ws, dims, stream=stream)
         else:
-            fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, k, outs[i % R],
+            fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, kl, outs[i % R],
                              None, None, ws, dims, stream=stream)
 
     # dense comparison: the same kernels over every cached row
@@ -472,7 +480,8 @@ def run_gpu(args):
     def e2e_step(r):
         L, kd = reps[r]
         d_in[r].copy_(h_in[r], non_blocking=True)
-        fasa_decode_step(d_q[r], d_pos[r], L.k, L.v, kd, L.dom_fc, d_lens[r], k, outs[r], None, None, ws, dims,
+        fasa_decode_step(d_q[r], d_pos[r], L.k, L.v, kd, L.dom_fc, d_lens[r], cfg.layer_budget(r % layers),
+                         outs[r], None, None, ws, dims,
                          stream=stream)
         h_out[r].copy_(outs[r], non_blocking=True)
 
@@ -543,6 +552,10 @@ def run_gpu(args):
             "data": "synthetic (seeded; pre-RoPE q/k ~ N(0,1) with x8 outlier FCs, v ~ N(0,1))",
             "config": {"workload": cfg.name, "batch": B, "q_heads": Hq, "kv_heads": H, "head_dim": d,
                        "context": cfg.context, "n_tip": cfg.n_tip, "budget": k, "rope_theta": cfg.rope_theta,
+                       **({"n_tip_per_head": list(cfg.n_tip_per_head)} if cfg.n_tip_per_head else {}),
+                       **({"budget_per_layer": f"{cfg.budget_per_layer[0]} .. {cfg.budget_per_layer[-1]} "
+                                               f"(mean {np.mean(cfg.budget_per_layer):.0f})"}
+                          if cfg.budget_per_layer else {}),
                        "cluster_ctas": C, "replicas": R,
                        "l2": f"{'inputs larger than L2' if R * per_step > L2_BYTES else 'NOT larger than L2 (profiling run)'}: "
                              f"{R} replicas x {per_step / 1e6:.2f} MB/step "
@@ -558,12 +571,13 @@ def run_gpu(args):
                                        if args.fasa_m else "device memory",
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": per_step,
-            **({"fasa_m": {"link_bytes_per_step": model["fac"] * layers,
+            **({"fasa_m": {"link_bytes_per_step": int(round(model["fac"] * layers)),
                            "link_gbs": round(model["fac"] * layers / sec_per_step / 1e9, 1),
                            "hbm_bytes_not_held_per_replica": int(2 * reps[0][0].k.numel()
                                                                  * reps[0][0].k.element_size())}}
                if args.fasa_m else {}),
-            "bytes_breakdown": {kk: model[kk] * layers for kk in ("tip", "fac", "q", "out", "small", "append")
+            "bytes_breakdown": {kk: int(round(model[kk] * layers))
+                                for kk in ("tip", "fac", "q", "out", "small", "append")
                                 if kk in model},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),

@@ -37,7 +37,16 @@
  *      k_dom     [B, Hkv, T_max/64, n_tip, 64, 2]  storage dtype: the
  *                                      dominant key columns, FC-major within
  *                                      blocks of 64 tokens
- *      dom_fc    [Hkv, n_tip]          int32, dominant FC indices in [0, d/2)
+ *      dom_fc    [Hkv, n_tip]          int32, dominant FC indices in [0, d/2);
+ *                                      a negative entry marks an unused
+ *                                      slot: head h's set I_dom is its
+ *                                      entries before the first negative one
+ *                                      (at least one), so heads may keep
+ *                                      different numbers of FCs (the per-head
+ *                                      N_tip of the FASA pages' "Layer-wise
+ *                                      and head-wise N_tip optimization").
+ *                                      n_tip is the longest set; a head with
+ *                                      fewer FCs reads only its planes.
  *      seq_lens  [B]                   int32, cached tokens 0..len-1
  *      scores    [B, Hkv, T_max]       fp32 (entries tau >= len unspecified)
  *      idx       [B, Hkv, budget]      int32, ascending; -1 past count
@@ -128,7 +137,9 @@ int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot,
  * of 64 tokens: k_dom[b,h,tau/64,j,tau%64,0:2] =
  * k_cache[b,h,tau, 2*dom_fc[h,j] : 2*dom_fc[h,j]+2] for tau < seq_lens[b]
  * (all tau < T_max when seq_lens is NULL).  A pure copy; one tile of whole
- * blocks is one contiguous range, so the TIP stage moves it with one bulk copy.
+ * blocks is one contiguous range, so the TIP stage moves it with one bulk copy
+ * (a head keeping fewer FCs: one copy of its leading planes per block).
+ * Unused slots (negative entries) are left untouched.
  */
 int fasa_build_kdom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens,
                     void* k_dom, const fasa_dims_t* dims, fasa_stream_t stream);
@@ -240,6 +251,20 @@ int fasa_fc_agreement_workspace_size(const fasa_dims_t* dims, size_t* bytes);
 int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* seq_lens, int32_t topk,
                       float* ca, void* workspace, size_t workspace_bytes, const fasa_dims_t* dims,
                       fasa_stream_t stream);
+
+/*
+ * Compound CA of a chosen FC set (the statistic the CA page reports for the
+ * dominant sets, its Table 1): Eq. 4 with alpha_i replaced by the summed
+ * scores of the FCs in head h's set (dom_fc[h, :] read as above) -- the TIP
+ * scores of that set:
+ *   cca[b,h] = |TopK-I(full, K') & TopK-I(sum_{i in dom} alpha_i, K')| / K'.
+ * Arguments as for fasa_fc_agreement; dom_fc int32 [Hkv, n_tip] (device),
+ * entries >= d/2 are skipped and set FASA_DEV_BAD_INPUT; cca
+ * fp32 [B, Hkv] (out).  Uses the same workspace (its size query suffices).
+ */
+int fasa_compound_agreement(const float* q_rot, const void* k_cache, const int32_t* dom_fc,
+                            const int32_t* seq_lens, int32_t topk, float* cca, void* workspace,
+                            size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
  * Algorithm 1, last step: dom_fc[h, 0..n_tip) = the n_tip FCs of highest

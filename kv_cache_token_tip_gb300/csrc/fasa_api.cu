@@ -361,9 +361,10 @@ __global__ void build_kdom_kernel(const T* K, const int* dom, const int* lens, T
            tau % KDOM_BLOCK;
   for (int j = 0; j < n; ++j) {
     int i = dom[h * n + j];
-    if (i < 0 || i >= D / 2) {
+    if (i < 0) continue;  // an unused slot of a head keeping fewer FCs
+    if (i >= D / 2) {
       atomicOr(status, 1);
-      i = min(max(i, 0), D / 2 - 1);
+      i = D / 2 - 1;
     }
     dst[(size_t)j * KDOM_BLOCK] = row[i];
   }
@@ -385,9 +386,10 @@ __global__ void append_kdom_kernel(const T* k_new, const int* dom, const int* to
            t % KDOM_BLOCK;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
     int i = dom[h * n + j];
-    if (i < 0 || i >= D / 2) {
+    if (i < 0) continue;  // an unused slot of a head keeping fewer FCs
+    if (i >= D / 2) {
       atomicOr(status, 1);
-      i = min(max(i, 0), D / 2 - 1);
+      i = D / 2 - 1;
     }
     dst[(size_t)j * KDOM_BLOCK] = row[i];
   }
@@ -685,9 +687,29 @@ int fasa_fc_agreement(const float* q_rot, const void* k_cache, const int32_t* se
   DevInfo di;
   st = device_info(&di);
   if (st) return st;
-  const cudaError_t e = launch_fc_agreement(q_rot, k_cache, seq_lens, topk, ca, dims->batch, dims->n_q_heads,
-                                            dims->n_kv_heads, dims->head_dim, dims->t_max, dims->dtype == FASA_BF16,
-                                            workspace, di.status, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_fc_agreement(q_rot, k_cache, seq_lens, nullptr, 0, topk, ca, dims->batch,
+                                            dims->n_q_heads, dims->n_kv_heads, dims->head_dim, dims->t_max,
+                                            dims->dtype == FASA_BF16, workspace, di.status,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+int fasa_compound_agreement(const float* q_rot, const void* k_cache, const int32_t* dom_fc,
+                            const int32_t* seq_lens, int32_t topk, float* cca, void* workspace,
+                            size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q_rot || !k_cache || !dom_fc || !seq_lens || !cca || topk < 1) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(q_rot)) return FASA_ERR_INVALID_ARG;
+  const size_t need = fc_agreement_workspace(dims->batch * dims->n_kv_heads, dims->head_dim, dims->t_max);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASA_ERR_WORKSPACE;
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  const cudaError_t e = launch_fc_agreement(q_rot, k_cache, seq_lens, dom_fc, dims->n_tip, topk, cca, dims->batch,
+                                            dims->n_q_heads, dims->n_kv_heads, dims->head_dim, dims->t_max,
+                                            dims->dtype == FASA_BF16, workspace, di.status,
+                                            reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);
 }
 

@@ -328,13 +328,18 @@ __device__ void decode_raw(const uint32_t (&u)[E * sizeof(T) / 4], float (&x)[E]
   }
 }
 
-template <typename T, int D>
+// COMPOUND: two rows per unit instead of d/2 + 1 -- the summed scores of the
+// chosen FCs dom_fc[h, 0..n_tip) (row 0) and the full scores (row 1).
+template <typename T, int D, bool COMPOUND>
 __global__ void __launch_bounds__(SC_NT) ca_scores_kernel(const float* __restrict__ q_rot, const T* __restrict__ k,
-                                                           const int* __restrict__ seq_lens, uint32_t* keys, int Hq,
-                                                           int Hkv, int T_max, int* status) {
+                                                           const int* __restrict__ seq_lens,
+                                                           const int* __restrict__ dom_fc, int n_tip, uint32_t* keys,
+                                                           int Hq, int Hkv, int T_max, int* status) {
   constexpr int F = D / 2, E = D / 32, S = SC_TT + 1;
+  constexpr int R = COMPOUND ? 2 : F + 1;  // key rows per unit; the full scores are row R - 1
   __shared__ float qs[D];
-  __shared__ uint32_t ks[(F + 1) * S];
+  __shared__ uint32_t ks[R * S];
+  __shared__ unsigned long long dmask;
   const int unit = blockIdx.y, t0 = blockIdx.x * SC_TT;
   const int b = unit / Hkv, h = unit - b * Hkv;
   const int G = Hq / Hkv;
@@ -361,6 +366,16 @@ __global__ void __launch_bounds__(SC_NT) ca_scores_kernel(const float* __restric
       if (g < G) a += q_rot[((size_t)b * Hq + (size_t)h * G + g) * D + d];
     qs[d] = a;
   }
+  if (COMPOUND && tid == 0) {
+    unsigned long long m = 0ull;
+    for (int j = 0; j < n_tip; ++j) {  // the head's set: the entries before the first negative one
+      const int i = dom_fc[(size_t)h * n_tip + j];
+      if (i < 0) break;
+      if (i < F) m |= 1ull << i;
+      else if (blockIdx.x == 0) atomicOr(status, 1);
+    }
+    dmask = m;
+  }
   __syncthreads();
   float qr[E];
 #pragma unroll
@@ -372,29 +387,38 @@ __global__ void __launch_bounds__(SC_NT) ca_scores_kernel(const float* __restric
     if (t0 + c >= len) continue;  // warp-uniform
     float x[E];
     decode_raw<T, E>(u[j], x);
-    float full = 0.f;
+    float full = 0.f, comp = 0.f;
 #pragma unroll
     for (int f = 0; f < E / 2; ++f) {
       const float a = fmaf(qr[2 * f], x[2 * f], qr[2 * f + 1] * x[2 * f + 1]);
-      ks[(lane * (E / 2) + f) * S + c] = score_key(a);
+      if constexpr (COMPOUND) {
+        if ((dmask >> (lane * (E / 2) + f)) & 1ull) comp += a;
+      } else {
+        ks[(lane * (E / 2) + f) * S + c] = score_key(a);
+      }
       full += a;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) full += __shfl_xor_sync(0xffffffffu, full, o);
-    if (lane == 0) ks[F * S + c] = score_key(full);
+    if constexpr (COMPOUND) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) comp += __shfl_xor_sync(0xffffffffu, comp, o);
+      if (lane == 0) ks[c] = score_key(comp);
+    }
+    if (lane == 0) ks[(R - 1) * S + c] = score_key(full);
   }
   __syncthreads();
-  uint32_t* out = keys + (size_t)unit * (F + 1) * T_max + t0;
-  for (int r = warp; r <= F; r += SC_NT / 32) {
+  uint32_t* out = keys + (size_t)unit * R * T_max + t0;
+  for (int r = warp; r < R; r += SC_NT / 32) {
 #pragma unroll
     for (int c = lane; c < SC_TT; c += 32)
       if (t0 + c < len) out[(size_t)r * T_max + c] = ks[r * S + c];
   }
 }
 
-// One CTA per (key row: FC 0..F-1 or the full scores F, unit).
+// One CTA per (key row r < R, unit).
 __global__ void __launch_bounds__(CA_NT, 4) ca_select_kernel(const uint32_t* __restrict__ keys,
-                                                           const int* __restrict__ seq_lens, int K, int F, int Hkv,
+                                                           const int* __restrict__ seq_lens, int K, int R, int Hkv,
                                                            int T_max, uint32_t* masks) {
   __shared__ uint32_t hist[4096];
   __shared__ uint2 list[CA_CAP];
@@ -403,14 +427,16 @@ __global__ void __launch_bounds__(CA_NT, 4) ca_select_kernel(const uint32_t* __r
   const int len = clamp_len(seq_lens, unit / Hkv, T_max);
   const int kk = min(K, len);
   if (kk == 0) return;
-  const size_t row = (size_t)unit * (F + 1) + r;
+  const size_t row = (size_t)unit * R + r;
   row_topk_mask(keys + row * T_max, len, kk, hist, list, &sc, masks + row * (T_max / 32));
 }
 
-// One CTA per (FC i, unit): CA = popcount(mask_i & mask_full) / K'.
+// One CTA per (row i < R - 1, unit): popcount(mask_i & mask_full) / K', the
+// full scores being row R - 1; written to ca[unit * (R - 1) + i].
 __global__ void __launch_bounds__(CN_NT) ca_count_kernel(const uint32_t* __restrict__ masks,
-                                                          const int* __restrict__ seq_lens, int K, int F, int Hkv,
+                                                          const int* __restrict__ seq_lens, int K, int R, int Hkv,
                                                           int T_max, float* ca) {
+  const int F = R - 1;
   __shared__ int part[CN_NT / 32];
   const int i = blockIdx.x, unit = blockIdx.y;
   const int len = clamp_len(seq_lens, unit / Hkv, T_max);
@@ -419,8 +445,8 @@ __global__ void __launch_bounds__(CN_NT) ca_count_kernel(const uint32_t* __restr
     if (threadIdx.x == 0) ca[(size_t)unit * F + i] = 1.f;
     return;
   }
-  const uint32_t* mi = masks + ((size_t)unit * (F + 1) + i) * (T_max / 32);
-  const uint32_t* mf = masks + ((size_t)unit * (F + 1) + F) * (T_max / 32);
+  const uint32_t* mi = masks + ((size_t)unit * R + i) * (T_max / 32);
+  const uint32_t* mf = masks + ((size_t)unit * R + F) * (T_max / 32);
   const int nw = (len + 31) >> 5;
   int both = 0;
   for (int w = threadIdx.x; w < nw; w += CN_NT) both += __popc(__ldg(mi + w) & __ldg(mf + w));
@@ -462,30 +488,34 @@ size_t fc_agreement_workspace(int units, int D, int T_max) {
   return (size_t)units * (D / 2 + 1) * ((size_t)T_max + T_max / 32) * 4;
 }
 
-cudaError_t launch_fc_agreement(const float* q_rot, const void* k, const int* lens, int K, float* ca, int B,
-                                int Hq, int Hkv, int D, int T_max, bool bf16, void* ws, int* status,
-                                cudaStream_t s) {
-  const int units = B * Hkv, F = D / 2;
+cudaError_t launch_fc_agreement(const float* q_rot, const void* k, const int* lens, const int* dom_fc, int n_tip,
+                                int K, float* ca, int B, int Hq, int Hkv, int D, int T_max, bool bf16, void* ws,
+                                int* status, cudaStream_t s) {
+  const int units = B * Hkv;
+  const bool comp = dom_fc != nullptr;
+  const int R = comp ? 2 : D / 2 + 1;
   uint32_t* keys = static_cast<uint32_t*>(ws);
   const dim3 grid((T_max + SC_TT - 1) / SC_TT, units);
+#define FASA_CA_SCORES(TT, DD, CC)                                                                             \
+  ca_scores_kernel<TT, DD, CC><<<grid, SC_NT, 0, s>>>(q_rot, static_cast<const TT*>(k), lens, dom_fc, n_tip, keys, \
+                                                      Hq, Hkv, T_max, status)
   if (bf16) {
-    if (D == 128)
-      ca_scores_kernel<__nv_bfloat16, 128><<<grid, SC_NT, 0, s>>>(
-          q_rot, static_cast<const __nv_bfloat16*>(k), lens, keys, Hq, Hkv, T_max, status);
-    else
-      ca_scores_kernel<__nv_bfloat16, 64><<<grid, SC_NT, 0, s>>>(
-          q_rot, static_cast<const __nv_bfloat16*>(k), lens, keys, Hq, Hkv, T_max, status);
+    if (D == 128) {
+      if (comp) FASA_CA_SCORES(__nv_bfloat16, 128, true); else FASA_CA_SCORES(__nv_bfloat16, 128, false);
+    } else {
+      if (comp) FASA_CA_SCORES(__nv_bfloat16, 64, true); else FASA_CA_SCORES(__nv_bfloat16, 64, false);
+    }
   } else {
-    if (D == 128)
-      ca_scores_kernel<float, 128><<<grid, SC_NT, 0, s>>>(q_rot, static_cast<const float*>(k), lens, keys, Hq,
-                                                          Hkv, T_max, status);
-    else
-      ca_scores_kernel<float, 64><<<grid, SC_NT, 0, s>>>(q_rot, static_cast<const float*>(k), lens, keys, Hq,
-                                                         Hkv, T_max, status);
+    if (D == 128) {
+      if (comp) FASA_CA_SCORES(float, 128, true); else FASA_CA_SCORES(float, 128, false);
+    } else {
+      if (comp) FASA_CA_SCORES(float, 64, true); else FASA_CA_SCORES(float, 64, false);
+    }
   }
-  uint32_t* masks = keys + (size_t)units * (F + 1) * T_max;
-  ca_select_kernel<<<dim3(F + 1, units), CA_NT, 0, s>>>(keys, lens, K, F, Hkv, T_max, masks);
-  ca_count_kernel<<<dim3(F, units), CN_NT, 0, s>>>(masks, lens, K, F, Hkv, T_max, ca);
+#undef FASA_CA_SCORES
+  uint32_t* masks = keys + (size_t)units * R * T_max;
+  ca_select_kernel<<<dim3(R, units), CA_NT, 0, s>>>(keys, lens, K, R, Hkv, T_max, masks);
+  ca_count_kernel<<<dim3(R - 1, units), CN_NT, 0, s>>>(masks, lens, K, R, Hkv, T_max, ca);
   return cudaGetLastError();
 }
 

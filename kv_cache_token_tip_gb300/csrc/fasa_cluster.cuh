@@ -61,6 +61,7 @@ struct Misc {
   int bx_off[C_MAX];     // where this CTA's entries go in each CTA
   uint32_t tip_done[4];  // per TIP stage: warps done with it so far (monotonic)
   int tip_last[4];       // per TIP stage: last tile issued into it (-1: none)
+  int nfc;               // this head's dominant-FC count (its leading valid entries)
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -333,7 +334,10 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 
   // Shared-memory set-up first: the release below then has no outstanding
   // global loads to wait for.
-  const int nfc = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
+  // nfc_max: the dominant-FC table's row length and K_dom's plane count; nfc:
+  // this head's count, the entries before the first negative one
+  const int nfc_max = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
+  int nfc = nfc_max;
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) mbar_init(smem_u32(&bars[s]), 1);
     if (flags & F_SELECT) mbar_init(smem_u32(&bars[7]), 1);  // score reload
@@ -364,7 +368,15 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   int len = p.seq_lens[b];
   // with F_APPEND the query sits at the new token's position, len
   const int m_pos = (flags & F_ROPE) ? ((flags & F_APPEND) ? len : p.pos[b]) : 0;
-  const int dom_i = (tid < p.n_tip && (flags & F_TIP)) ? p.dom_fc[h * p.n_tip + tid] : 0;
+  const int dom_i = (tid < nfc_max && (flags & F_TIP)) ? p.dom_fc[h * nfc_max + tid] : 0;
+  if ((flags & F_TIP) && warp == 0) {  // this head's count, from two ballots
+    const int d1 = lane + 32 < nfc_max ? p.dom_fc[h * nfc_max + lane + 32] : 0;
+    const unsigned b0 = __ballot_sync(0xffffffffu, lane < nfc_max && dom_i < 0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && d1 < 0);
+    nfc = b0 ? __ffs(b0) - 1 : (b1 ? 31 + __ffs(b1) : nfc_max);
+    nfc = max(nfc, 1);  // an empty set: slot 0 is used (and reported by the check below)
+    if (lane == 0) ms->nfc = nfc;
+  }
   // F_APPEND: the new token's key and value pairs (thread i < D/2: pair i),
   // loaded here with the other small inputs whichever CTA turns out to own it
   T kn0 = T(0.f), kn1 = T(0.f), vn0 = T(0.f), vn1 = T(0.f);
@@ -431,18 +443,26 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   const int ntiles = do_tip ? (nloc_s + tt - 1) / tt : 0;
   // k_dom is [.., T_max/KB, n_tip, KB, 2]: a tile of whole blocks is one
   // contiguous range, moved by a single bulk copy
+  // (a head using fewer than nfc_max planes takes the leading nfc planes of
+  // each block: one copy per block, packed in the stage)
   const uint32_t fc_row_bytes = (uint32_t)KB * 2 * ES;
-  const uint32_t blk_bytes = (uint32_t)nfc * fc_row_bytes;
-  const uint32_t stage_bytes = (uint32_t)(tt / KB) * blk_bytes;
-  const T* kd_unit = reinterpret_cast<const T*>(p.k_dom) + (size_t)unit * nfc * p.T_max * 2;
-  auto tip_issue = [&](int it) {  // one thread
+  const uint32_t stage_bytes = (uint32_t)(tt / KB) * nfc_max * fc_row_bytes;
+  const T* kd_unit = reinterpret_cast<const T*>(p.k_dom) + (size_t)unit * nfc_max * p.T_max * 2;
+  auto tip_issue = [&](int it) {  // one thread of warp 0 (its nfc is this head's)
     const int s = it % ns;
     const int tau0 = t0 + it * tt;
     const int nblk = (min(tt, t1s - tau0) + KB - 1) / KB;
-    const uint32_t bytes = (uint32_t)nblk * blk_bytes;
+    const uint32_t blk_bytes = (uint32_t)nfc * fc_row_bytes;
     const uint32_t bar = smem_u32(&bars[s]);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(smem_u32(big + s * stage_bytes), kd_unit + (size_t)(tau0 / KB) * nfc * KB * 2, bytes, bar);
+    mbar_arrive_expect_tx(bar, (uint32_t)nblk * blk_bytes);
+    const T* src = kd_unit + (size_t)(tau0 / KB) * nfc_max * KB * 2;
+    if (nfc == nfc_max) {
+      bulk_g2s(smem_u32(big + s * stage_bytes), src, (uint32_t)nblk * blk_bytes, bar);
+    } else {
+      for (int bi = 0; bi < nblk; ++bi)
+        bulk_g2s(smem_u32(big + s * stage_bytes + bi * blk_bytes), src + (size_t)bi * nfc_max * KB * 2, blk_bytes,
+                 bar);
+    }
     ms->tip_last[s] = it;
   };
   if (tid == 0)
@@ -463,9 +483,10 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     }
   }
   __syncthreads();
+  if (flags & F_TIP) nfc = ms->nfc;
   if (do_tip) {
     for (int j = tid; j < nfc; j += NT) {
-      int i = (j == tid) ? dom_i : p.dom_fc[h * nfc + j];
+      int i = (j == tid) ? dom_i : p.dom_fc[h * nfc_max + j];
       if (i < 0 || i >= D / 2) {
         bad = true;
         i = min(max(i, 0), D / 2 - 1);
@@ -502,8 +523,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       knew[i] = make_float2(to_f32<T>(r0), to_f32<T>(r1));
     }
     __syncthreads();
-    T* kdw = const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc * KB + (t_new % KB)) * 2;
-    auto dom_at = [&](int j) { return min(max(p.dom_fc[h * nfc + j], 0), D / 2 - 1); };
+    T* kdw = const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc_max * KB + (t_new % KB)) * 2;
+    auto dom_at = [&](int j) { return min(max(p.dom_fc[h * nfc_max + j], 0), D / 2 - 1); };
     for (int j = tid; j < nfc; j += NT) {
       const float2 kp = knew[dom_at(j)];
       kdw[(size_t)j * KB * 2] = from_f32<T>(kp.x);

@@ -79,9 +79,11 @@ int max_active_clusters_f32(int flags, int head_dim, int C, int smem_bytes);
 
 // Contextual Agreement and the choice of dominant FCs (fasa_ca.cu).
 size_t fc_agreement_workspace(int units, int D, int T_max);
-cudaError_t launch_fc_agreement(const float* q_rot, const void* k, const int* lens, int K, float* ca, int B,
-                                int Hq, int Hkv, int D, int T_max, bool bf16, void* ws, int* status,
-                                cudaStream_t s);
+// dom_fc null: the CA of every FC (ca [B*Hkv, D/2]); else the compound CA of
+// the n_tip FCs dom_fc[h, :] (ca [B*Hkv]).
+cudaError_t launch_fc_agreement(const float* q_rot, const void* k, const int* lens, const int* dom_fc, int n_tip,
+                                int K, float* ca, int B, int Hq, int Hkv, int D, int T_max, bool bf16, void* ws,
+                                int* status, cudaStream_t s);
 cudaError_t launch_select_dominant(const float* ca_mean, int Hkv, int F, int n, int* dom_fc, cudaStream_t s);
 
 }  // namespace fasa

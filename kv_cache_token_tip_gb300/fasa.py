@@ -21,7 +21,7 @@ EXPORTS = [
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
     "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
-    "fasa_select_dominant_fcs",
+    "fasa_select_dominant_fcs", "fasa_compound_agreement",
 ]
 
 
@@ -91,6 +91,7 @@ def lib():
                                         ctypes.c_int),
             "fasa_fc_agreement_workspace_size": ([dp, ctypes.POINTER(sz)], ctypes.c_int),
             "fasa_fc_agreement": ([vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
+            "fasa_compound_agreement": ([vp, vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_select_dominant_fcs": ([vp, i32, vp, dp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -265,6 +266,20 @@ def fasa_fc_agreement(q_rot, k_cache, seq_lens, topk: int, ca, dims: FasaDims, w
     _check("fasa_fc_agreement", lib().fasa_fc_agreement(
         _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"),
         _ptr(seq_lens, _i32(), "seq_lens"), int(topk), _ptr(ca, _f32(), "ca"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), ctypes.byref(dims),
+        _stream(stream)))
+
+
+def fasa_compound_agreement(q_rot, k_cache, dom_fc, seq_lens, topk: int, cca, dims: FasaDims, workspace=None,
+                            stream=None):
+    """Compound CA of the chosen FCs dom_fc [Hkv, n_tip] per (batch, KV head):
+    cca [B, Hkv] fp32.  Without a workspace one is allocated here."""
+    if workspace is None:
+        import torch
+        workspace = torch.empty(fasa_fc_agreement_workspace_size(dims), dtype=torch.uint8, device=cca.device)
+    _check("fasa_compound_agreement", lib().fasa_compound_agreement(
+        _ptr(q_rot, _f32(), "q_rot"), _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens"), int(topk), _ptr(cca, _f32(), "cca"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), ctypes.byref(dims),
         _stream(stream)))
 

@@ -20,7 +20,7 @@ def oracle_unit(layer, b, h, budget, n_tip=None):
     K = host_f64(layer.k[b, h, :L], cfg.dtype)
     V = host_f64(layer.v[b, h, :L], cfg.dtype)
     q_rot = O.apply_rope_q(q[None], np.array([layer.pos_host[b]]), cfg.rope_theta)[0]
-    dom = layer.dom_fc_host[h]
+    dom = O.dominant_set(layer.dom_fc_host[h])
     s = O.tip_scores_unit(q_rot, K, dom)
     idx = O.topk_select_unit(s, budget)
     out = O.focused_attention_unit(q_rot, K, V, idx)

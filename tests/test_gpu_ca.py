@@ -158,6 +158,57 @@ def test_fc_agreement_threshold_fallbacks(case):
     _check_unit(ca[0, 0], q[0].astype(np.float64), k[0, 0].astype(np.float64), K, exact=True)
 
 
+def _gpu_cca(q_rot, k, dom, lens, K, dims):
+    import torch
+    from kv_cache_token_tip_gb300 import fasa_compound_agreement, fasa_device_status
+    cca = torch.full((dims.batch, dims.n_kv_heads), float("nan"), dtype=torch.float32, device="cuda")
+    fasa_compound_agreement(q_rot, k, dom, lens, K, cca, dims)
+    assert fasa_device_status() == 0
+    return cca.cpu().numpy()
+
+
+def test_compound_agreement_against_oracle():
+    """Compound CA of the layer's dominant sets against the oracle (near-tie
+    band on both boundaries), plus two identities that must hold bit for bit:
+    the set of every FC gives 1, and a one-FC set gives that FC's CA."""
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for, fasa_apply_rope_q
+    cfg = configs.CONFIGS["llama3_8b_ctx32k"].with_(context=8192, batch=3)
+    L = gpu_gen.make_layer(cfg, 0)
+    lens = [8192, 3000, 0]
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    dims = dims_for(cfg)
+    q_rot = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
+    fasa_apply_rope_q(L.q, lens_d, q_rot, dims)
+    K = cfg.budget
+    cca = _gpu_cca(q_rot, L.k, L.dom_fc, lens_d, K, dims)
+    qr = q_rot.cpu().numpy().astype(np.float64)
+    G = cfg.group
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            if lens[b] == 0:
+                assert cca[b, h] == 1.0
+                continue
+            q_g = qr[b, h * G:(h + 1) * G]
+            K_rows = P.host_f64(L.k[b, h, :lens[b]], cfg.dtype)
+            dom = L.dom_fc_host[h]
+            ref = O.compound_agreement_unit(q_g, K_rows, dom, K)
+            A = O.fc_scores_unit(q_g, K_rows)
+            kk = min(K, lens[b])
+            band = _band(A.sum(axis=0), kk) + _band(A[dom].sum(axis=0), kk)
+            assert abs(round(cca[b, h] * kk) - round(ref * kk)) <= band
+    # every FC: the summed scores are the full scores
+    all_fc = torch.arange(cfg.head_dim // 2, dtype=torch.int32, device="cuda").repeat(cfg.n_kv_heads, 1)
+    d_all = dims_for(cfg, n_tip=cfg.head_dim // 2)
+    assert np.all(_gpu_cca(q_rot, L.k, all_fc.contiguous(), lens_d, K, d_all) == 1.0)
+    # one FC per head: equals fasa_fc_agreement's value for that FC
+    ca = _gpu_ca(q_rot, L.k, lens_d, K, dims).cpu().numpy()
+    for i in (0, 17, 63):
+        one = torch.full((cfg.n_kv_heads, 1), i, dtype=torch.int32, device="cuda")
+        got = _gpu_cca(q_rot, L.k, one, lens_d, K, dims_for(cfg, n_tip=1))
+        assert np.array_equal(got, ca[:, :, i])
+
+
 def test_select_dominant_equals_oracle_with_ties():
     import torch
     from kv_cache_token_tip_gb300 import dims_for, fasa_select_dominant_fcs

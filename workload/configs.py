@@ -27,6 +27,16 @@ class Config:
     layers: int = 1
     ragged: Optional[tuple] = None   # (lo, hi): per-sequence length ~ U{lo..hi}
     seed: int = 0
+    # per-KV-head dominant-FC counts (each <= n_tip, the table's row length)
+    n_tip_per_head: Optional[tuple] = None
+    # per-layer token budgets (each <= budget, which sizes the workspace)
+    budget_per_layer: Optional[tuple] = None
+
+    def head_n_tip(self, h: int) -> int:
+        return self.n_tip if self.n_tip_per_head is None else self.n_tip_per_head[h]
+
+    def layer_budget(self, layer: int) -> int:
+        return self.budget if self.budget_per_layer is None else self.budget_per_layer[layer]
 
     @property
     def group(self) -> int:
@@ -76,6 +86,26 @@ CONFIGS = {
         name="llama3_8b_b4_ctx128k", dtype="bf16", batch=4, n_q_heads=32, n_kv_heads=8,
         head_dim=128, rope_theta=5e5, context=131072, n_tip=8, budget=2048,
         n_outlier=4, seed=_seed(5)),
+    # Variants the pages describe (per-head N_tip, the Oracle upper bound,
+    # per-layer budgets), each a first-class workload of its own:
+    # Llama-3-8B 32K with per-KV-head N_tip of 4..28 (mean 16, as uniform 16).
+    "llama3_8b_ctx32k_ragged_ntip": Config(
+        name="llama3_8b_ctx32k_ragged_ntip", dtype="bf16", batch=1, n_q_heads=32, n_kv_heads=8,
+        head_dim=128, rope_theta=5e5, context=32768, n_tip=28, budget=256,
+        n_outlier=4, seed=_seed(2), n_tip_per_head=(4, 8, 12, 16, 16, 20, 24, 28)),
+    # Llama-3-8B 32K with every FC dominant: TIP scores are the full logits
+    # (the pages' "Oracle" selection, run through the same kernels).
+    "llama3_8b_ctx32k_oraclek": Config(
+        name="llama3_8b_ctx32k_oraclek", dtype="bf16", batch=1, n_q_heads=32, n_kv_heads=8,
+        head_dim=128, rope_theta=5e5, context=32768, n_tip=64, budget=256,
+        n_outlier=4, seed=_seed(2)),
+    # The Mistral-7B 32-layer step with pyramid budgets: 384 at the first
+    # layer down to 128 at the last (mean 256, as the uniform workload).
+    "mistral_7b_l32_b32_pyramid": Config(
+        name="mistral_7b_l32_b32_pyramid", dtype="bf16", batch=32, n_q_heads=32,
+        n_kv_heads=8, head_dim=128, rope_theta=1e6, context=32768, n_tip=12,
+        budget=384, n_outlier=4, layers=32, ragged=(4096, 32768), seed=_seed(4),
+        budget_per_layer=tuple(int(round(384 - 256 * l / 31)) for l in range(32))),
 }
 
 # Order used by tests: the pages' workloads from smallest to largest.

@@ -83,7 +83,15 @@ def outlier_fcs(cfg: Config, layer: int) -> np.ndarray:
 
 
 def dominant_fcs(cfg: Config, layer: int, n_tip: int = None) -> np.ndarray:
-    """[Hkv, n_tip] int32: the head's outlier FCs plus a seeded draw of others."""
+    """[Hkv, n_tip] int32: the head's outlier FCs plus a seeded draw of others.
+    With per-head counts, head h keeps its own count of FCs (drawn the same
+    way) and the rest of its row is -1 (unused slots)."""
+    if n_tip is None and cfg.n_tip_per_head is not None:
+        out = np.full((cfg.n_kv_heads, cfg.n_tip), -1, dtype=np.int32)
+        for h in range(cfg.n_kv_heads):
+            n_h = cfg.n_tip_per_head[h]
+            out[h, :n_h] = dominant_fcs(cfg, layer, n_h)[h]
+        return out
     n_tip = cfg.n_tip if n_tip is None else n_tip
     outl = outlier_fcs(cfg, layer)
     dom = np.zeros((cfg.n_kv_heads, n_tip), dtype=np.int32)
