@@ -239,8 +239,11 @@ def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: 
         O.focused_attention_unit(q_rot, K, V, idx)
         return nb
 
-    for i in range(warmup):
+    warm_until = time.perf_counter() + min(5.0, seconds)
+    for i in range(warmup):   # untimed; bounded in time like the timed part
         one(i)
+        if time.perf_counter() >= warm_until:
+            break
     steps, nbytes = 0, 0
     t0 = time.perf_counter()
     while steps < max_steps:
@@ -274,8 +277,11 @@ def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmu
         O.contextual_agreement_unit(q_rot, K, cfg.budget)
         return nb
 
-    for i in range(warmup):
+    warm_until = time.perf_counter() + min(5.0, seconds)
+    for i in range(warmup):   # untimed; bounded in time like the timed part
         one(i)
+        if time.perf_counter() >= warm_until:
+            break
     steps, nbytes = 0, 0
     t0 = time.perf_counter()
     while steps < max_steps:

@@ -209,6 +209,34 @@ def test_compound_agreement_against_oracle():
         assert np.array_equal(got, ca[:, :, i])
 
 
+def test_compound_agreement_fp32_and_ragged_sets():
+    """fp32 keys, 64-dim heads, and dominant rows that end early (-1): the
+    compound CA reads each head's set as the entries before its first -1."""
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for, fasa_apply_rope_q
+    cfg = configs.CONFIGS["tiny_fp32_ctx1k"].with_(batch=2)
+    L = gpu_gen.make_layer(cfg, 0)
+    lens = [1024, 300]
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    dom = np.array([[3, 9, 17, -1, -1, -1], [0, 1, 2, 3, 30, 31]], dtype=np.int32)
+    dims = dims_for(cfg, n_tip=dom.shape[1])
+    q_rot = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
+    fasa_apply_rope_q(L.q, lens_d, q_rot, dims)
+    K = 64
+    cca = _gpu_cca(q_rot, L.k, torch.from_numpy(dom).cuda(), lens_d, K, dims)
+    qr = q_rot.cpu().numpy().astype(np.float64)
+    G = cfg.group
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            q_g = qr[b, h * G:(h + 1) * G]
+            K_rows = P.host_f64(L.k[b, h, :lens[b]], cfg.dtype)
+            ref = O.compound_agreement_unit(q_g, K_rows, dom[h], K)
+            A = O.fc_scores_unit(q_g, K_rows)
+            kk = min(K, lens[b])
+            band = _band(A.sum(axis=0), kk) + _band(A[O.dominant_set(dom[h])].sum(axis=0), kk)
+            assert abs(round(cca[b, h] * kk) - round(ref * kk)) <= band
+
+
 def test_select_dominant_equals_oracle_with_ties():
     import torch
     from kv_cache_token_tip_gb300 import dims_for, fasa_select_dominant_fcs
