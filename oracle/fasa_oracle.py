@@ -45,7 +45,7 @@ __all__ = [
     "tip_score", "topk_select", "focused_attention", "dense_attention",
     "decode_step", "append_token", "decode_step_append", "build_kdom", "bytes_fraction",
     "theoretical_speedup", "fc_scores_unit", "ca_from_scores", "contextual_agreement_unit",
-    "calibrate_dominant_fcs", "compound_agreement_unit", "dominant_set",
+    "calibrate_dominant_fcs", "compound_agreement_unit", "dominant_set", "fasa_m_gpu_bytes",
 ]
 
 
@@ -379,6 +379,17 @@ def bytes_fraction(n_tip: int, d: int, budget: int, t: int) -> float:
     """
     d_dom = 2 * n_tip
     return (t * d_dom + 2 * budget * d) / (2.0 * t * d)
+
+
+def fasa_m_gpu_bytes(n_layers: int, seq_len: int, d: int, n_tip: int, budget: int,
+                     bytes_per_param: int = 2) -> float:
+    """Eq. 10 ("Hardware-Aware Variants", FASA-M): GPU memory per head of the
+    memory-optimised variant,
+        N_layers x (L d_dom + b d_nondom + b d) x bytes_per_param,
+    d_dom = 2 N_tip, d_nondom = d - d_dom, b = N_fac: the dominant keys of
+    every token, plus the selected tokens' other key dimensions and values."""
+    d_dom = 2 * n_tip
+    return float(n_layers * (seq_len * d_dom + budget * (d - d_dom) + budget * d) * bytes_per_param)
 
 
 def theoretical_speedup(n_tip: int, d: int, budget: int, t: int) -> float:

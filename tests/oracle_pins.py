@@ -549,4 +549,22 @@ def check_ragged_kdom_slots(o):
     assert np.array_equal(kd[0, 1, 0, 1], K[0, 1, :, 4:6])
 
 
+def check_fasa_m_memory(o):
+    """Eq. 10 against the page's worked example (tests/golden/fasa_m_memory.json):
+    d_dom = 0.25 d and b = 0.1 L give 0.25 + 0.075 + 0.1 = 0.425 L d per head,
+    about 4.7x below the 2 L d of a full cache."""
+    with open(os.path.join(GOLDEN, "fasa_m_memory.json")) as f:
+        c0, c1 = json.load(f)["cases"]
+    L, d, n, b = c0["seq_len"], c0["d"], c0["n_tip"], c0["budget"]
+    assert 2 * n == c0["dominant_coef"] * d and b == c0["values_coef"] * L
+    per_head = o.fasa_m_gpu_bytes(1, L, d, n, b, bytes_per_param=1)
+    assert abs(per_head - c0["total_coef"] * L * d) < 1e-9 * L * d
+    parts = (c0["dominant_coef"], c0["nondominant_coef"], c0["values_coef"])
+    assert abs(sum(parts) - c0["total_coef"]) < 1e-12
+    assert abs(c1["full_coef"] / c0["total_coef"] - c1["reduction_approx"]) <= c1["abs_tol"]
+    # layers and element size scale it linearly; no budget leaves the dominant keys
+    assert o.fasa_m_gpu_bytes(32, L, d, n, b, 2) == 64 * per_head
+    assert o.fasa_m_gpu_bytes(1, L, d, n, 0, 1) == L * 2 * n
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -154,6 +154,11 @@ def _dominant_set_sentinel_as_fc0(dom_row):
     return [max(int(i), 0) for i in dom_row]
 
 
+def _fasa_m_values_by_length(n_layers, seq_len, d, n_tip, budget, bytes_per_param=2):
+    d_dom = 2 * n_tip
+    return float(n_layers * (seq_len * d_dom + budget * (d - d_dom) + seq_len * d) * bytes_per_param)
+
+
 MUTATIONS = {
     "rope_row_vector_sign": ("rope_rotate", _rope_row_convention),
     "rope_rotate_half_pairing": ("rope_rotate", _rope_rotate_half),
@@ -171,6 +176,7 @@ MUTATIONS = {
     "compound_compares_set_with_itself": ("compound_agreement_unit", _compound_vs_itself),
     "ragged_set_reads_past_the_sentinel": ("dominant_set", _dominant_set_skips_gaps),
     "ragged_sentinel_taken_as_fc0": ("dominant_set", _dominant_set_sentinel_as_fc0),
+    "fasa_m_values_scale_with_length": ("fasa_m_gpu_bytes", _fasa_m_values_by_length),
 }
 
 
