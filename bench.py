@@ -68,6 +68,16 @@ def algorithmic_bytes(cfg, lens, budget=None) -> dict:
                 total=tip + sel + q + out + small, dense_total=dense)
 
 
+def fasa_m_eq10_bytes(cfg) -> int:
+    """Eq. 10 ("Hardware-Aware Variants", FASA-M) for one layer of the
+    workload: per (batch, KV head), the dominant key columns of every cache
+    slot (L = T_max, d_dom = 2 n_tip) plus the budget's worth of the other key
+    dimensions and of values (b = the budget)."""
+    d, es, d_dom = cfg.head_dim, cfg.elem_bytes, 2 * cfg.n_tip
+    per_head = cfg.context * d_dom + cfg.budget * (d - d_dom) + cfg.budget * d
+    return int(cfg.batch * cfg.n_kv_heads * per_head * es)
+
+
 def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     for f in (KERNEL_SOURCES if sources is None else sources):
@@ -580,7 +590,15 @@ def run_gpu(args):
             **({"fasa_m": {"link_bytes_per_step": int(round(model["fac"] * layers)),
                            "link_gbs": round(model["fac"] * layers / sec_per_step / 1e9, 1),
                            "hbm_bytes_not_held_per_replica": int(2 * reps[0][0].k.numel()
-                                                                 * reps[0][0].k.element_size())}}
+                                                                 * reps[0][0].k.element_size()),
+                           # what one layer's step keeps in HBM (the library allocates
+                           # nothing), against Eq. 10's estimate for the layer
+                           "hbm_bytes_held_per_replica": int(sum(
+                               t.numel() * t.element_size() for t in (reps[0][1], reps[0][0].q, reps[0][0].pos,
+                                                                      reps[0][0].seq_lens, reps[0][0].dom_fc,
+                                                                      outs[0]))),
+                           "workspace_bytes": int(ws.numel()) if ws is not None else 0,
+                           "eq10_bytes_per_replica": fasa_m_eq10_bytes(cfg)}}
                if args.fasa_m else {}),
             "bytes_breakdown": {kk: int(round(model[kk] * layers))
                                 for kk in ("tip", "fac", "q", "out", "small", "append")

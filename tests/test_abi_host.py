@@ -137,3 +137,16 @@ def test_ragged_lengths_in_range():
     cfg = configs.CONFIGS["mistral_7b_l32_b32_ragged"]
     lens = synth.seq_lens(cfg)
     assert lens.shape == (32,) and lens.min() >= 4096 and lens.max() <= 32768
+
+
+def test_fasa_m_memory_model_is_eq10():
+    """bench.py's FASA-M footprint estimate is Eq. 10 of the oracle, summed
+    over the (batch, KV head) units of one layer."""
+    import bench
+    import oracle as O
+    from workload import configs
+    for name in ("llama3_8b_ctx32k", "qwen25_7b_b8_ctx16k", "llama3_8b_b4_ctx128k", "tiny_fp32_ctx1k"):
+        cfg = configs.CONFIGS[name]
+        ref = cfg.batch * cfg.n_kv_heads * O.fasa_m_gpu_bytes(1, cfg.context, cfg.head_dim, cfg.n_tip, cfg.budget,
+                                                               cfg.elem_bytes)
+        assert bench.fasa_m_eq10_bytes(cfg) == ref

@@ -79,3 +79,37 @@ def test_append_step_with_host_caches():
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(kd_dev, kd_host_run)
     assert torch.equal(Kd.cpu(), Kh) and torch.equal(Vd.cpu(), Vh)
+
+
+def test_fasa_m_hbm_footprint_within_eq10():
+    """With the caches in host memory, what the step keeps in HBM (K_dom, q,
+    lengths, positions, the FC table, the output, the workspace) is within
+    Eq. 10's estimate for the layer, and the library allocates no device
+    memory of its own across steps."""
+    import torch
+    import oracle as O
+    from kv_cache_token_tip_gb300 import dims_for, fasa_decode_step, fasa_device_status
+    for name, over in (("llama3_8b_ctx32k", dict()), ("llama3_8b_b4_ctx128k", dict(batch=2))):
+        cfg = configs.CONFIGS[name].with_(**over)
+        L = gpu_gen.make_layer(cfg, 0)
+        dims = dims_for(cfg)
+        kd = build_kdom(L, dims)
+        Kh, Vh = L.k.cpu().pin_memory(), L.v.cpu().pin_memory()
+        del L.k, L.v
+        torch.cuda.empty_cache()
+        ws = _ws(dims, cfg.budget)
+        out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
+        held = [kd, L.q, L.pos, L.seq_lens, L.dom_fc, out] + ([ws] if ws is not None else [])
+        held_bytes = sum(t.numel() * t.element_size() for t in held)
+        eq10 = cfg.batch * cfg.n_kv_heads * O.fasa_m_gpu_bytes(1, cfg.context, cfg.head_dim, cfg.n_tip,
+                                                               cfg.budget, cfg.elem_bytes)
+        assert held_bytes <= eq10
+        fasa_decode_step(L.q, L.pos, Kh, Vh, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, ws, dims)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        for _ in range(3):
+            fasa_decode_step(L.q, L.pos, Kh, Vh, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, ws, dims)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert fasa_device_status() == 0
+        assert np.all(np.isfinite(out.cpu().numpy()))
