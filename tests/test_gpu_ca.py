@@ -80,8 +80,8 @@ def _check_unit(ca_gpu, q_rot_g, K_rows, K, exact=False):
 
 CASES = [
     # (config, overrides, lengths, K)
-    ("llama3_8b_ctx32k", dict(context=8192, batch=3), [5000, 8192, 0], 256),
-    ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2), [4096, 700], 1000),
+    ("llama3_8b_ctx32k", dict(context=8192, batch=3), [5001, 8192, 0], 256),   # ragged tails
+    ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2), [4096, 701], 1000),
     ("llama3_8b_ctx32k", dict(context=1024, batch=2), [100, 1000], 256),   # t < K: CA = 1
     ("tiny_fp32_ctx1k", dict(batch=2), [1024, 5], 64),
 ]
@@ -175,7 +175,7 @@ def test_compound_agreement_against_oracle():
     from kv_cache_token_tip_gb300 import dims_for, fasa_apply_rope_q
     cfg = configs.CONFIGS["llama3_8b_ctx32k"].with_(context=8192, batch=3)
     L = gpu_gen.make_layer(cfg, 0)
-    lens = [8192, 3000, 0]
+    lens = [8192, 3003, 0]
     lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
     dims = dims_for(cfg)
     q_rot = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
