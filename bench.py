@@ -533,6 +533,42 @@ def run_gpu(args):
     last = ((E - 1) * layers + layers - 1) % R
     if not torch.equal(h_out[last], outs[last].cpu()):
         raise RuntimeError("end-to-end output copy does not match the device output")
+
+    # zero-copy: the step reads q/pos/lens from the same pinned host buffers
+    # and writes its output into pinned host memory in place (the library's
+    # host-resident step I/O), so each step is one graph of one launch
+    h_q = [h_in[r][:qbytes].view(reps[0][0].q.dtype).view(reps[0][0].q.shape) for r in range(R)]
+    h_pos = [h_in[r][qoff:qoff + 4 * B].view(torch.int32) for r in range(R)]
+    h_lens = [h_in[r][qoff + 4 * B:].view(torch.int32) for r in range(R)]
+    h_out_zc = [torch.empty((B, Hq, d), dtype=torch.float32).pin_memory() for _ in range(R)]
+
+    def zc_step(r):
+        L, kd = reps[r]
+        fasa_decode_step(h_q[r], h_pos[r], L.k, L.v, kd, L.dom_fc, h_lens[r], cfg.layer_budget(r % layers),
+                         h_out_zc[r], None, None, ws, dims, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            zc_step(r)
+    torch.cuda.synchronize()
+    zc_graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                zc_step(r)
+        zc_graphs.append(g)
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(E):
+            for l in range(layers):
+                zc_graphs[(i * layers + l) % R].replay()
+            stream.synchronize()
+    zc_per_step = max_over_ranks(pg, time.perf_counter() - t0) / E
+    if not torch.equal(h_out_zc[last], outs[last].cpu()):
+        raise RuntimeError("zero-copy output does not match the device output")
     status = fasa_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -609,12 +645,16 @@ def run_gpu(args):
             "dense": {"us_per_step": round(dense_sec * 1e6, 3),
                       "achieved_gbs": round(model["dense_total"] * layers / dense_sec / 1e9, 1),
                       "sparse_vs_dense_speedup": round(dense_sec / sec_per_step, 3)},
-            "e2e": {"value": round(world * per_step / e2e_per_step / 1e12, 4), "unit": "TB/s",
-                    "us_per_step": round(e2e_per_step * 1e6, 3),
+            "e2e": {"value": round(world * per_step / zc_per_step / 1e12, 4), "unit": "TB/s",
+                    "us_per_step": round(zc_per_step * 1e6, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "mode": "CUDA graph per step: pinned H2D copy of q/pos/lens, fasa_decode_step, D2H copy of "
-                            "out; host sync every step",
-                    "eager_us_per_step": round(e2e_eager_per_step * 1e6, 3)},
+                    "mode": "zero-copy: fasa_decode_step reads q/pos/lens from pinned host memory and writes out "
+                            "into pinned host memory in place (one CUDA graph of one launch per step); host sync "
+                            "every step",
+                    "copy_us_per_step": round(e2e_per_step * 1e6, 3),
+                    "copy_mode": "CUDA graph per step: pinned H2D copy of q/pos/lens, fasa_decode_step, D2H copy "
+                                 "of out; host sync every step",
+                    "copy_eager_us_per_step": round(e2e_eager_per_step * 1e6, 3)},
             "gpu_launches": K * layers,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -22,6 +22,12 @@
  *    the caches only row by row in the attention gather (and the append step
  *    writes its one row), so a step then moves just the selected K/V rows
  *    over the host link; TIP reads k_dom, which stays in device memory.
+ *  - Zero-copy step I/O: the per-step inputs and outputs of fasa_decode_step
+ *    (q, pos, seq_lens, out, idx_out, count_out) may also be page-locked
+ *    host memory addressable by the device.  The kernel reads them (a few
+ *    KB) and writes them in place over the host link, so a host-driven
+ *    decode loop needs no separate copies around the step; the caller
+ *    synchronises the stream before reading the results.
  *  - Return value: FASA_OK, or an error code.  Arguments are validated on
  *    the host before any launch; on an error nothing is launched and nothing
  *    is written.  Values that live in device memory (sequence lengths,

@@ -105,8 +105,8 @@ def lib():
 # ---------------------------------------------------------------- marshalling
 def _ptr(x, dtype=None, name="tensor", host_ok=False):
     """Device pointer of a contiguous tensor.  With host_ok, a tensor in pinned
-    host memory is accepted too (the GPU reads it in place over the
-    host link: the FASA-M placement of the K/V caches)."""
+    host memory is accepted too (the GPU reads or writes it in place over the
+    host link: the FASA-M placement of the K/V caches, zero-copy step I/O)."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -224,11 +224,11 @@ def fasa_decode_step(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget: 
     if workspace is not None and not isinstance(workspace, int):
         ws_bytes = workspace.numel() * workspace.element_size()
     _check("fasa_decode_step", lib().fasa_decode_step(
-        _ptr(q, _store_dtypes(), "q"), _ptr(pos, _i32(), "pos"),
+        _ptr(q, _store_dtypes(), "q", True), _ptr(pos, _i32(), "pos", True),
         _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
-        _ptr(seq_lens, _i32(), "seq_lens"), int(budget), _ptr(out, _f32(), "out"),
-        _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
+        _ptr(seq_lens, _i32(), "seq_lens", True), int(budget), _ptr(out, _f32(), "out", True),
+        _ptr(idx_out, _i32(), "idx_out", True), _ptr(count_out, _i32(), "count_out", True),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
 
 

@@ -113,3 +113,32 @@ def test_fasa_m_hbm_footprint_within_eq10():
         assert torch.cuda.mem_get_info()[0] == free0
         assert fasa_device_status() == 0
         assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+def test_step_io_in_host_memory():
+    """Zero-copy step I/O: q, pos, lengths, output, indices and counts in
+    pinned host memory give the device run's results bit for bit."""
+    import torch
+    from kv_cache_token_tip_gb300 import dims_for, fasa_decode_step, fasa_device_status
+    cfg = configs.CONFIGS["llama3_8b_ctx32k"].with_(context=8192, batch=2)
+    L = gpu_gen.make_layer(cfg, 0)
+    L.seq_lens = torch.tensor([8192, 3001], dtype=torch.int32, device="cuda")
+    L.pos = L.seq_lens.clone()
+    dims = dims_for(cfg)
+    kd = build_kdom(L, dims)
+    ws = _ws(dims, cfg.budget)
+    shape_o = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    shape_i = (cfg.batch, cfg.n_kv_heads, cfg.budget)
+    res = []
+    for host in (False, True):
+        mk = (lambda t: t.cpu().pin_memory()) if host else (lambda t: t)
+        q, pos, lens = mk(L.q), mk(L.pos), mk(L.seq_lens)
+        out = mk(torch.full(shape_o, float("nan"), dtype=torch.float32, device="cuda"))
+        idx = mk(torch.full(shape_i, -7, dtype=torch.int32, device="cuda"))
+        cnt = mk(torch.full(shape_i[:2], -7, dtype=torch.int32, device="cuda"))
+        fasa_decode_step(q, pos, L.k, L.v, kd, L.dom_fc, lens, cfg.budget, out, idx, cnt, ws, dims)
+        torch.cuda.synchronize()
+        assert fasa_device_status() == 0
+        res.append((out.cpu(), idx.cpu(), cnt.cpu()))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
