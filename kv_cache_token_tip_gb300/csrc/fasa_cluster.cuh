@@ -1164,17 +1164,29 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const int ntile = (fr_n + RT - 1) / RT;
     // Merges nrec partial records (o[0..D), m, l) per head, stored at
     // mst[(g * nrec + r) * (D + 2)], into this CTA's record part[g].
+    // (the FAC scratch stile is idle here: wts holds each head's maximum and
+    // record weights, computed once instead of once per element)
     auto merge_records = [&](const float* mst, int nrec) {
-      for (int x = tid; x < G * (D + 2); x += NT) {
-        const int g = x / (D + 2), e = x - g * (D + 2);
+      float* wts = stile;  // [G][nrec] weights exp2(m_r - M), then [G] maxima
+      if (tid < G) {
+        const int g = tid;
         float M = -CUDART_INF_F;
         for (int r = 0; r < nrec; ++r) M = fmaxf(M, mst[(g * nrec + r) * (D + 2) + D]);
-        float val = M;
+        for (int r = 0; r < nrec; ++r) {
+          const float m_r = mst[(g * nrec + r) * (D + 2) + D];
+          wts[g * nrec + r] = m_r != -CUDART_INF_F ? exp2f(m_r - M) : 0.f;
+        }
+        wts[G * nrec + g] = M;
+      }
+      __syncthreads();
+      for (int x = tid; x < G * (D + 2); x += NT) {
+        const int g = x / (D + 2), e = x - g * (D + 2);
+        float val = wts[G * nrec + g];
         if (e != D) {
           float acc = 0.f;
           for (int r = 0; r < nrec; ++r) {
-            const float* sp = mst + (g * nrec + r) * (D + 2);
-            if (sp[D] != -CUDART_INF_F) acc += exp2f(sp[D] - M) * sp[e];
+            const float w = wts[g * nrec + r];
+            if (w != 0.f) acc += w * mst[(g * nrec + r) * (D + 2) + e];
           }
           val = acc;
         }
@@ -1429,34 +1441,44 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     if ((flags & F_IDX_OUT) && need_select) push_count();
     cluster_sync();
 
+    // Finish this CTA's slice: lpg lanes per output group (the power of two
+    // >= C), lane r taking CTA r's record, reduced with width-lpg shuffles; a
+    // warp takes 32 / lpg groups per pass, so every shuffle runs with all 32
+    // lanes.
     const int q0 = (ngrp * (int)crank) / C, q1 = (ngrp * ((int)crank + 1)) / C;
-    for (int q = q0 + tid; q < q1; q += NT) {
-      const int g = q / (D / 4), e4 = q - g * (D / 4);
-      float M = -CUDART_INF_F;
-      for (int r = 0; r < C; ++r) M = fmaxf(M, recv_ml[r * G + g].x);
-      float L = 0.f;
+    const int lpg = C <= 1 ? 1 : 1 << (32 - __clz(C - 1));
+    const int gpw = 32 / lpg;  // groups per warp and pass
+    for (int qw = q0 + gpw * warp; qw < q1; qw += gpw * NW) {  // warp-uniform bound
+      const int q = qw + lane / lpg, r = lane & (lpg - 1);
+      const bool ok = q < q1 && r < C;
+      const int g = ok ? q / (D / 4) : 0, e4 = ok ? q - g * (D / 4) : 0;
+      const float2 ml = ok ? recv_ml[r * G + g] : make_float2(-CUDART_INF_F, 0.f);
+      float M = ml.x;
+      for (int o = lpg >> 1; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, lpg));
+      const float w = (ml.x != -CUDART_INF_F) ? exp2f(ml.x - M) : 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (M != -CUDART_INF_F) {
-        for (int r = 0; r < C; ++r) {
-          const float2 ml = recv_ml[r * G + g];
-          if (ml.x == -CUDART_INF_F) continue;
-          const float w = exp2f(ml.x - M);
-          L += w * ml.y;
-          const float4 v = recv_o[r * sl + q - q0];
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
+      if (w != 0.f) {
+        const float4 v = recv_o[r * sl + q - q0];
+        acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+      }
+      float L = w * ml.y;
+      for (int o = lpg >> 1; o >= 1; o >>= 1) {
+        L += __shfl_xor_sync(0xffffffffu, L, o, lpg);
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o, lpg);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o, lpg);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o, lpg);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o, lpg);
+      }
+      if (r == 0 && q < q1) {
+        if (L > 0.f) {
+          const float inv = 1.f / L;
+          acc.x *= inv;
+          acc.y *= inv;
+          acc.z *= inv;
+          acc.w *= inv;
         }
+        *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G + g) * D + e4 * 4) = acc;
       }
-      if (L > 0.f) {
-        const float inv = 1.f / L;
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
-      }
-      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G + g) * D + e4 * 4) = acc;
     }
     if (flags & F_IDX_OUT) write_idx_out();
   } else if (need_select) {
