@@ -26,11 +26,12 @@ def header_symbols():
     return sorted(set(re.findall(r"\b(fasa_[a-z_]+)\s*\(", src)))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_decode_path_calls():
     syms = header_symbols()
     for name in ("fasa_apply_rope_q", "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention",
                  "fasa_decode_step", "fasa_dense_attention", "fasa_build_kdom", "fasa_append_kdom",
-                 "fasa_workspace_size", "fasa_device_status"):
+                 "fasa_workspace_size", "fasa_device_status", "fasa_decode_step_append",
+                 "fasa_fc_agreement", "fasa_compound_agreement", "fasa_select_dominant_fcs"):
         assert name in syms
 
 
@@ -150,3 +151,34 @@ def test_fasa_m_memory_model_is_eq10():
         ref = cfg.batch * cfg.n_kv_heads * O.fasa_m_gpu_bytes(1, cfg.context, cfg.head_dim, cfg.n_tip, cfg.budget,
                                                                cfg.elem_bytes)
         assert bench.fasa_m_eq10_bytes(cfg) == ref
+
+
+def test_variant_workloads():
+    """The per-head, all-FC and pyramid-budget workloads: each head's row holds
+    its own count of distinct FCs (its outlier FCs first in the draw) padded
+    with -1; every FC is dominant in the all-FC workload; the pyramid budgets
+    fall from 384 to 128 with mean 256 and the byte model follows them."""
+    import bench
+    import oracle as O
+    from workload import configs, synth
+    cfg = configs.CONFIGS["llama3_8b_ctx32k_ragged_ntip"]
+    dom = synth.dominant_fcs(cfg, 0)
+    outl = synth.outlier_fcs(cfg, 0)
+    assert dom.shape == (cfg.n_kv_heads, cfg.n_tip) and cfg.n_tip == max(cfg.n_tip_per_head)
+    for h in range(cfg.n_kv_heads):
+        s = O.dominant_set(dom[h])
+        assert len(s) == cfg.n_tip_per_head[h] == len(set(s))
+        assert all(0 <= i < cfg.n_fc for i in s) and np.all(dom[h, len(s):] == -1)
+        assert set(outl[h][:min(cfg.n_outlier, len(s))].tolist()) <= set(s)
+    assert sum(cfg.n_tip_per_head) == 16 * cfg.n_kv_heads
+    ok = configs.CONFIGS["llama3_8b_ctx32k_oraclek"]
+    assert np.array_equal(synth.dominant_fcs(ok, 0), np.tile(np.arange(ok.n_fc), (ok.n_kv_heads, 1)))
+    py = configs.CONFIGS["mistral_7b_l32_b32_pyramid"]
+    b = py.budget_per_layer
+    assert len(b) == py.layers and b[0] == 384 and b[-1] == 128 and sum(b) == 256 * py.layers
+    assert all(x >= y for x, y in zip(b, b[1:])) and max(b) == py.budget
+    lens = synth.seq_lens(py)
+    uni = configs.CONFIGS["mistral_7b_l32_b32_ragged"]
+    tot_py = sum(bench.algorithmic_bytes(py, lens, py.layer_budget(l))["fac"] for l in range(py.layers))
+    tot_uni = bench.algorithmic_bytes(uni, lens)["fac"] * uni.layers
+    assert abs(tot_py - tot_uni) < 0.01 * tot_uni   # same mean budget, lengths mostly above 384
