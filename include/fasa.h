@@ -9,8 +9,9 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every tensor pointer is a DEVICE pointer owned by the caller.  Nothing
- *    is allocated or freed by the library.  Calls are asynchronous on
+ *  - Every tensor pointer is owned by the caller and is a DEVICE pointer
+ *    unless one of the two placements below says otherwise.  Nothing is
+ *    allocated or freed by the library.  Calls are asynchronous on
  *    `stream` (NULL = the legacy default stream).
  *  - FASA-M placement (the FASA pages, "Hardware-Aware Variants": keep the
  *    dominant key cache on the GPU, offload the rest of the KV cache to host
