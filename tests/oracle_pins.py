@@ -162,6 +162,55 @@ def check_topk_bruteforce(o):
         assert tuple(int(x) for x in got) == best[1], (s, k, got, best)
 
 
+def check_topk_batched_layout(o):
+    """The batched TopK-I: each (batch, KV head) row holds the brute-force
+    best set of min(k, len) tokens (ties to the smaller index) in ascending
+    order, then -1; count = min(k, len); an empty sequence selects nothing."""
+    rng = _rng(83)
+    B, H, T, k = 3, 2, 9, 4
+    scores = rng.integers(-2, 3, size=(B, H, T)).astype(np.float64)
+    lens = np.array([9, 3, 0])
+    idx, cnt = o.topk_select(scores, lens, k)
+    assert idx.shape == (B, H, k) and cnt.shape == (B, H)
+    for b in range(B):
+        for h in range(H):
+            L = int(lens[b])
+            kk = min(k, L)
+            assert cnt[b, h] == kk
+            best = min(itertools.combinations(range(L), kk), key=lambda sub: (-scores[b, h, list(sub)].sum(), sub))
+            assert tuple(int(x) for x in idx[b, h, :kk]) == best
+            assert np.all(idx[b, h, kk:] == -1)
+
+
+def check_fac_subset_vs_sdpa(o):
+    """FAC over index subsets equals torch's scaled_dot_product_attention over
+    the gathered rows, with query head hq reading KV head hq // G."""
+    import torch
+    rng = _rng(89)
+    B, Hq, Hkv, T, d, k = 2, 6, 3, 25, 32, 7
+    q = rng.standard_normal((B, Hq, d))
+    K = rng.standard_normal((B, Hkv, T, d))
+    V = rng.standard_normal((B, Hkv, T, d))
+    idx = np.full((B, Hkv, k), -1, dtype=np.int64)
+    cnt = np.zeros((B, Hkv), dtype=np.int64)
+    for b in range(B):
+        for h in range(Hkv):
+            c = int(rng.integers(1, k + 1))
+            idx[b, h, :c] = np.sort(rng.choice(T, c, replace=False))
+            cnt[b, h] = c
+    out = o.focused_attention(q, K, V, idx, cnt)
+    G = Hq // Hkv
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // G
+            sel = idx[b, h, :cnt[b, h]]
+            qt = torch.from_numpy(q[b, hq][None, None, :])
+            kt = torch.from_numpy(K[b, h, sel][None])
+            vt = torch.from_numpy(V[b, h, sel][None])
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, 0].numpy()
+            assert np.allclose(out[b, hq], ref, rtol=1e-12, atol=1e-12)
+
+
 def check_topk_signed_zero_and_order(o):
     """-0 and +0 are equal scores; output is ascending; k >= len keeps all."""
     s = np.array([0.0, -0.0, 1.0, -0.0, 0.0])
