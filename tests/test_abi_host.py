@@ -89,6 +89,40 @@ def test_null_and_misaligned_pointers_rejected(L):
     assert L.fasa_device_status(None, None) == 1
 
 
+def test_calibration_arguments_rejected_before_launch(L):
+    """The calibration entry points validate on the host: dims, null and
+    misaligned pointers, K < 1, n_tip outside 1..d/2, a missing or short
+    workspace -- all before any CUDA call."""
+    d = _dims()
+    P = 0x10000
+    need = ctypes.c_size_t(0)
+    assert L.fasa_fc_agreement_workspace_size(ctypes.byref(d), ctypes.byref(need)) == 0
+    units, F, T = d.batch * d.n_kv_heads, d.head_dim // 2, d.t_max
+    assert need.value == units * (F + 1) * (T + T // 32) * 4
+    ws, n = P, need.value
+    assert L.fasa_fc_agreement_workspace_size(ctypes.byref(d), None) == 1
+    bad = _dims(n_tip=0)
+    assert L.fasa_fc_agreement_workspace_size(ctypes.byref(bad), ctypes.byref(need)) == 1
+    assert need.value == 0
+    fa = L.fasa_fc_agreement
+    assert fa(P, P, P, 256, P, ws, n, ctypes.byref(bad), None) == 1
+    assert fa(None, P, P, 256, P, ws, n, ctypes.byref(d), None) == 1
+    assert fa(P, P + 8, P, 256, P, ws, n, ctypes.byref(d), None) == 1    # k_cache not 16-byte aligned
+    assert fa(P, P, P, 0, P, ws, n, ctypes.byref(d), None) == 1
+    assert fa(P, P, P, 256, P, None, n, ctypes.byref(d), None) == 3
+    assert fa(P, P, P, 256, P, ws, n - 1, ctypes.byref(d), None) == 3
+    assert fa(P, P, P, 256, P, ws + 4, n, ctypes.byref(d), None) == 3  # workspace not 16-byte aligned
+    ca = L.fasa_compound_agreement
+    assert ca(P, P, None, P, 256, P, ws, n, ctypes.byref(d), None) == 1
+    assert ca(P, P, P, P, 0, P, ws, n, ctypes.byref(d), None) == 1
+    assert ca(P, P, P, P, 256, P, ws, n - 16, ctypes.byref(d), None) == 3
+    sd = L.fasa_select_dominant_fcs
+    assert sd(P, 0, P, ctypes.byref(d), None) == 1
+    assert sd(P, F + 1, P, ctypes.byref(d), None) == 1
+    assert sd(None, 4, P, ctypes.byref(d), None) == 1
+    assert sd(P, 4, None, ctypes.byref(d), None) == 1
+
+
 def test_status_strings(L):
     for code, name in ((0, b"FASA_OK"), (1, b"FASA_ERR_INVALID_ARG"), (2, b"FASA_ERR_UNSUPPORTED"),
                        (3, b"FASA_ERR_WORKSPACE"), (4, b"FASA_ERR_CUDA"), (99, b"FASA_ERR_UNKNOWN")):
