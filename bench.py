@@ -36,7 +36,8 @@ METRIC = "FASA decode-step µs and achieved HBM TB/s (TIP+top-k+FAC) at 32K ctx"
 DEFAULT_WORKLOAD = "llama3_8b_ctx32k"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_cluster.cuh",
+KERNEL_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_step.cuh",
+                  "kv_cache_token_tip_gb300/csrc/fasa_cluster.cuh",
                   "kv_cache_token_tip_gb300/csrc/fasa_ptx.cuh",
                   "kv_cache_token_tip_gb300/csrc/fasa_internal.h",
                   "kv_cache_token_tip_gb300/csrc/fasa_api.cu"]

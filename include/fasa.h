@@ -91,7 +91,10 @@ enum {
 /* Device status word bits (fasa_device_status). */
 enum {
   FASA_DEV_BAD_INPUT = 1,    /* a device-resident value was out of range and clamped */
-  FASA_DEV_TIMEOUT = 2       /* a bounded wait for an asynchronous copy expired      */
+  FASA_DEV_TIMEOUT = 2,      /* a bounded device wait expired (a copy or a peer CTA) */
+  FASA_DEV_UNDRAINED = 4     /* after a timeout a copy had still not landed: the     */
+                             /* kernel left its staging memory alone and skipped the */
+                             /* attention of the affected rows (outputs unreliable)  */
 };
 
 enum { FASA_F32 = 0, FASA_BF16 = 1 };
@@ -316,9 +319,26 @@ int fasa_decode_step_noalloc(const void* q, const int32_t* pos,
 
 /*
  * Synchronises `stream`, stores the device status word of the current device
- * in *status (FASA_DEV_* bits, 0 = clean) and clears it.
+ * in *status (FASA_DEV_* bits, 0 = clean) and clears it.  There is one word
+ * per device, shared by every call on every stream of that device: a bit may
+ * come from any call since the last read, and a read clears it for all of
+ * them.  Callers that run steps on several streams at once read it only
+ * after synchronising all of them.
  */
 int fasa_device_status(fasa_stream_t stream, int32_t* status);
+
+/*
+ * Fault injection for tests (the pages have no counterpart).  Sets, for the
+ * calls launched after it in this process, the bound of every device wait
+ * (wait_limit_ns > 0; the default is 1 s) and, when drop_tip_tile >= 0,
+ * makes the fused step's TIP stage of that tile index arm its barrier but
+ * never issue the copy, so the waits on it run out: the launch then returns
+ * with FASA_DEV_TIMEOUT (and FASA_DEV_UNDRAINED) in the status word, no copy
+ * left in flight, and the stream usable.  fasa_test_fault_injection(1000000000, -1)
+ * restores the defaults.  FASA_ERR_INVALID_ARG for a zero limit or a tile
+ * below -1.
+ */
+int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile);
 
 /* Cluster size (CTAs per (b, KV head)) the fused kernels use on this device. */
 int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas);

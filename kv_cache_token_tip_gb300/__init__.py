@@ -12,7 +12,7 @@ from .fasa import (  # noqa: F401
     fasa_build_kdom, fasa_cluster_size, fasa_decode_step, fasa_decode_step_append, fasa_decode_step_noalloc,
     fasa_dense_attention,
     fasa_device_status, fasa_fc_agreement, fasa_fc_agreement_workspace_size,
-    fasa_select_dominant_fcs, fasa_compound_agreement,
+    fasa_select_dominant_fcs, fasa_compound_agreement, fasa_test_fault_injection,
     fasa_focused_attention, fasa_max_budget, fasa_tip_score, fasa_topk_select, fasa_workspace_size,
     lib, library_path,
 )

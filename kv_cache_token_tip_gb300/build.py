@@ -23,9 +23,10 @@ LIBFASA = os.path.join(PKG, "libfasa.so")
 LIBSYNTH = os.path.join(ROOT, "workload", "libfasa_synth.so")
 
 FASA_SOURCES = [os.path.join(PKG, "csrc", f) for f in
-                ("fasa_api.cu", "fasa_cluster_bf16.cu", "fasa_cluster_f32.cu", "fasa_noalloc.cu", "fasa_ca.cu")]
+                ("fasa_api.cu", "fasa_cluster_bf16.cu", "fasa_cluster_f32.cu", "fasa_step_bf16.cu", "fasa_noalloc.cu",
+                 "fasa_ca.cu")]
 FASA_DEPS = [os.path.join(PKG, "csrc", f) for f in
-             ("fasa_cluster.cuh", "fasa_ptx.cuh", "fasa_internal.h")] + [
+             ("fasa_cluster.cuh", "fasa_step.cuh", "fasa_ptx.cuh", "fasa_internal.h")] + [
     os.path.join(ROOT, "include", "fasa.h")]
 SYNTH_SOURCES = [os.path.join(ROOT, "workload", "csrc", "synth_gen.cu")]
 

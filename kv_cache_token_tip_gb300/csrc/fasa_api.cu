@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -21,6 +22,16 @@ namespace {
 __device__ int g_status;  // FASA_DEV_* bits, per device
 
 thread_local int t_last_cuda_error = 0;
+
+// Bound of every device wait (fasa_test_fault_injection can shorten it) and
+// the test hook that leaves one TIP tile's copy unissued (-1: none).
+unsigned long long g_wait_ns = 1000000000ull;
+int g_drop_tip_tile = -1;
+
+#ifdef FASA_PHASE_TRACE
+// Phase timestamps of the step kernel (tracing builds only): 16 per CTA.
+unsigned long long* g_trace = nullptr;
+#endif
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
@@ -250,6 +261,7 @@ void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
   p.budget = budget;
   fill_rope_turns(p, d);
   p.status = status;
+  p.wait_ns = g_wait_ns;
 }
 
 // Plans and launches the cluster kernel.  Cluster size: the explicit
@@ -300,6 +312,200 @@ int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t
   }
   const cudaError_t e = d->dtype == FASA_F32 ? launch_cluster_f32(p, d->head_dim, C, stream)
                                              : launch_cluster_bf16(p, d->head_dim, C, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FASA_OK;
+}
+
+// ------------------------------------------------------- bf16 fused step
+// Shared-memory plan of the step kernel (fasa_step.cuh) for cluster size C.
+//
+// Persistent regions: mbarriers, scratch, rotated queries, q-bar, the digit
+// histograms, the CTA's scores (when its range fits), the first-round
+// receive slots (C x cap1 packed entries), the own selection, and the
+// combine's receive slices.  The "big" region is the TIP staging (every
+// tile of the range at once when it fits, else a ring), then the FAC
+// staging, the second-round receive slots and the warp records.
+//
+// Returns FASA_OK, or FASA_ERR_UNSUPPORTED when it does not fit in `limit`.
+int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit) {
+  const int D = d->head_dim, G = d->n_q_heads / d->n_kv_heads, nfc = d->n_tip, k = p.budget;
+  constexpr int ES = 2;
+  const int chunkT = align_up(ceil_div(d->t_max, C), KDOM_BLOCK);
+  // first-round list: k/C plus four standard deviations of a random share
+  // (a single CTA lists its exact top k); receive slack for the rest of the
+  // threshold's digit-0 bucket
+  const double e = (double)k / C;
+  int rho = C == 1 ? k : (int)ceil(e + 4.0 * sqrt(e) + 4.0);
+  rho = std::max(1, std::min(rho, chunkT));
+  const int cap1 = align_up(rho + std::max(32, rho / 4), 16);
+  const int cap2 = C == 1 ? 0 : align_up(k + std::max(32, k / 8), 16);
+  const int s_cap = chunkT <= S_CAP_MAX ? chunkT : 0;
+  const int rows_cap = std::min(k, std::max(cap1, cap2));
+  const int ngrp4 = G * (D / 4);
+  const int sl = ceil_div(ngrp4, C);
+  int off = 0;
+  p.off_bar = off;
+  off += ST_BARS * 8;
+  p.off_misc = off;
+  off += ST_MISC_BYTES;
+  p.off_qrot = off;
+  off += G * D * 4;
+  p.off_qbar = off;
+  off += align_up(2 * nfc * 4, 16);
+  p.off_hist = off;
+  off += HLOC_BINS * 4;
+  p.off_uh = off;
+  off += UH_BINS * 4;
+  p.off_sc = off;
+  off += s_cap * 4;
+  p.off_recv1 = off;
+  off += C * cap1 * 8;
+  p.off_rows = off;
+  off += align_up(rows_cap * 4, 16);
+  p.off_comb = off;
+  off += align_up(C * sl * 16 + C * G * 8, 16);
+  off = align_up(off, 128);
+  p.off_big = off;
+  const int room = limit - off;
+  if (room <= 0) return FASA_ERR_UNSUPPORTED;
+  // after TIP: FAC slots (then the P tiles), the second-round slots (written
+  // only once every CTA drained its gathers), the warp records
+  auto fac_slots = [&](int wst) { return wst * NW * 2 * GR * D * ES; };
+  const int pt_bytes = NW * G_MAX * PTS * 4;
+  const int rec_bytes = (G_MAX * NW * (D + 2) + G_MAX * (D + 4) + G_MAX * NW + G_MAX) * 4;
+  const int recv2_bytes = C * cap2 * 8;
+  // TIP staging: the whole range at once (no refill) with the smallest tile
+  // that needs at most ST_MAX_STAGES stages, else a ring of at least two
+  // stages holding up to 128 KB.  Warp w scores the 128-token units w,
+  // w + NW, ...; in a ring, stages x (units per tile) must be a multiple of
+  // NW so that every warp meets the same stages in every round of ns tiles
+  // and so waits on each of their phases in order (a parity wait on a
+  // barrier two phases behind would pass at once).
+  const int fc_tok = nfc * 2 * ES;  // bytes per token over all planes
+  int tile = 0, stages = 0;
+  for (int t = TIP_UNIT; t <= 4096 && !tile; t *= 2) {
+    const int st = ceil_div(chunkT, t);
+    if (st <= ST_MAX_STAGES && st * t * fc_tok <= room) {
+      tile = t;
+      stages = st;
+    }
+  }
+  for (int t = 1024; t >= TIP_UNIT && !tile; t /= 2) {
+    const int step = std::max(1, NW / (t / TIP_UNIT));  // stage counts that keep the rounds aligned
+    int best = 0;
+    for (int st = std::max(2, step); st <= ST_MAX_STAGES; st += step) {
+      if (st % step != 0) continue;
+      if (st * t * fc_tok > std::min(room, std::max(131072, 2 * t * fc_tok))) break;
+      best = st;
+    }
+    if (best) {
+      tile = t;
+      stages = best;
+    }
+  }
+  if (!tile) return FASA_ERR_UNSUPPORTED;
+  const int tip_bytes = stages * tile * fc_tok;
+  // FAC staging: two groups in flight per warp when they fit; the first
+  // round's list is gathered during the exchange when it fits the first issue
+  int wst = 0;
+  for (int w = 2; w >= 1 && !wst; --w)
+    if (fac_slots(w) + pt_bytes <= room) wst = w;
+  if (!wst) return FASA_ERR_UNSUPPORTED;
+  const int spec = (C > 1 && cap1 <= wst * NW * GR) ? 1 : 0;
+  const int reload = (s_cap == 0 && !spec && chunkT * 4 <= room) ? 1 : 0;
+  int big = std::max(tip_bytes, fac_slots(wst) + pt_bytes);
+  big = std::max(big, std::max(rec_bytes, recv2_bytes));
+  if (reload) big = std::max(big, chunkT * 4);
+  if (big > room) return FASA_ERR_UNSUPPORTED;
+  p.s_cap = s_cap;
+  p.tip_tile = tile;
+  p.tip_stages = stages;
+  p.rho = rho;
+  p.cap1 = cap1;
+  p.cap2 = cap2;
+  p.spec = spec;
+  p.fac_wst = wst;
+  p.rows_cap = rows_cap;
+  p.reload = reload;
+  p.off_recv2 = p.off_big;
+  p.off_pt = p.off_big + fac_slots(wst);
+  p.smem_total = p.off_big + big;
+  *ws = s_cap == 0 ? (size_t)d->batch * d->n_kv_heads * d->t_max * 4 : 0;
+  return FASA_OK;
+}
+
+void fill_step(StepParams& p, const fasa_dims_t* d, int32_t budget) {
+  memset(&p, 0, sizeof(p));
+  p.B = d->batch;
+  p.Hq = d->n_q_heads;
+  p.Hkv = d->n_kv_heads;
+  p.G = d->n_q_heads / d->n_kv_heads;
+  p.T_max = d->t_max;
+  p.n_tip = d->n_tip;
+  p.budget = budget;
+  Params tmp;
+  fill_rope_turns(tmp, d);
+  memcpy(p.rope_turns, tmp.rope_turns, sizeof(p.rope_turns));
+  p.wait_ns = g_wait_ns;
+  p.drop_stage = g_drop_tip_tile;
+#ifdef FASA_PHASE_TRACE
+  p.trace = g_trace;
+#endif
+}
+
+// The bf16 step kernel serves fasa_decode_step when these dims plan.
+bool step_kernel_applies(const fasa_dims_t* d) { return d->dtype == FASA_BF16; }
+
+// Plans (and launches) the step kernel.  Cluster size: the override, else
+// the largest C <= 16 for which every unit's cluster is resident at once,
+// else (several waves) the smallest C that launches.  FASA_ERR_UNSUPPORTED:
+// no plan; the caller then uses the general cluster kernel.
+int step_plan_and_launch(StepParams& p, const fasa_dims_t* d, void* ws, size_t ws_bytes, bool launch,
+                         size_t* ws_need, int* C_out, cudaStream_t stream) {
+  DevInfo di;
+  int st = device_info(&di);
+  if (st) return st;
+  p.status = di.status;
+  const int units = d->batch * d->n_kv_heads;
+  int C = 0;
+  size_t need = 0;
+  auto capacity = [&](int c) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, d->head_dim, c, p.smem_total);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int n = max_active_clusters_step_bf16(d->head_dim, c, p.smem_total);
+    cache.emplace(key, n);
+    return n;
+  };
+  if (d->reserved > 0) {
+    if (plan_step(p, d, d->reserved, &need, di.smem_optin) != FASA_OK) return FASA_ERR_UNSUPPORTED;
+    if (capacity(d->reserved) < 1) return FASA_ERR_UNSUPPORTED;
+    C = d->reserved;
+  } else {
+    for (int c = C_MAX; c >= 1 && !C; --c) {
+      if (plan_step(p, d, c, &need, di.smem_optin) != FASA_OK) continue;
+      if (capacity(c) >= units) C = c;
+    }
+    for (int c = 1; c <= 4 && !C; ++c) {
+      if (plan_step(p, d, c, &need, di.smem_optin) != FASA_OK) continue;
+      if (capacity(c) >= 1) C = c;
+    }
+    if (!C) return FASA_ERR_UNSUPPORTED;
+    if (plan_step(p, d, C, &need, di.smem_optin) != FASA_OK) return FASA_ERR_UNSUPPORTED;
+  }
+  if (ws_need) *ws_need = need;
+  if (C_out) *C_out = C;
+  if (!launch) return FASA_OK;
+  if (need > 0) {
+    if (!ws || ws_bytes < need || !aligned16(ws)) return FASA_ERR_WORKSPACE;
+    p.scores = reinterpret_cast<float*>(ws);
+  }
+  const cudaError_t e = launch_step_bf16(p, d->head_dim, C, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FASA_OK;
 }
@@ -449,6 +655,12 @@ int fasa_workspace_size(const fasa_dims_t* dims, int32_t budget, size_t* bytes) 
   int st = check_dims(dims);
   if (st) return st;
   if (!bytes || budget < 1) return FASA_ERR_INVALID_ARG;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, budget);
+    st = step_plan_and_launch(sp, dims, nullptr, 0, false, bytes, nullptr, nullptr);
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
   Params p;
   fill_common(p, dims, budget, nullptr);
   return plan_and_launch(p, dims, F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT, nullptr, 0, false, bytes, nullptr,
@@ -459,9 +671,19 @@ int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas) {
   int st = check_dims(dims);
   if (st) return st;
   if (!ctas) return FASA_ERR_INVALID_ARG;
+  int C = 0;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, 1);
+    st = step_plan_and_launch(sp, dims, nullptr, 0, false, nullptr, &C, nullptr);
+    if (st == FASA_OK) {
+      *ctas = C;
+      return FASA_OK;
+    }
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
   Params p;
   fill_common(p, dims, 1, nullptr);
-  int C = 0;
   st = plan_and_launch(p, dims, F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT, nullptr, 0, false, nullptr, &C,
                        nullptr);
   if (st) return st;
@@ -620,6 +842,23 @@ int fasa_decode_step(const void* q, const int32_t* pos, const void* k_cache, con
   if (!q || !pos || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
     return FASA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, budget);
+    sp.q = q;
+    sp.pos = pos;
+    sp.k_cache = k_cache;
+    sp.v_cache = v_cache;
+    sp.k_dom = k_dom;
+    sp.dom_fc = dom_fc;
+    sp.seq_lens = seq_lens;
+    sp.out = out;
+    sp.idx_out = idx_out;
+    sp.count_out = count_out;
+    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
   Params p;
   fill_common(p, dims, budget, nullptr);
   p.q = q;
@@ -647,6 +886,26 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
     return FASA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, budget);
+    sp.flags = F_APPEND;
+    sp.q = q;
+    sp.pos = seq_lens;
+    sp.k_new = k_new;
+    sp.v_new = v_new;
+    sp.k_cache = k_cache;
+    sp.v_cache = v_cache;
+    sp.k_dom = k_dom;
+    sp.dom_fc = dom_fc;
+    sp.seq_lens = seq_lens;
+    sp.out = out;
+    sp.idx_out = idx_out;
+    sp.count_out = count_out;
+    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
   Params p;
   fill_common(p, dims, budget, nullptr);
   p.q = q;
@@ -721,6 +980,17 @@ int fasa_select_dominant_fcs(const float* ca_mean, int32_t n_tip, int32_t* dom_f
   const cudaError_t e = launch_select_dominant(ca_mean, dims->n_kv_heads, dims->head_dim / 2, n_tip, dom_fc,
                                                reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
+#ifdef FASA_PHASE_TRACE
+void fasa_debug_set_trace(void* buf) { g_trace = reinterpret_cast<unsigned long long*>(buf); }
+#endif
+
+int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile) {
+  if (wait_limit_ns == 0 || drop_tip_tile < -1) return FASA_ERR_INVALID_ARG;
+  g_wait_ns = wait_limit_ns;
+  g_drop_tip_tile = drop_tip_tile;
+  return FASA_OK;
 }
 
 int fasa_device_status(fasa_stream_t stream, int32_t* status) {

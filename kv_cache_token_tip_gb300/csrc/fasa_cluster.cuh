@@ -39,7 +39,6 @@
 
 namespace fasa {
 
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s for one bulk-copy wait
 
 enum : int { MODE_NONE = 0, MODE_FILL = 1, MODE_TIES = 2, MODE_CAND = 3, MODE_BX = 4 };
 // Largest threshold bucket resolved by exchanging its entries (see the
@@ -565,7 +564,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const uint32_t parity = (uint32_t)(it / ns) & 1u;
     int stop = lane == 0 ? *reinterpret_cast<volatile int*>(&ms->tip_fail) : 0;
     if (__shfl_sync(0xffffffffu, stop, 0)) break;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), parity, WAIT_LIMIT_NS);
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), parity, p.wait_ns);
     if (!__all_sync(0xffffffffu, ok)) {
       tip_fail = 1;
       if (lane == 0) atomicOr(&ms->tip_fail, 1);
@@ -595,7 +594,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
       // let copies still in flight land before the shared memory is reused
       for (int s = 0; s < ns; ++s)
         if (ms->tip_last[s] >= 0)
-          mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, WAIT_LIMIT_NS);
+          mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, p.wait_ns);
     }
     __syncthreads();
   }
@@ -724,7 +723,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     }
     bool reload_wait = reload;
     auto reload_done = [&]() {
-      if (reload_wait && !mbar_wait_bounded(rbar, 0u, WAIT_LIMIT_NS)) atomicOr(p.status, 2);
+      if (reload_wait && !mbar_wait_bounded(rbar, 0u, p.wait_ns)) atomicOr(p.status, 2);
       reload_wait = false;
     };
     const float* scr = reload ? reinterpret_cast<const float*>(big) : scr_g;

@@ -56,6 +56,7 @@ struct Params {
   int* count_out;
   float* out;               // [B,Hq,D] fp32
   int* status;              // device status word
+  unsigned long long wait_ns;  // bound of every device wait
   // shared-memory layout (bytes), computed by the host
   int s_cap;                // scores kept per CTA in shared memory (0: global)
   int tip_tile;             // tokens per TIP pipeline tile
@@ -69,6 +70,48 @@ struct Params {
       off_part, off_recv, off_big, smem_total;
 };
 
+// The bf16 fused-step kernel (fasa_step.cuh): its plan and arguments.
+constexpr int ST_MAX_STAGES = 12;  // TIP stage mbarriers [0, 12)
+constexpr int ST_BARS = 16;        // + two selection exchanges, the combine, the score reload
+constexpr int ST_MISC_BYTES = 1024;
+constexpr int UH_BINS = 256;       // histogram of the union's 8-bit digits
+constexpr int TIP_UNIT = 128;      // tokens per warp step of TIP (32 lanes x 4)
+
+struct StepParams {
+  int B, Hq, Hkv, G, T_max, n_tip, budget, flags;
+  // RoPE frequencies as fixed-point turns: theta_i / (2 pi) * 2^64
+  unsigned long long rope_turns[64];
+  const void* q;  // pre-RoPE stored query [B, Hq, D]
+  const int* pos;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_dom;
+  const int* dom_fc;
+  const int* seq_lens;
+  float* scores;  // [B, Hkv, T_max] score workspace when s_cap == 0
+  const void* k_new;  // F_APPEND: the new token's pre-RoPE key [B, Hkv, D]
+  const void* v_new;  //           and value [B, Hkv, D]
+  int* idx_out;
+  int* count_out;
+  float* out;
+  int* status;
+  unsigned long long* trace;  // phase timestamps (tracing builds only)
+  unsigned long long wait_ns; // bound of every device wait
+  int drop_stage;             // test hook: this TIP tile's copy is never issued (-1: none)
+  // plan (host)
+  int s_cap;       // scores per CTA kept in shared memory (0: workspace)
+  int tip_tile;    // tokens per TIP stage (multiple of TIP_UNIT)
+  int tip_stages;  // TIP ring depth (>= the CTA's tiles: no refill)
+  int rho;         // first-round list length per CTA
+  int cap1, cap2;  // receive slots per source CTA, first and second round
+  int spec;        // gather the first-round list before the selection is final
+  int fac_wst;     // FAC groups in flight per warp (1 or 2)
+  int rows_cap;    // capacity of the own-selection list
+  int reload;      // copy workspace scores back into shared memory for the sweeps
+  int off_bar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb, off_big,
+      off_recv2, off_pt, smem_total;
+};
+
 // Kernel launchers (one translation unit per storage type).
 cudaError_t launch_cluster_bf16(const Params& p, int head_dim, int C, cudaStream_t s);
 cudaError_t launch_cluster_f32(const Params& p, int head_dim, int C, cudaStream_t s);
@@ -76,6 +119,8 @@ cudaError_t launch_cluster_f32(const Params& p, int head_dim, int C, cudaStream_
 // of size C for this configuration (0 if C cannot be launched).
 int max_active_clusters_bf16(int flags, int head_dim, int C, int smem_bytes);
 int max_active_clusters_f32(int flags, int head_dim, int C, int smem_bytes);
+cudaError_t launch_step_bf16(const StepParams& p, int head_dim, int C, cudaStream_t s);
+int max_active_clusters_step_bf16(int head_dim, int C, int smem_bytes);
 
 // Contextual Agreement and the choice of dominant FCs (fasa_ca.cu).
 size_t fc_agreement_workspace(int units, int D, int T_max);

@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(PKG, "libfasa.so")
 
 FASA_F32, FASA_BF16 = 0, 1
-FASA_DEV_BAD_INPUT, FASA_DEV_TIMEOUT = 1, 2
+FASA_DEV_BAD_INPUT, FASA_DEV_TIMEOUT, FASA_DEV_UNDRAINED = 1, 2, 4
 
 EXPORTS = [
     "fasa_version", "fasa_status_string", "fasa_last_cuda_error", "fasa_max_budget",
@@ -21,7 +21,7 @@ EXPORTS = [
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
     "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
-    "fasa_select_dominant_fcs", "fasa_compound_agreement",
+    "fasa_select_dominant_fcs", "fasa_compound_agreement", "fasa_test_fault_injection",
 ]
 
 
@@ -93,6 +93,7 @@ def lib():
             "fasa_fc_agreement": ([vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_compound_agreement": ([vp, vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_select_dominant_fcs": ([vp, i32, vp, dp, vp], ctypes.c_int),
+            "fasa_test_fault_injection": ([ctypes.c_uint64, i32], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -308,3 +309,9 @@ def fasa_device_status(stream=None) -> int:
     out = ctypes.c_int32(0)
     _check("fasa_device_status", lib().fasa_device_status(_stream(stream), ctypes.byref(out)))
     return out.value
+
+
+def fasa_test_fault_injection(wait_limit_ns: int = 1_000_000_000, drop_tip_tile: int = -1) -> None:
+    """Test hook: bound of every device wait, and one TIP tile whose copy the
+    fused step never issues (-1: none).  The defaults restore normal runs."""
+    _check("fasa_test_fault_injection", lib().fasa_test_fault_injection(int(wait_limit_ns), int(drop_tip_tile)))
