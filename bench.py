@@ -220,20 +220,30 @@ def unit_bytes(cfg, L: int, h: int = 0) -> int:
     return L * cfg.head_n_tip(h) * 2 * es + min(L, cfg.budget) * 2 * d * es + G * d * es + G * d * 4
 
 
-def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 2):
+def _wait_go(go):
+    """Blocks until the parent process says go (a line on stdin), when asked."""
+    if go:
+        print("ready", flush=True)
+        sys.stdin.readline()
+
+
+def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 2,
+                  unit_offset: int = 0, go: bool = False):
     """Times the fp64 oracle (as it stands, single-threaded numpy) on a bounded
     sample of the workload: each step is one (batch, KV head) unit of the
     decode step -- RoPE of its query group, TIP over its cached tokens, TopK-I
-    and FAC -- cycling over the first `n_units` units, host-generated with the
-    workload's recipe.  Runs `warmup` untimed steps, then timed steps until
-    `max_steps` or `seconds` is reached.  Returns (seconds, steps, bytes)."""
+    and FAC -- cycling over `n_units` units from `unit_offset`, host-generated
+    with the workload's recipe.  Runs `warmup` untimed steps, then timed steps
+    until `max_steps` or `seconds` is reached.  Returns (seconds, steps, bytes)."""
     import oracle as O
     lens = synth.seq_lens(cfg)
     G = cfg.group
     q_all = O.decode_stored(synth.store(synth.gen_q(cfg, 0), cfg.dtype), cfg.dtype)
     dom = synth.dominant_fcs(cfg, 0)
     units = []
-    for u in range(min(n_units, cfg.batch * cfg.n_kv_heads)):
+    n_all = cfg.batch * cfg.n_kv_heads
+    for uu in range(min(n_units, n_all)):
+        u = (unit_offset + uu) % n_all
         b, h = divmod(u, cfg.n_kv_heads)
         L = int(lens[b])
         kk, vv = synth.gen_kv_head(cfg, 0, b, h, t_count=L)
@@ -255,6 +265,7 @@ def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: 
         one(i)
         if time.perf_counter() >= warm_until:
             break
+    _wait_go(go)
     steps, nbytes = 0, 0
     t0 = time.perf_counter()
     while steps < max_steps:
@@ -265,7 +276,8 @@ def oracle_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: 
     return time.perf_counter() - t0, steps, nbytes
 
 
-def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 1):
+def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmup: int = 0, n_units: int = 1,
+                     unit_offset: int = 0, go: bool = False):
     """Times the fp64 oracle's calibration on a bounded sample: each step is one
     (batch, KV head) unit -- RoPE of its query group at position len, then the
     Contextual Agreement (Eq. 4) of every FC over its cached tokens with K = the
@@ -275,7 +287,9 @@ def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmu
     G = cfg.group
     q_all = O.decode_stored(synth.store(synth.gen_q(cfg, 0), cfg.dtype), cfg.dtype)
     units = []
-    for u in range(min(n_units, cfg.batch * cfg.n_kv_heads)):
+    n_all = cfg.batch * cfg.n_kv_heads
+    for uu in range(min(n_units, n_all)):
+        u = (unit_offset + uu) % n_all
         b, h = divmod(u, cfg.n_kv_heads)
         L = int(lens[b])
         kk, _ = synth.gen_kv_head(cfg, 0, b, h, t_count=L)
@@ -293,6 +307,7 @@ def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmu
         one(i)
         if time.perf_counter() >= warm_until:
             break
+    _wait_go(go)
     steps, nbytes = 0, 0
     t0 = time.perf_counter()
     while steps < max_steps:
@@ -303,18 +318,44 @@ def oracle_ca_sample(cfg, seconds: float = 12.0, max_steps: int = 10 ** 9, warmu
     return time.perf_counter() - t0, steps, nbytes
 
 
-def run_oracle_leg(cfg, seconds: float, max_steps: int = 10 ** 9, warmup: int = 0, fn: str = "oracle_sample"):
-    """Runs oracle_sample (or `fn`) in a child process with BLAS limited to one
-    thread so the reported core count is exact."""
+def run_oracle_leg(cfg, seconds: float, max_steps: int = 10 ** 9, warmup: int = 0, fn: str = "oracle_sample",
+                   procs: int = 0):
+    """Runs oracle_sample (or `fn`) on every host core: one child process per
+    core, each with BLAS limited to one thread and its own units of the
+    workload.  The children set up their inputs, then start their timed loops
+    together; the result sums their steps and bytes over the longest timed
+    loop.  Returns dict(seconds, steps, bytes, procs, steps_per_proc)."""
+    procs = procs or (os.cpu_count() or 1)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import json,sys; sys.path.insert(0, %r); import bench; from workload import configs; "
-            "cfg = configs.CONFIGS[%r]; t, n, b = bench.%s(cfg, %r, %r, %r); "
-            "print(json.dumps({'seconds': t, 'steps': n, 'bytes': b}))"
-            % (ROOT, cfg.name, fn, seconds, max_steps, warmup))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    kids = []
+    for i in range(procs):
+        code = ("import json,sys; sys.path.insert(0, %r); import bench; from workload import configs; "
+                "cfg = configs.CONFIGS[%r]; t, n, b = bench.%s(cfg, %r, %r, %r, unit_offset=%d, go=True); "
+                "print(json.dumps({'seconds': t, 'steps': n, 'bytes': b}), flush=True)"
+                % (ROOT, cfg.name, fn, seconds, max_steps, warmup, 2 * i))
+        kids.append(subprocess.Popen([sys.executable, "-c", code], env=env, stdin=subprocess.PIPE,
+                                     stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+    try:
+        for k in kids:   # every child has its inputs ready
+            line = k.stdout.readline()
+            if line.strip() != "ready":
+                raise RuntimeError(f"oracle child failed before timing: {line!r} {k.stderr.read()[-2000:]}")
+        for k in kids:
+            k.stdin.write("go\n")
+            k.stdin.flush()
+        res = []
+        for k in kids:
+            out, err = k.communicate(timeout=1800)
+            if k.returncode != 0:
+                raise RuntimeError(err[-2000:])
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    finally:
+        for k in kids:
+            if k.poll() is None:
+                k.kill()
+    return dict(seconds=max(r["seconds"] for r in res), steps=sum(r["steps"] for r in res),
+                bytes=sum(r["bytes"] for r in res), procs=procs,
+                steps_per_proc=max(r["steps"] for r in res))
 
 
 # ----------------------------------------------------------------------------
@@ -333,6 +374,18 @@ def make_replicas(cfg, R, dims):
         reps.append((L, kd))
     torch.cuda.synchronize()
     return reps
+
+
+SUBMIT_DELAY_S = 100e-6
+
+
+def gpu_delay(seconds: float):
+    """A bounded spin on the GPU (torch's sleep kernel, about `seconds` at the
+    maximum SM clock) on the current stream."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(seconds * 2.07e9))
 
 
 def capture(fn, n_steps, stream):
@@ -441,23 +494,29 @@ def run_gpu(args):
     if status:
         raise RuntimeError(f"device status {status} after warm-up")
 
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # T trials of exactly K timed steps each; the reported time is the median
+    # trial.  Before each trial a short GPU-side delay (a bounded spin) keeps
+    # the GPU busy while the host submits the graphs, so the trial times
+    # device execution, not graph submission.
+    trials = max(1, args.trials)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(trials)]
     barrier(pg, local)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):   # graphs replay on the current stream
-            ev0.record(stream)
-            for _ in range(KL // chunk):
-                g_chunk.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            ev1.record(stream)
+            for ev0, ev1 in evs:
+                gpu_delay(SUBMIT_DELAY_S)
+                ev0.record(stream)
+                for _ in range(KL // chunk):
+                    g_chunk.replay()
+                if g_rem is not None:
+                    g_rem.replay()
+                ev1.record(stream)
         torch.cuda.synchronize()
     barrier(pg, local)
     torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
-    ms_total = max_over_ranks(pg, ms_total)
-    sec_per_step = ms_total / 1e3 / K
+    trial_ms = [max_over_ranks(pg, ev0.elapsed_time(ev1)) for ev0, ev1 in evs]
+    sec_per_step = statistics.median(trial_ms) / 1e3 / K
 
     # dense baseline (same machinery), fewer steps
     Kd = max(R, min(K // 8, 4096))
@@ -581,9 +640,10 @@ def run_gpu(args):
     line = None
     if args.cpu_baseline and rank == 0 and world == 1:
         cb = run_oracle_leg(cfg, args.cpu_seconds)
-        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s "
-                         f"(host-generated inputs, numpy fp64, 1 BLAS thread); "
+        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": cb["procs"], "kind": "oracle",
+               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s on "
+                         f"{cb['procs']} host cores (one process per core, 1 BLAS thread each, timed loops "
+                         f"started together; host-generated inputs, numpy fp64); "
                          f"{cb['seconds'] / cb['steps'] * B * H * layers * 1e6:.0f} us per whole decode step"}
     else:
         cpu = None
@@ -597,6 +657,11 @@ def run_gpu(args):
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(sec_per_step * 1e3, 6),
             "us_per_step": round(sec_per_step * 1e6, 3),
+            "trials": {"n": trials, "statistic": "median",
+                       "us_per_step": [round(t * 1e3 / K, 3) for t in trial_ms],
+                       "timing": f"{trials} trials of exactly {K} steps (CUDA-graph replay, CUDA events on the "
+                                 f"launching stream; a {SUBMIT_DELAY_S * 1e6:.0f} us GPU spin before each trial "
+                                 f"keeps graph submission out of the timed region)"},
             "tokens_per_s": round(world * B / sec_per_step, 1),
             "higher_is_better": True,
             "scaling": "weak",
@@ -776,9 +841,10 @@ def run_calibrate(args):
     cpu = None
     if args.cpu_baseline and rank == 0 and world == 1:
         cb = run_oracle_leg(cfg, args.cpu_seconds, fn="oracle_ca_sample")
-        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s "
-                         f"(host-generated inputs, numpy fp64, 1 BLAS thread); "
+        cpu = {"value": cb["bytes"] / cb["seconds"] / 1e12, "unit": "TB/s", "cores": cb["procs"], "kind": "oracle",
+               "sample": f"{cb['steps']} (batch, KV head) units of {cfg.name} in {cb['seconds']:.1f} s on "
+                         f"{cb['procs']} host cores (one process per core, 1 BLAS thread each; host-generated "
+                         f"inputs, numpy fp64); "
                          f"{cb['seconds'] / cb['steps'] * B * H * 1e3:.0f} ms per whole call"}
     if rank == 0:
         line = {
@@ -815,9 +881,10 @@ def run_calibrate(args):
 
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle timed on the host cores.  Each step is
-    one (batch, KV head) unit of the workload (a bounded sample); W untimed
-    warm-up steps, then at most K timed steps, stopped after --cpu-seconds."""
+    """The reference arm: the fp64 oracle timed on every host core.  One step
+    is one (batch, KV head) unit of the workload on each core at once (a
+    bounded sample); W untimed warm-up steps, then at most K timed steps,
+    stopped after --cpu-seconds."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
@@ -827,21 +894,23 @@ def run_reference(args):
     cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps, args.warmup,
                         fn="oracle_ca_sample" if cal else "oracle_sample")
     val = cb["bytes"] / cb["seconds"] / 1e12
-    per_unit = cb["seconds"] / cb["steps"]
+    per_step = cb["seconds"] / cb["steps_per_proc"]
     line = {
         "impl": "reference",
         "metric": CA_METRIC if cal else METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
-        "steps": cb["steps"], "warmup": args.warmup,
-        "ms_per_step": per_unit * 1e3, "higher_is_better": True, "scaling": "weak",
+        "steps": cb["steps_per_proc"], "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, host-generated)",
         "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.n_q_heads,
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "context": cfg.context,
                    "n_tip": cfg.n_tip, "budget": cfg.budget,
-                   "step": "one (batch, KV head) unit of the "
-                           + ("calibration (CA of every FC, topk = budget)" if cal else "decode step")},
-        "cpu_baseline": {"value": val, "unit": "TB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{cb['steps']} units in {cb['seconds']:.1f} s, bounded to "
-                                   f"~{args.cpu_seconds:.0f} s (numpy fp64, 1 BLAS thread)"},
+                   "step": f"one (batch, KV head) unit of the "
+                           + ("calibration (CA of every FC, topk = budget)" if cal else "decode step")
+                           + f" on each of {cb['procs']} host cores"},
+        "cpu_baseline": {"value": val, "unit": "TB/s", "cores": cb["procs"], "kind": "oracle",
+                         "sample": f"{cb['steps']} units in {cb['seconds']:.1f} s on {cb['procs']} cores, bounded "
+                                   f"to ~{args.cpu_seconds:.0f} s (numpy fp64, one process per core, 1 BLAS "
+                                   f"thread each)"},
         "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -864,6 +933,8 @@ def main(argv=None):
                          "fasa_decode_step")
     ap.add_argument("--calibrate", action="store_true",
                     help="time the offline calibration (fasa_fc_agreement) instead of the decode step")
+    ap.add_argument("--trials", type=int, default=5,
+                    help="timed trials of K steps each; the median trial is reported")
     ap.add_argument("--replicas", type=int, default=0,
                     help="input replicas rotated through (0: enough to exceed 4x L2, as timing requires; "
                          "a smaller count is for profiler captures)")

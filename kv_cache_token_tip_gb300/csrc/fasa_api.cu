@@ -28,10 +28,6 @@ thread_local int t_last_cuda_error = 0;
 unsigned long long g_wait_ns = 1000000000ull;
 int g_drop_tip_tile = -1;
 
-#ifdef FASA_PHASE_TRACE
-// Phase timestamps of the step kernel (tracing builds only): 16 per CTA.
-unsigned long long* g_trace = nullptr;
-#endif
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
@@ -359,11 +355,14 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.off_sc = off;
   off += s_cap * 4;
   p.off_recv1 = off;
-  off += C * cap1 * 8;
+  off += C * (cap1 + 2) * 8;  // per source: a 16-byte header, then the entries
   p.off_rows = off;
   off += align_up(rows_cap * 4, 16);
+  const int comb_slot = sl * 16 + align_up(G * 8, 16);
   p.off_comb = off;
-  off += align_up(C * sl * 16 + C * G * 8, 16);
+  off += C * comb_slot;
+  p.off_comb_snd = off;
+  off += C * comb_slot;
   off = align_up(off, 128);
   p.off_big = off;
   const int room = limit - off;
@@ -372,8 +371,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   // only once every CTA drained its gathers), the warp records
   auto fac_slots = [&](int wst) { return wst * NW * 2 * GR * D * ES; };
   const int pt_bytes = NW * G_MAX * PTS * 4;
-  const int rec_bytes = (G_MAX * NW * (D + 2) + G_MAX * (D + 4) + G_MAX * NW + G_MAX) * 4;
-  const int recv2_bytes = C * cap2 * 8;
+  const int rec_bytes = (G_MAX * NW * (D + 2) + G_MAX * NW + G_MAX) * 4;
+  const int recv2_bytes = C == 1 ? 0 : C * (cap2 + 2) * 8;
   // TIP staging: the whole range at once (no refill) with the smallest tile
   // that needs at most ST_MAX_STAGES stages, else a ring of at least two
   // stages holding up to 128 KB.  Warp w scores the 128-token units w,
@@ -427,6 +426,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.fac_wst = wst;
   p.rows_cap = rows_cap;
   p.reload = reload;
+  p.comb_slot = comb_slot;
   p.off_recv2 = p.off_big;
   p.off_pt = p.off_big + fac_slots(wst);
   p.smem_total = p.off_big + big;
@@ -448,9 +448,6 @@ void fill_step(StepParams& p, const fasa_dims_t* d, int32_t budget) {
   memcpy(p.rope_turns, tmp.rope_turns, sizeof(p.rope_turns));
   p.wait_ns = g_wait_ns;
   p.drop_stage = g_drop_tip_tile;
-#ifdef FASA_PHASE_TRACE
-  p.trace = g_trace;
-#endif
 }
 
 // The bf16 step kernel serves fasa_decode_step when these dims plan.
@@ -982,9 +979,6 @@ int fasa_select_dominant_fcs(const float* ca_mean, int32_t n_tip, int32_t* dom_f
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);
 }
 
-#ifdef FASA_PHASE_TRACE
-void fasa_debug_set_trace(void* buf) { g_trace = reinterpret_cast<unsigned long long*>(buf); }
-#endif
 
 int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile) {
   if (wait_limit_ns == 0 || drop_tip_tile < -1) return FASA_ERR_INVALID_ARG;

@@ -95,7 +95,6 @@ struct StepParams {
   int* count_out;
   float* out;
   int* status;
-  unsigned long long* trace;  // phase timestamps (tracing builds only)
   unsigned long long wait_ns; // bound of every device wait
   int drop_stage;             // test hook: this TIP tile's copy is never issued (-1: none)
   // plan (host)
@@ -108,8 +107,9 @@ struct StepParams {
   int fac_wst;     // FAC groups in flight per warp (1 or 2)
   int rows_cap;    // capacity of the own-selection list
   int reload;      // copy workspace scores back into shared memory for the sweeps
-  int off_bar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb, off_big,
-      off_recv2, off_pt, smem_total;
+  int comb_slot;   // bytes of one combine slot: an output slice and every head's (m, l)
+  int off_bar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb, off_comb_snd,
+      off_big, off_recv2, off_pt, smem_total;
 };
 
 // Kernel launchers (one translation unit per storage type).

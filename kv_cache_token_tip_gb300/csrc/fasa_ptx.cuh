@@ -170,6 +170,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 1-D bulk copy from this CTA's shared memory to another CTA's of the
+// cluster (dst and bar from dsmem_map), completion on that CTA's barrier.
+// src, dst 16-byte aligned, bytes a multiple of 16.  The source must have
+// been made visible to the async proxy (fence_proxy_async) by its writers.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ---- cp.async (16-byte, L2-only) ---------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");

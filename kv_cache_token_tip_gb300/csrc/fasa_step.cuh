@@ -28,21 +28,24 @@
 //      accumulation).  The per-head partial records (o, m, l) are cut into
 //      output slices and pushed to the CTAs that finish those slices.
 //
-// Exchanges are distributed-shared-memory stores followed by one
-// release-arrive per destination on that CTA's mbarrier: a CTA waits only
-// for the data it needs, every wait is bounded, and one cluster barrier at
-// the end keeps each CTA's shared memory alive until no peer can touch it.
+// The exchange and the combine move each CTA's list or record slice to the
+// other CTAs as one bulk copy per destination (shared memory to shared
+// memory), completing on the destination's mbarrier: a CTA waits only for
+// the data it needs, every wait is bounded, and one cluster barrier at the
+// end keeps each CTA's shared memory alive until no copy or peer can touch
+// it.
 #pragma once
 
 #include <limits.h>
 
+#include "../../include/fasa.h"
 #include "fasa_cluster.cuh"
 
 namespace fasa {
 
-constexpr int SB_X1 = 12;          // first selection exchange (C arrivals)
+constexpr int SB_X1 = 12;          // first selection exchange (the peers' bulk copies)
 constexpr int SB_X2 = 13;          // second selection exchange (C arrivals)
-constexpr int SB_COMB = 14;        // partial records for the combine (C arrivals)
+constexpr int SB_COMB = 14;        // partial records for the combine (the peers' bulk copies)
 constexpr int SB_RELOAD = 15;      // score reload from the workspace
 
 
@@ -56,10 +59,14 @@ struct StepMisc {
   int hist_clobbered;   // the digit-0 histogram was overwritten by later digits
   uint32_t tip_done[ST_MAX_STAGES];
   int tip_last[ST_MAX_STAGES];
-  int4 hdr1[C_MAX];     // per source CTA: (listed, cut short, shared staging unusable, -)
-  int4 hdr2[C_MAX];
   int sel[C_MAX];       // per source CTA: its entries >= theta
   int n_rows;
+  uint32_t list_max;    // largest key listed
+  int bkt_n;            // entries gathered from the union's threshold bucket
+  unsigned long long theta;
+  uint32_t chist[64];   // coarse histogram of the score keys (key >> 26)
+  unsigned long long bkt[32];
+  int bkt_src[32];
 };
 static_assert(sizeof(StepMisc) <= ST_MISC_BYTES, "step scratch too small");
 
@@ -71,10 +78,17 @@ struct SelRule {
 };
 
 #ifdef FASA_PHASE_TRACE
-#define STEP_TRACE(i)                                                                   \
-  do {                                                                                  \
-    if (threadIdx.x == 0 && p.trace)                                                    \
-      p.trace[((size_t)blockIdx.y * gridDim.x + blockIdx.x) * 16 + (i)] = global_timer_ns(); \
+// Tracing builds: lane 0 of every warp stores globaltimer (ns) in slot i and
+// clock64 in slot 32 + i of its 64-slot record; 32 slots per warp.
+__device__ unsigned long long* g_step_trace;
+#define STEP_TRACE(i)                                                                                 \
+  do {                                                                                                \
+    if ((threadIdx.x & 31) == 0 && g_step_trace) {                                                    \
+      unsigned long long* tr_ =                                                                       \
+          g_step_trace + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * NW + (threadIdx.x >> 5)) * 64; \
+      tr_[(i)] = global_timer_ns();                                                                   \
+      tr_[32 + (i)] = clock64();                                                                      \
+    }                                                                                                 \
   } while (0)
 #else
 #define STEP_TRACE(i) \
@@ -83,6 +97,14 @@ struct SelRule {
 #endif
 
 __device__ __forceinline__ int warp_sum_i(int v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// 2^x by the hardware approximation (relative error ~2^-22; -inf -> +0):
+// the softmax weights need far less than that.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Exclusive prefix over the lanes of a warp.
 __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
@@ -101,32 +123,30 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
 template <int NB>
 __device__ __forceinline__ void find_digit(const uint32_t* hist, int k_rem, int* scan, int* out) {
   constexpr int M = NB / NT;
-  static_assert(M >= 1 && NB % NT == 0 && M % 4 == 0, "bins per thread");
+  static_assert(M >= 4 && NB % NT == 0 && M % 4 == 0, "bins per thread");
   const int tid = threadIdx.x;
   const int base = NB - (tid + 1) * M;
-  uint32_t c[M];
-#pragma unroll
-  for (int q = 0; q < M / 4; ++q) {
-    const uint4 v = reinterpret_cast<const uint4*>(hist + base)[q];
-    c[4 * q] = v.x;
-    c[4 * q + 1] = v.y;
-    c[4 * q + 2] = v.z;
-    c[4 * q + 3] = v.w;
-  }
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist + base);
   int tsum = 0;
-#pragma unroll
-  for (int i = 0; i < M; ++i) tsum += (int)c[i];
+#pragma unroll 1
+  for (int q = 0; q < M / 4; ++q) {
+    const uint4 v = h4[q];
+    tsum += (int)(v.x + v.y + v.z + v.w);
+  }
   int total;
   int run = block_excl_scan(tsum, scan, total);
-#pragma unroll
-  for (int i = M - 1; i >= 0; --i) {
-    const int ci = (int)c[i];
-    if (run < k_rem && k_rem <= run + ci) {
-      out[0] = base + i;
-      out[1] = run;
-      out[2] = ci;
+  if (run < k_rem && k_rem <= run + tsum) {  // the digit is among this thread's bins
+#pragma unroll 1
+    for (int i = M - 1; i >= 0; --i) {
+      const int ci = (int)hist[base + i];
+      if (k_rem <= run + ci) {
+        out[0] = base + i;
+        out[1] = run;
+        out[2] = ci;
+        break;
+      }
+      run += ci;
     }
-    run += ci;
   }
   __syncthreads();
 }
@@ -168,22 +188,18 @@ __device__ __forceinline__ void tip4(const unsigned char* row, int nfc_rt, const
   for (int t = 0; t < 4; ++t) acc[t] = a0[t] + a1[t];
 }
 
-// Up to four scores at scr[tl..tl+4) below `end`, as keys; ok marks the valid ones.
+// The four scores at scr[tl..tl+4) as keys; ok marks those below `end`.
+// tl is a multiple of 4 and the score buffers extend to a multiple of 4
+// (shared memory: the CTA's whole token chunk; workspace: T_max), so the
+// 16-byte load stays inside them.
 __device__ __forceinline__ void keys4(const float* scr, int tl, int end, uint32_t (&key)[4], bool (&ok)[4]) {
-  if (tl + 4 <= end) {
-    const float4 x = *reinterpret_cast<const float4*>(scr + tl);
-    key[0] = score_key(x.x);
-    key[1] = score_key(x.y);
-    key[2] = score_key(x.z);
-    key[3] = score_key(x.w);
-    ok[0] = ok[1] = ok[2] = ok[3] = true;
-  } else {
+  const float4 x = *reinterpret_cast<const float4*>(scr + tl);
+  key[0] = score_key(x.x);
+  key[1] = score_key(x.y);
+  key[2] = score_key(x.z);
+  key[3] = score_key(x.w);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      ok[t] = tl + t < end;
-      key[t] = ok[t] ? score_key(scr[tl + t]) : 0u;
-    }
-  }
+  for (int t = 0; t < 4; ++t) ok[t] = tl + t < end;
 }
 
 // The rule that selects this CTA's top r scores (stable order) -- or, when
@@ -191,14 +207,16 @@ __device__ __forceinline__ void keys4(const float* scr, int tl, int end, uint32_
 // (a longer prefix of the same order).  scr holds the CTA's nloc scores;
 // hist the digit-0 histogram of their keys (rebuilt first unless hist_ok).
 // Later digits (10 + 10 bits) overwrite the histogram.  Every thread calls it.
-__device__ SelRule local_rule(int r, int cap, bool hist_ok, const float* scr, int nloc, uint32_t* hist,
-                              StepMisc* ms) {
+__device__ __noinline__ SelRule local_rule(int r, int cap, bool hist_ok, const float* scr, int nloc,
+                                           uint32_t* hist, StepMisc* ms) {
   const int tid = threadIdx.x;
   if (r >= nloc) return SelRule{0u, INT_MAX};  // every key is >= 0
   if (!hist_ok) {
     uint4* z = reinterpret_cast<uint4*>(hist);
+#pragma unroll 1
     for (int i = tid; i < HLOC_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
+#pragma unroll 1
     for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
       uint32_t key[4];
       bool ok[4];
@@ -217,10 +235,13 @@ __device__ SelRule local_rule(int r, int cap, bool hist_ok, const float* scr, in
   if (tid == 0) ms->hist_clobbered = 1;
   int k_rem = r - gt0;
   uint32_t prefix = (uint32_t)d0;
+#pragma unroll 1
   for (int dg = 1; dg <= 2; ++dg) {
     const int shift = dg == 1 ? 10 : 0;
+#pragma unroll 1
     for (int i = tid; i < 1024; i += NT) hist[i] = 0u;
     __syncthreads();
+#pragma unroll 1
     for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
       uint32_t key[4];
       bool ok[4];
@@ -241,17 +262,21 @@ __device__ SelRule local_rule(int r, int cap, bool hist_ok, const float* scr, in
 // Lists the entries of this CTA's nloc scores (tokens t0..) that rule R
 // selects, in token order, into dst as packed (key << 32 | ~token): a
 // larger value comes earlier in the stable order.  Warp w sweeps its own
-// contiguous share of the tokens, four per lane per step.  Returns the count
-// (at most cap entries are written).  Every thread calls it.
-__device__ int list_rule(SelRule R, const float* scr, int nloc, int t0, unsigned long long* dst, int cap,
-                         StepMisc* ms) {
+// contiguous share of the tokens, four per lane per step (lane-major token
+// order, so a lane's place follows from ballots).  Returns the count (at
+// most cap entries are written).  Every thread calls it.
+template <bool TIES>
+__device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc, int t0, unsigned long long* dst,
+                                           int cap, StepMisc* ms) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool ties = R.need != INT_MAX;
+  const unsigned lt = (1u << lane) - 1u;
+  constexpr bool ties = TIES;
   const int wlen = (((nloc + NW - 1) / NW) + 3) & ~3;
   const int w0 = min(nloc, warp * wlen), w1 = min(nloc, w0 + wlen);
   int tie_base = 0;
-  if (ties) {
+  if constexpr (ties) {
     int c = 0;
+#pragma unroll 1
     for (int tl = w0 + lane * 4; tl < w1; tl += 128) {
       uint32_t key[4];
       bool ok[4];
@@ -262,38 +287,42 @@ __device__ int list_rule(SelRule R, const float* scr, int nloc, int t0, unsigned
     c = warp_sum_i(c);
     if (lane == 0) ms->scan2[warp] = c;
     __syncthreads();
+#pragma unroll 1
     for (int w = 0; w < warp; ++w) tie_base += ms->scan2[w];
   }
-  // selection flags of a lane's four tokens; tb = ties before this step (CTA)
-  auto flags4 = [&](int tl, int tb, uint32_t (&key)[4], bool (&sel)[4], int& nties) {
+  // selection flags of a lane's four tokens; tb = this CTA's ties before the
+  // step, returned advanced past it
+  auto flags4 = [&](int tl, int& tb, uint32_t (&key)[4], bool (&sel)[4]) {
     bool ok[4];
     keys4(scr, tl, w1, key, ok);
-    int lt = 0;
+    if constexpr (!ties) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) lt += ok[t] && key[t] == R.thr;
-    int before = 0;
-    nties = 0;
-    if (ties) {
-      before = warp_excl_scan(lt, lane);
-      nties = __shfl_sync(0xffffffffu, before + lt, 31);
+      for (int t = 0; t < 4; ++t) sel[t] = ok[t] && key[t] >= R.thr;
+      return;
     }
-    int rank = tb + before;
+    bool tie[4];
+    int rank = tb;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const bool tie = ok[t] && key[t] == R.thr;
-      sel[t] = ok[t] && (key[t] > R.thr || (tie && rank < R.need));
-      rank += tie;
+      tie[t] = ok[t] && key[t] == R.thr;
+      const unsigned bt = __ballot_sync(0xffffffffu, tie[t]);
+      rank += __popc(bt & lt);
+      tb += __popc(bt);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      sel[t] = ok[t] && (key[t] > R.thr || (tie[t] && rank < R.need));
+      rank += tie[t];
     }
   };
   int cnt = 0;
   {
     int tb = tie_base;
+#pragma unroll 1
     for (int tl0 = w0; tl0 < w1; tl0 += 128) {
       uint32_t key[4];
       bool sel[4];
-      int nt;
-      flags4(tl0 + lane * 4, tb, key, sel, nt);
-      tb += nt;
+      flags4(tl0 + lane * 4, tb, key, sel);
 #pragma unroll
       for (int t = 0; t < 4; ++t) cnt += sel[t];
     }
@@ -301,6 +330,7 @@ __device__ int list_rule(SelRule R, const float* scr, int nloc, int t0, unsigned
   cnt = warp_sum_i(cnt);
   if (lane == 0) ms->scan[warp] = cnt;
   __syncthreads();
+  STEP_TRACE(26);
   int base = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
@@ -309,126 +339,421 @@ __device__ int list_rule(SelRule R, const float* scr, int nloc, int t0, unsigned
     total += c;
   }
   int tb = tie_base;
+  uint32_t kmax = 0u;
+#pragma unroll 1
   for (int tl0 = w0; tl0 < w1; tl0 += 128) {
     uint32_t key[4];
     bool sel[4];
-    int nt;
     const int tl = tl0 + lane * 4;
-    flags4(tl, tb, key, sel, nt);
-    tb += nt;
-    const int mine = (int)sel[0] + (int)sel[1] + (int)sel[2] + (int)sel[3];
-    const int bef = warp_excl_scan(mine, lane);
-    int at = base + bef;
+    flags4(tl, tb, key, sel);
+    int at = base;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const unsigned bs = __ballot_sync(0xffffffffu, sel[t]);
+      at += __popc(bs & lt);
+      base += __popc(bs);
+    }
 #pragma unroll
     for (int t = 0; t < 4; ++t)
       if (sel[t]) {
         if (at < cap)
           dst[at] = ((unsigned long long)key[t] << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)(t0 + tl + t));
         ++at;
+        kmax = max(kmax, key[t]);
       }
-    base += __shfl_sync(0xffffffffu, bef + mine, 31);
   }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0 && kmax) atomicMax(&ms->list_max, kmax);
   __syncthreads();
   return min(total, cap);
 }
 
-// Sends this CTA's list (slot crank of `recv`, n entries, already in place
-// locally) and its header to every other CTA of the cluster, then arrives on
-// every CTA's exchange barrier `bar_off`.  Every thread calls it.
-__device__ __forceinline__ void push_list(unsigned long long* recv, int cap, int n, int4 hdr, int4* hdrs,
-                                          uint32_t bar_local, uint32_t crank, int C) {
-  const int tid = threadIdx.x;
-  const int nvec = (n + 1) >> 1;  // 16-byte vectors of two entries
-  const uint32_t slot = smem_u32(recv + (size_t)crank * cap);
-  const uint4* src = reinterpret_cast<const uint4*>(recv + (size_t)crank * cap);
-  for (int x = tid; x < (C - 1) * nvec; x += NT) {
-    const int rr = x / nvec, v = x - rr * nvec;
+// list_rule_t for any rule, out of line (ties on the threshold key, second round).
+__device__ __noinline__ int list_rule_any(SelRule R, const float* scr, int nloc, int t0, unsigned long long* dst,
+                                          int cap, StepMisc* ms) {
+  return R.need == INT_MAX ? list_rule_t<false>(R, scr, nloc, t0, dst, cap, ms)
+                           : list_rule_t<true>(R, scr, nloc, t0, dst, cap, ms);
+}
+
+// Exchange slots: slot r of a receive region holds source CTA r's list --
+// a 16-byte header (int4: entries, cut short, staging unusable, -) and then
+// the entries (packed u64), `stride` u64 per slot in all.
+__device__ __forceinline__ int4* slot_hdr(unsigned long long* recv, int stride, int r) {
+  return reinterpret_cast<int4*>(recv + (size_t)r * stride);
+}
+__device__ __forceinline__ const int4* slot_hdr(const unsigned long long* recv, int stride, int r) {
+  return reinterpret_cast<const int4*>(recv + (size_t)r * stride);
+}
+
+// Sends this CTA's slot (header and n entries, in place locally) to every
+// other CTA of the cluster with distributed-shared-memory stores, then
+// arrives on every CTA's barrier (count C).  Every thread calls it.
+__device__ __forceinline__ void push_list(unsigned long long* recv, int stride, int n, uint32_t bar_local,
+                                          uint32_t crank, int C) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = (n + 3) >> 1;  // 16-byte vectors: the header, then two entries each
+  const uint32_t slot = smem_u32(recv + (size_t)crank * stride);
+  const uint4* src = reinterpret_cast<const uint4*>(recv + (size_t)crank * stride);
+#pragma unroll 1
+  for (int rr = warp; rr < C - 1; rr += NW) {  // warp per destination, lanes over the vectors
     const uint32_t r = (uint32_t)(rr + (rr >= (int)crank));
-    dsmem_st_v4u32(dsmem_map(slot + v * 16, r), src[v]);
+#pragma unroll 1
+    for (int v = lane; v < nvec; v += 32) dsmem_st_v4u32(dsmem_map(slot + v * 16, r), src[v]);
   }
-  if (tid < C)
-    dsmem_st_v4u32(dsmem_map(smem_u32(&hdrs[crank]), (uint32_t)tid),
-                   make_uint4((uint32_t)hdr.x, (uint32_t)hdr.y, (uint32_t)hdr.z, (uint32_t)hdr.w));
   __syncthreads();
   if (tid < C) mbar_arrive_remote(dsmem_map(bar_local, (uint32_t)tid));
 }
 
-// The k-th largest value theta of the union of the C received lists (slot r
-// holds hdrs[r].x entries; values are distinct), by 8-bit most-significant
-// digits: exactly k entries are >= theta (the caller guarantees the union
-// holds at least k).  Also stores per source the count of its entries >=
-// theta in ms->sel.  Every thread calls it.
-__device__ unsigned long long union_kth(const unsigned long long* recv, const int4* hdrs, int cap, int C, int k,
-                                        uint32_t* uh, StepMisc* ms) {
+// The k-th largest value theta of the union of the C received lists (exchange
+// slots of `stride` u64, slot r holding its header's count of entries, at
+// most cap; values are distinct): exactly k entries are >=
+// theta (the caller guarantees the union holds at least k).  The bits above
+// the highest one where the union's maximum and minimum differ are common to
+// every entry; the rest is resolved by 11-bit digits, most significant
+// first, each a histogram in `hb` (2048 bins).  Also stores per source the
+// count of its entries >= theta in ms->sel.  Every thread calls it.
+__device__ __noinline__ unsigned long long union_kth(const unsigned long long* recv, int stride, int cap, int C,
+                                                     int k, uint32_t* hb, StepMisc* ms) {
+  constexpr int NB = 2048, DB = 11;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  static_assert(NT == UH_BINS, "one digit bin per thread");
-  unsigned long long prefix = 0ull;
-  int shift = 64, k_rem = k;
   const int nslots = C * cap;
-  while (true) {
-    shift -= 8;
-    uh[tid] = 0u;
-    __syncthreads();
-    for (int f = tid; f < nslots; f += NT) {
-      const int r = f / cap, i = f - r * cap;
-      if (i < hdrs[r].x) {
-        const unsigned long long x = recv[f];
-        if (shift == 56 || (x >> (shift + 8)) == prefix) atomicAdd(&uh[(uint32_t)(x >> shift) & 255u], 1u);
-      }
+  const float inv_cap = 1.f / (float)cap;
+  // slot f = r * cap + i of the flattened lists; (f + 0.5) / cap stays at
+  // least 0.5 / cap away from an integer, far above the fp32 rounding error
+  auto entry = [&](int f, unsigned long long& x) -> bool {
+    const int r = __float2int_rz(((float)f + 0.5f) * inv_cap);
+    const int i = f - r * cap;
+    if (i >= slot_hdr(recv, stride, r)->x) return false;
+    x = recv[(size_t)r * stride + 2 + i];
+    return true;
+  };
+  unsigned long long mx = 0ull, mn = ~0ull;
+#pragma unroll 1
+  for (int f = tid; f < nslots; f += NT) {
+    unsigned long long x;
+    if (entry(f, x)) {
+      mx = max(mx, x);
+      mn = min(mn, x);
     }
-    __syncthreads();
-    if (warp == 0) {
-      // lane L owns bins 255 - 8L - j, j = 0..7, counted from the top
-      uint32_t c[8];
-      int s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = uh[255 - 8 * lane - j];
-        s += (int)c[j];
-      }
-      int run = warp_excl_scan(s, lane);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (run < k_rem && k_rem <= run + (int)c[j]) {
-          ms->dig = 255 - 8 * lane - j;
-          ms->gt = run;
-          ms->bucket = (int)c[j];
-        }
-        run += (int)c[j];
-      }
-    }
-    __syncthreads();
-    const int d = ms->dig, gt = ms->gt, bucket = ms->bucket;
-    k_rem -= gt;
-    prefix = (prefix << 8) | (unsigned long long)d;
-    if (bucket == k_rem || shift == 0) break;
   }
-  const unsigned long long theta = prefix << shift;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  }
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(hb);  // [NW] maxima, [NW] minima
+  if (lane == 0) {
+    red[warp] = mx;
+    red[NW + warp] = mn;
+  }
+  __syncthreads();
+  mx = red[0];
+  mn = red[NW];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    mx = max(mx, red[w]);
+    mn = min(mn, red[NW + w]);
+  }
+  __syncthreads();
+  STEP_TRACE(16);
+  const unsigned long long diff = mx ^ mn;
+  int shift = diff ? 64 - __clzll((long long)diff) : 0;  // bits below `shift` are still open
+  unsigned long long prefix = shift == 64 ? 0ull : (mx >> shift);
+  int k_rem = k;
+  int* res = &ms->dig;
+  int pass = 0;
+  while (shift > 0) {
+    const int nb = min(DB, shift);
+    shift -= nb;
+    {
+      uint4* z = reinterpret_cast<uint4*>(hb);
+#pragma unroll 1
+      for (int i = tid; i < NB / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int f = tid; f < nslots; f += NT) {
+      unsigned long long x;
+      if (entry(f, x) && (shift + nb == 64 || (x >> (shift + nb)) == prefix))
+        atomicAdd(&hb[(uint32_t)(x >> shift) & ((1u << nb) - 1u)], 1u);
+    }
+    __syncthreads();
+    if (pass < 3) STEP_TRACE(17 + 2 * pass);
+    find_digit<NB>(hb, k_rem, ms->scan, res);
+    if (pass < 3) STEP_TRACE(18 + 2 * pass);
+    ++pass;
+    k_rem -= res[1];
+    prefix = (prefix << nb) | (unsigned long long)res[0];
+    if (res[2] == k_rem) break;
+  }
+  const unsigned long long theta = shift == 64 ? 0ull : (prefix << shift);
+#pragma unroll 1
   for (int r = warp; r < C; r += NW) {
     int c = 0;
-    for (int i = lane; i < hdrs[r].x; i += 32) c += recv[(size_t)r * cap + i] >= theta;
+#pragma unroll 1
+    for (int i = lane; i < slot_hdr(recv, stride, r)->x; i += 32) c += recv[(size_t)r * stride + 2 + i] >= theta;
     c = warp_sum_i(c);
     if (lane == 0) ms->sel[r] = c;
   }
   __syncthreads();
+  STEP_TRACE(23);
   return theta;
+}
+
+// Warp 0: the digit-0 bin (key >> 20) holding the r-th largest key, read
+// from the 64-bin coarse histogram (key >> 26) and then the 64 fine bins of
+// the coarse bin found, one warp scan each.  Writes ms->dig / gt (keys in
+// larger bins) / bucket.  1 <= r <= the histogram's total.
+__device__ __forceinline__ void warp_find_d0(const uint32_t* hist, const uint32_t* chist, int r, StepMisc* ms) {
+  const int lane = threadIdx.x & 31;
+  int base = 0, above = 0;
+  const uint32_t* h = chist;
+#pragma unroll 1
+  for (int level = 0; level < 2; ++level) {
+    // lane L holds bins 63 - 2L and 62 - 2L of this level (counted from the top)
+    const int ca = (int)h[63 - 2 * lane], cb = (int)h[62 - 2 * lane];
+    const int sum = ca + cb;
+    const int before = above + warp_excl_scan(sum, lane);
+    const bool mine = before < r && r <= before + sum;
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    int bin = 63 - 2 * lane, gt = before, cnt = ca;
+    if (r > before + ca) {
+      bin -= 1;
+      gt += ca;
+      cnt = cb;
+    }
+    bin = __shfl_sync(0xffffffffu, bin, src);
+    gt = __shfl_sync(0xffffffffu, gt, src);
+    cnt = __shfl_sync(0xffffffffu, cnt, src);
+    base = base * 64 + bin;
+    above = gt;
+    if (level == 1 && lane == 0) {
+      ms->dig = base;
+      ms->gt = gt;
+      ms->bucket = cnt;
+    }
+    h = hist + base * 64;
+  }
+}
+
+// The k-th largest value theta of the union of the C received lists
+// (exchange slots of `stride` u64; a slot's header carries its count and the
+// smallest and largest key it listed; values are distinct): exactly k
+// entries are >= theta (the caller guarantees the union holds at least k).
+// One pass bins every entry by its key's offset from the smallest key,
+// shifted to at most 2048 bins (hb); the bin holding the k-th entry is
+// found; a second pass counts each source's entries in higher bins and
+// gathers that bin's entries, which one warp ranks.  A bin of more than 32
+// entries (dense or tied keys) falls back to the radix search.  Stores per
+// source the count of its entries >= theta in ms->sel.  A warp sweeps whole
+// sources.  Every thread calls it.
+__device__ __forceinline__ unsigned long long union_select(const unsigned long long* recv, int stride, int cap,
+                                                           int C, int k, uint32_t* hb, StepMisc* ms) {
+  constexpr int NB = 2048;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // lane r reads source r's header
+  if (lane < C) {
+    const int4 hd = *slot_hdr(recv, stride, lane);
+    if (hd.x > 0) {
+      lo = (uint32_t)hd.z;
+      hi = (uint32_t)hd.w;
+    }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t span = hi - lo;  // keys lie in [lo, hi]
+  const int shift = max(0, (32 - __clz((int)(span | 1u))) - 11);
+  {
+    uint4* z = reinterpret_cast<uint4*>(hb);
+#pragma unroll 1
+    for (int i = tid; i < NB / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) ms->bkt_n = 0;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int r = warp; r < C; r += NW) {
+    const unsigned long long* e = recv + (size_t)r * stride + 2;
+    const int n = min(slot_hdr(recv, stride, r)->x, cap);
+#pragma unroll 1
+    for (int i = lane; i < n; i += 32) atomicAdd(&hb[((uint32_t)(e[i] >> 32) - lo) >> shift], 1u);
+  }
+  __syncthreads();
+  find_digit<NB>(hb, k, ms->scan, &ms->dig);
+  const uint32_t bs = (uint32_t)ms->dig;
+  const int k_rem = k - ms->gt, nbk = ms->bucket;
+  if (nbk > 32) return union_kth(recv, stride, cap, C, k, hb, ms);  // (uniform)
+#pragma unroll 1
+  for (int r = warp; r < C; r += NW) {
+    const unsigned long long* e = recv + (size_t)r * stride + 2;
+    const int n = min(slot_hdr(recv, stride, r)->x, cap);
+    int above = 0;
+#pragma unroll 1
+    for (int i = lane; i < n; i += 32) {
+      const unsigned long long x = e[i];
+      const uint32_t b = ((uint32_t)(x >> 32) - lo) >> shift;
+      above += b > bs;
+      if (b == bs) {
+        const int j = atomicAdd(&ms->bkt_n, 1);
+        ms->bkt[j] = x;
+        ms->bkt_src[j] = r;
+      }
+    }
+    above = warp_sum_i(above);
+    if (lane == 0) ms->sel[r] = above;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long x = lane < nbk ? ms->bkt[lane] : 0ull;  // (lanes >= nbk hold 0: never larger)
+    int rank = 0;  // entries of the bin larger than x
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rank += __shfl_sync(0xffffffffu, x, i) > x;
+    if (lane < nbk) {
+      if (rank == k_rem - 1) ms->theta = x;
+      if (rank < k_rem) atomicAdd(&ms->sel[ms->bkt_src[lane]], 1);
+    }
+  }
+  __syncthreads();
+  return ms->theta;
+}
+
+// ----------------------------------------------------------- rare paths
+// Out of line so that the common path's code stays short (instruction fetch,
+// not arithmetic, bounds most phases of a launch this size).
+
+// A TIP stage wait ran out: report it, and let the copies still in flight
+// land before the staging is reused -- one that does not within one more
+// wait bound (all stages together) is reported, and the staging is left
+// alone.  One thread.
+__device__ __noinline__ void tip_fail_drain(uint64_t* bars, StepMisc* ms, int ns, uint64_t wait_ns, int* status) {
+  atomicOr(status, FASA_DEV_TIMEOUT);
+  bool drained = true;
+  const uint64_t start = global_timer_ns();
+#pragma unroll 1
+  for (int s = 0; s < ns; ++s)
+    if (ms->tip_last[s] >= 0) {
+      const uint64_t spent = global_timer_ns() - start;
+      const uint64_t left = spent < wait_ns ? wait_ns - spent : 1ull;
+      drained &= mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, left);
+    }
+  if (!drained) {
+    atomicOr(status, FASA_DEV_UNDRAINED);
+    ms->big_unsafe = 1;
+  }
+}
+
+// Copies this CTA's nloc workspace scores (scw, written by its own threads)
+// back into shared memory at dst with bulk copies, one share per warp.
+// Returns false when the copy did not land in time.  Every thread calls it.
+__device__ __noinline__ bool reload_scores(const float* scw, int nloc, unsigned char* dst, uint32_t rbar,
+                                           uint64_t wait_ns) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nv = (nloc + 3) >> 2;
+  const int per_w = (nv + NW - 1) / NW;
+  const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
+  fence_proxy_async_global();  // this thread's score stores, before the copy reads them
+  __syncthreads();
+  if (lane == 0) {
+    if (warp == 0) mbar_arrive_expect_tx(rbar, (uint32_t)nv * 16u);
+    if (v1 > v0) bulk_g2s(smem_u32(dst) + v0 * 16, scw + v0 * 4, (uint32_t)(v1 - v0) * 16u, rbar);
+  }
+  return __syncthreads_and(mbar_wait_bounded(rbar, 0u, wait_ns)) != 0;
+}
+
+// F_APPEND, in the CTA that owns the new token: rotate its key (pairs kn,
+// stored dtype) by position t_new, store key and value vn at index t_new of
+// the caches and the key's dominant FCs in K_dom (slot row kdw), and return
+// (thread 0) the token's TIP score computed exactly as the TIP loop scores a
+// streamed token: same FC order and accumulation, stored precision.
+// `scratch` holds D/2 float2.  Every thread calls it.
+template <int D>
+__device__ __noinline__ float append_own_token(const unsigned long long* turns, __nv_bfloat162 kn, __nv_bfloat162 vn,
+                                               int t_new, __nv_bfloat16* Kw, __nv_bfloat16* Vw, __nv_bfloat16* kdw,
+                                               const int* dom, int nfc, const float* qbar, bool score,
+                                               float2* scratch) {
+  using T = __nv_bfloat16;
+  const int tid = threadIdx.x;
+  if (tid < D / 2) {
+    const int i = tid;
+    const float x0 = __low2float(kn), x1 = __high2float(kn);
+    const float2 c = rope_cos_sin(turns[i], t_new);
+    const T r0 = __float2bfloat16_rn(x0 * c.x - x1 * c.y), r1 = __float2bfloat16_rn(x0 * c.y + x1 * c.x);
+    Kw[2 * i] = r0;
+    Kw[2 * i + 1] = r1;
+    Vw[2 * i] = __low2bfloat16(vn);
+    Vw[2 * i + 1] = __high2bfloat16(vn);
+    scratch[i] = make_float2(__bfloat162float(r0), __bfloat162float(r1));
+  }
+  __syncthreads();
+  auto dom_at = [&](int j) { return min(max(dom[j], 0), D / 2 - 1); };
+#pragma unroll 1
+  for (int j = tid; j < nfc; j += NT) {
+    const float2 kp = scratch[dom_at(j)];
+    kdw[(size_t)j * KDOM_BLOCK * 2] = __float2bfloat16_rn(kp.x);
+    kdw[(size_t)j * KDOM_BLOCK * 2 + 1] = __float2bfloat16_rn(kp.y);
+  }
+  float s_new = 0.f;
+  if (tid == 0 && score) {
+    float a0 = 0.f, a1 = 0.f;
+    auto fc_add = [&](int j, float& a) {
+      const float2 kp = scratch[dom_at(j)];
+      a = fmaf(qbar[2 * j], kp.x, fmaf(qbar[2 * j + 1], kp.y, a));
+    };
+    int j = 0;
+    for (; j + 2 <= nfc; j += 2) {
+      fc_add(j, a0);
+      fc_add(j + 1, a1);
+    }
+    if (j < nfc) fc_add(j, a0);
+    s_new = a0 + a1;
+  }
+  __syncthreads();
+  return s_new;
+}
+
+// The second round of the selection: every CTA sends its exact local top-k
+// (their union always holds the unit's top k) and the k-th entry of the
+// union is found again.  The staging that receives the lists must be idle
+// in every CTA first: the gathers still in flight are drained and the
+// cluster synchronises.  Returns theta; ms->sel holds the per-source counts.
+// Every thread of every CTA of the cluster calls it (the decision to run it
+// is taken on the same exchanged data everywhere).
+__device__ __noinline__ unsigned long long second_round(int k_eff, int nloc, int t0, int cap2, const float* scr,
+                                                        uint32_t* hist, unsigned long long* recv2, StepMisc* ms,
+                                                        uint32_t bar_x2, uint32_t crank, int C, uint64_t xwait,
+                                                        int* status) {
+  const int tid = threadIdx.x;
+  cp_async_wait<0>();
+  __syncthreads();
+  cluster_sync();
+  const int stride = cap2 + 2;
+  const SelRule R2 = local_rule(min(k_eff, nloc), cap2, ms->hist_clobbered == 0, scr, nloc, hist, ms);
+  const int n2 = list_rule_any(R2, scr, nloc, t0, recv2 + (size_t)crank * stride + 2, cap2, ms);
+  if (tid == 0) *slot_hdr(recv2, stride, crank) = make_int4(n2, nloc > n2 ? 1 : 0, 0, 0);
+  __syncthreads();
+  push_list(recv2, stride, n2, bar_x2, crank, C);
+  if (!mbar_wait_cluster_bounded(bar_x2, 0u, xwait) && tid == 0) atomicOr(status, FASA_DEV_TIMEOUT);
+  if (tid < C) slot_hdr(recv2, stride, tid)->x = min(max(slot_hdr(recv2, stride, tid)->x, 0), cap2);
+  __syncthreads();
+  const int total = __reduce_add_sync(0xffffffffu, (threadIdx.x & 31) < C ? slot_hdr(recv2, stride, threadIdx.x & 31)->x : 0);
+  return total >= k_eff ? union_kth(recv2, stride, cap2, C, k_eff, hist, ms) : 0ull;
 }
 
 template <int D>
 __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant__ StepParams p) {
   using T = __nv_bfloat16;
   constexpr int ES = 2;
-  constexpr int KB = KDOM_BLOCK;  // k_dom tokens per block
-  constexpr int ROWB = D * ES;    // bytes of one K/V row
-  constexpr int CPR = ROWB / 16;  // 16-byte chunks per row
+  constexpr int KB = KDOM_BLOCK;         // k_dom tokens per block
+  constexpr int ROWB = D * ES;           // bytes of one K/V row
+  constexpr int CPR = ROWB / 16;         // 16-byte chunks per row
   constexpr uint32_t FCB = KB * 2 * ES;  // one FC of one k_dom block
+  constexpr uint32_t GSLOT_B = 2u * GR * ROWB;
   extern __shared__ __align__(1024) unsigned char smem[];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int C = (int)cluster_size();
   const int unit = blockIdx.y;
-  const int b = unit / p.Hkv, h = unit - (unit / p.Hkv) * p.Hkv;
+  const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   const int G = p.G;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
@@ -441,74 +766,86 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   unsigned long long* recv1 = reinterpret_cast<unsigned long long*>(smem + p.off_recv1);
   int* rows = reinterpret_cast<int*>(smem + p.off_rows);
   unsigned char* big = smem + p.off_big;
-  unsigned long long* recv2 = reinterpret_cast<unsigned long long*>(smem + p.off_recv2);
 
   STEP_TRACE(0);
-  // ---------------------------------------------------------------- set-up
   const int nfc_max = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
-  if (tid == 0) {
-    for (int s = 0; s < ns; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    mbar_init(smem_u32(&bars[SB_X1]), (uint32_t)C);
-    mbar_init(smem_u32(&bars[SB_X2]), (uint32_t)C);
-    mbar_init(smem_u32(&bars[SB_COMB]), (uint32_t)C);
-    mbar_init(smem_u32(&bars[SB_RELOAD]), 1);
+  // barriers first: their fence must not wait for the loads below
+  if (warp == 0 && lane < ST_BARS && (lane < ns || lane >= ST_MAX_STAGES)) {
+    // X1 and COMB complete when the C - 1 peers' bulk copies have landed
+    // (their bytes are expected here, with the one local arrival); X2 takes
+    // one arrival per CTA
+    mbar_init(smem_u32(&bars[lane]), lane == SB_X2 ? (uint32_t)C : 1u);
     fence_mbar_init();
-    ms->tip_fail = 0;
-    ms->big_unsafe = 0;
-    ms->hist_clobbered = 0;
-    ms->n_rows = 0;
-    for (int r = 0; r < C_MAX; ++r) ms->sel[r] = 0;
-    for (int s = 0; s < ST_MAX_STAGES; ++s) {
-      ms->tip_done[s] = 0u;
-      ms->tip_last[s] = -1;
+    if (lane == SB_X1) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * (p.cap1 + 2) * 8));
+    if (lane == SB_COMB) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * p.comb_slot));
+  }
+  // small inputs: every load is in flight during the rest of the set-up, and
+  // the query pairs stay in their stored form until used
+  const bool append = (p.flags & F_APPEND) != 0;
+  bool bad = false;
+  int len = p.seq_lens[b];
+  int m_pos = append ? 0 : p.pos[b];
+  const int dom_i = tid < nfc_max ? p.dom_fc[h * nfc_max + tid] : 0;
+  const int dom_hi = (warp == 0 && lane + 32 < nfc_max) ? p.dom_fc[h * nfc_max + lane + 32] : 0;
+  __nv_bfloat162 kn = __float2bfloat162_rn(0.f), vn = kn;
+  if (append && tid < D / 2) {  // (element-aligned inputs: two 2-byte loads each)
+    const T* knp = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D + 2 * tid;
+    const T* vnp = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D + 2 * tid;
+    kn = __halves2bfloat162(knp[0], knp[1]);
+    vn = __halves2bfloat162(vnp[0], vnp[1]);
+  }
+  constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;
+  T qv0[QPAIRS], qv1[QPAIRS];
+#pragma unroll
+  for (int k = 0; k < QPAIRS; ++k) {
+    const int x = tid + k * NT;
+    qv0[k] = qv1[k] = T(0.f);
+    if (x < G * (D / 2)) {
+      const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D + 2 * x;
+      qv0[k] = qg[0];
+      qv1[k] = qg[1];
+    }
+  }
+
+  // ---------------------------------------------------------------- set-up
+  // the RoPE table goes to shared memory (each thread reads its own entry
+  // later; per-thread indices into kernel parameters would serialize)
+  unsigned long long* turns = reinterpret_cast<unsigned long long*>(uh);  // [D/2]
+  if (tid < D / 2) turns[tid] = p.rope_turns[tid];
+  if (warp == 0) {
+    if (lane < ST_MAX_STAGES) {
+      ms->tip_done[lane] = 0u;
+      ms->tip_last[lane] = -1;
+    }
+    if (lane < C_MAX) ms->sel[lane] = 0;
+    ms->chist[lane] = 0u;
+    ms->chist[lane + 32] = 0u;
+    if (lane == 0) {
+      ms->tip_fail = 0;
+      ms->big_unsafe = 0;
+      ms->hist_clobbered = 0;
+      ms->n_rows = 0;
+      ms->list_max = 0u;
     }
   }
   {
     uint4* z = reinterpret_cast<uint4*>(hist);
     for (int i = tid; i < HLOC_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-  // release: the initialised barriers are visible to every peer before its
-  // first remote arrive (the matching wait comes after TIP)
-  cluster_arrive();
+  // The barrier inits were fenced at cluster scope above; the matching wait
+  // (after TIP) comes before any peer touches this CTA's shared memory.  A
+  // relaxed arrive does not wait for this thread's loads still in flight.
+  cluster_arrive_relaxed();
   __syncthreads();
+  STEP_TRACE(12);
 
-  // small inputs, all loads in flight together
-  const bool append = (p.flags & F_APPEND) != 0;
-  bool bad = false;
-  int len = p.seq_lens[b];
-  int m_pos = append ? 0 : p.pos[b];
-  const int dom_i = tid < nfc_max ? p.dom_fc[h * nfc_max + tid] : 0;
   int nfc = nfc_max;
   if (warp == 0) {  // this head's count: the entries before the first negative one
-    const int d1 = lane + 32 < nfc_max ? p.dom_fc[h * nfc_max + lane + 32] : 0;
     const unsigned b0 = __ballot_sync(0xffffffffu, lane < nfc_max && dom_i < 0);
-    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && d1 < 0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && dom_hi < 0);
     nfc = b0 ? __ffs(b0) - 1 : (b1 ? 31 + __ffs(b1) : nfc_max);
     nfc = max(nfc, 1);  // an empty set uses slot 0 (reported below)
     if (lane == 0) ms->nfc = nfc;
-  }
-  // F_APPEND: the new token's key and value pairs (thread i < D/2: pair i),
-  // loaded whichever CTA turns out to own the token
-  T kn0 = T(0.f), kn1 = T(0.f), vn0 = T(0.f), vn1 = T(0.f);
-  if (append && tid < D / 2) {
-    const T* kn = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D;
-    const T* vn = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D;
-    kn0 = kn[2 * tid];
-    kn1 = kn[2 * tid + 1];
-    vn0 = vn[2 * tid];
-    vn1 = vn[2 * tid + 1];
-  }
-  constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;
-  float2 qv[QPAIRS];
-#pragma unroll
-  for (int k = 0; k < QPAIRS; ++k) {
-    const int x = tid + k * NT;
-    qv[k] = make_float2(0.f, 0.f);
-    if (x < G * (D / 2)) {
-      const int g = x / (D / 2), i = x - g * (D / 2);
-      const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G + g) * D + 2 * i;
-      qv[k] = make_float2(to_f32<T>(qg[0]), to_f32<T>(qg[1]));
-    }
   }
   if (len < 0 || len > p.T_max) {
     bad = true;
@@ -546,7 +883,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   const int ntiles = need_select ? (nloc_s + tt - 1) / tt : 0;
   const uint32_t stage_bytes = (uint32_t)(tt / KB) * nfc_max * FCB;
   const T* kd_unit = reinterpret_cast<const T*>(p.k_dom) + (size_t)unit * nfc_max * p.T_max * 2;
-  auto tip_issue = [&](int it) {  // one thread; nfc is this head's count
+  auto tip_issue = [&](int it) {  // one thread per tile; nfc is this head's count
     const int s = it % ns;
     const int tau0 = t0 + it * tt;
     const int nblk = (min(tt, t1s - tau0) + KB - 1) / KB;
@@ -558,6 +895,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       if (nfc == nfc_max) {
         bulk_g2s(smem_u32(big + s * stage_bytes), src, (uint32_t)nblk * blk_bytes, bar);
       } else {
+#pragma unroll 1
         for (int bi = 0; bi < nblk; ++bi)
           bulk_g2s(smem_u32(big + s * stage_bytes + bi * blk_bytes), src + (size_t)bi * nfc_max * KB * 2, blk_bytes,
                    bar);
@@ -565,24 +903,24 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     }
     ms->tip_last[s] = it;
   };
-  if (tid == 0)
-    for (int it = 0; it < min(ns, ntiles); ++it) tip_issue(it);
+  if (warp == 0 && lane < min(ns, ntiles)) tip_issue(lane);  // one stage per lane
+  STEP_TRACE(13);
 
   // ------------------------------------------------------------ query prep
-#pragma unroll
+#pragma unroll 1
   for (int k = 0; k < QPAIRS; ++k) {
     const int x = tid + k * NT;
     if (x < G * (D / 2)) {
-      const int g = x / (D / 2), i = x - g * (D / 2);
-      const float2 c = rope_cos_sin(p.rope_turns[i], m_pos);
-      *reinterpret_cast<float2*>(&qrot[g * D + 2 * i]) =
-          make_float2(qv[k].x * c.x - qv[k].y * c.y, qv[k].x * c.y + qv[k].y * c.x);
+      const int i = x & (D / 2 - 1);
+      const float2 c = rope_cos_sin(turns[i], m_pos);
+      const float x0 = __bfloat162float(qv0[k]), x1 = __bfloat162float(qv1[k]);
+      *reinterpret_cast<float2*>(&qrot[2 * x]) = make_float2(x0 * c.x - x1 * c.y, x0 * c.y + x1 * c.x);
     }
   }
   __syncthreads();
   nfc = ms->nfc;
-  for (int j = tid; j < nfc; j += NT) {
-    int i = (j == tid) ? dom_i : p.dom_fc[h * nfc_max + j];
+  if (tid < nfc) {  // q-bar: the group sum of the rotated query on the dominant FCs
+    int i = dom_i;
     if (i < 0 || i >= D / 2) {
       bad = true;
       i = min(max(i, 0), D / 2 - 1);
@@ -592,55 +930,18 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       a0 += qrot[g * D + 2 * i];
       a1 += qrot[g * D + 2 * i + 1];
     }
-    qbar[2 * j] = a0;
-    qbar[2 * j + 1] = a1;
+    qbar[2 * tid] = a0;
+    qbar[2 * tid + 1] = a1;
   }
   __syncthreads();
-
-  // F_APPEND, in the CTA that owns the new token: rotate its key by its
-  // position, store key and value at index t_new of the cache and the key's
-  // dominant FCs in K_dom, and score it exactly as the TIP loop scores a
-  // streamed token (same FC order and accumulation, stored precision).
   float s_new = 0.f;
-  if (own_new) {
-    float2* knew = reinterpret_cast<float2*>(uh);  // rotated key pairs, as stored (D/2 <= UH_BINS/2)
-    T* Kw = const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D;
-    T* Vw = const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D;
-    if (tid < D / 2) {
-      const int i = tid;
-      const float x0 = to_f32<T>(kn0), x1 = to_f32<T>(kn1);
-      const float2 c = rope_cos_sin(p.rope_turns[i], t_new);
-      const T r0 = from_f32<T>(x0 * c.x - x1 * c.y), r1 = from_f32<T>(x0 * c.y + x1 * c.x);
-      Kw[2 * i] = r0;
-      Kw[2 * i + 1] = r1;
-      Vw[2 * i] = vn0;
-      Vw[2 * i + 1] = vn1;
-      knew[i] = make_float2(to_f32<T>(r0), to_f32<T>(r1));
-    }
-    __syncthreads();
-    T* kdw = const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc_max * KB + (t_new % KB)) * 2;
-    auto dom_at = [&](int j) { return min(max(p.dom_fc[h * nfc_max + j], 0), D / 2 - 1); };
-    for (int j = tid; j < nfc; j += NT) {
-      const float2 kp = knew[dom_at(j)];
-      kdw[(size_t)j * KB * 2] = from_f32<T>(kp.x);
-      kdw[(size_t)j * KB * 2 + 1] = from_f32<T>(kp.y);
-    }
-    if (tid == 0 && need_select) {
-      float a0 = 0.f, a1 = 0.f;
-      auto fc_add = [&](int j, float& a) {
-        const float2 kp = knew[dom_at(j)];
-        a = fmaf(qbar[2 * j], kp.x, fmaf(qbar[2 * j + 1], kp.y, a));
-      };
-      int j = 0;
-      for (; j + 2 <= nfc; j += 2) {
-        fc_add(j, a0);
-        fc_add(j + 1, a1);
-      }
-      if (j < nfc) fc_add(j, a0);
-      s_new = a0 + a1;
-    }
-    __syncthreads();
-  }
+  if (own_new)  // (uh: the RoPE table, then this scratch)
+    s_new = append_own_token<D>(turns, kn, vn, t_new,
+                                const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D,
+                                const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D,
+                                const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc_max * KB + (t_new % KB)) * 2,
+                                p.dom_fc + h * nfc_max, nfc, qbar, need_select,
+                                reinterpret_cast<float2*>(uh) + D / 2);
   STEP_TRACE(1);
 
   // ---------------------------------------------------------------- TIP scan
@@ -651,7 +952,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   float* scw = p.s_cap > 0 ? sc_s : p.scores + (size_t)unit * p.T_max + t0;
   if (own_new && need_select && tid == 0) {  // the appended token's score, as TIP would
     scw[nloc_s] = s_new;
-    atomicAdd(&hist[score_key(s_new) >> 20], 1u);
+    const uint32_t key = score_key(s_new);
+    atomicAdd(&hist[key >> 20], 1u);
+    atomicAdd(&ms->chist[key >> 26], 1u);
   }
   const int upt = tt / TIP_UNIT;
   const int nunits = ntiles > 0 ? (nloc_s + TIP_UNIT - 1) / TIP_UNIT : 0;
@@ -688,7 +991,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      if (tl + t < nloc_s) atomicAdd(&hist[score_key(acc[t]) >> 20], 1u);
+      if (tl + t < nloc_s) {
+        const uint32_t key = score_key(acc[t]);
+        atomicAdd(&hist[key >> 20], 1u);
+        atomicAdd(&ms->chist[key >> 26], 1u);
+      }
     if (ring) {
       // every lane's reads of the stage returned (they fed the FMAs above)
       __syncwarp();
@@ -703,24 +1010,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     }
   }
   if (__syncthreads_or(tip_fail | (nunits > 0 ? ms->tip_fail : 0))) {
-    if (tid == 0) {
-      atomicOr(p.status, 2);
-      // copies still in flight must land before the staging is reused; one
-      // that does not within one more wait bound (for all stages together)
-      // is reported and the staging is left alone
-      bool drained = true;
-      const uint64_t start = global_timer_ns();
-      for (int s = 0; s < ns; ++s)
-        if (ms->tip_last[s] >= 0) {
-          const uint64_t spent = global_timer_ns() - start;
-          const uint64_t left = spent < p.wait_ns ? p.wait_ns - spent : 1ull;
-          drained &= mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, left);
-        }
-      if (!drained) {
-        atomicOr(p.status, 4);
-        ms->big_unsafe = 1;
-      }
-    }
+    if (tid == 0) tip_fail_drain(bars, ms, ns, p.wait_ns, p.status);
     __syncthreads();
   }
   const bool big_ok = ms->big_unsafe == 0;
@@ -737,12 +1027,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   // ---------------------------------------------------------------- top-k
   unsigned long long theta = 0ull;
   int n1 = 0;
-  bool second = false;         // the second exchange decided the selection
-  int sel_before = 0;          // selected tokens of the lower-ranked CTAs
+  bool second = false;  // the second exchange decided the selection
+  int sel_before = 0;   // selected tokens of the lower-ranked CTAs
   const bool spec = p.spec != 0 && big_ok;
   const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * D;
   const T* Vb = reinterpret_cast<const T*>(p.v_cache) + (size_t)unit * p.T_max * D;
-  constexpr uint32_t GSLOT_B = 2u * GR * ROWB;
   // FAC rows: fr_n rows, contiguous tokens fr_r0.. or a list -- the
   // first-round list itself (masked by theta) or the compact own selection
   const unsigned long long* fslot = nullptr;
@@ -753,107 +1042,118 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     if (fslot) return (int)(0xFFFFFFFFu - (uint32_t)fslot[i]);
     return rows[i];
   };
-  // The first fac_wst groups of every warp, issued by the whole CTA (group g
-  // belongs to warp g % NW, slot g / NW).  Rows past fr_n are zero-filled:
-  // the tensor cores multiply them by zero weights, which must not meet
-  // stale NaNs.  Row chunk c sits at chunk position c ^ (row & 7) so the
-  // eight rows an ldmatrix reads fall in distinct banks.
+  // Gathers chunks [c0, c0 + nc) of row i's K then V (CPR chunks each) into
+  // its group's slot: group g belongs to warp g % NW, its slot (g / NW) mod
+  // fac_wst (the slots are reused in turn); chunk c of a row sits at
+  // chunk position c ^ (row & 7) so the eight rows an ldmatrix reads fall in
+  // distinct banks.  Rows past fr_n are zero-filled: the tensor cores
+  // multiply them by zero weights, which must not meet stale NaNs.
+  auto row_chunks = [&](int i, int c0, int nc) {
+    const int g = i / GR, rr = i & (GR - 1);
+    const uint32_t st0 =
+        smem_u32(big) + (uint32_t)((g % NW) * p.fac_wst + (g / NW) % p.fac_wst) * GSLOT_B + rr * ROWB;
+    const bool real = i < fr_n;
+    const size_t off = real ? (size_t)row_token(i) * D : 0;
+#pragma unroll 1
+    for (int c = c0; c < c0 + nc; ++c) {
+      const int which = c >= CPR, ch = c - which * CPR;
+      cp_async16_zfill(st0 + which * GR * ROWB + ((ch ^ (rr & 7)) << 4), (which ? Vb : Kb) + off + ch * (16 / ES),
+                       real ? 16u : 0u);
+    }
+  };
+  // the first fac_wst groups of every warp, issued by the whole CTA: four
+  // threads per row, each a quarter of its chunks
   auto fac_start = [&]() {
     const int nfirst = min((fr_n + GR - 1) / GR * GR, p.fac_wst * NW * GR);
-    for (int c = tid; c < nfirst * 2 * CPR; c += NT) {
-      const int i = c / (2 * CPR), rem = c - i * (2 * CPR);
-      const int which = rem >= CPR, ch = rem - which * CPR;
-      const int g = i / GR, rr = i - g * GR;
-      const uint32_t st0 = smem_u32(big) + (uint32_t)((g % NW) * p.fac_wst + g / NW) * GSLOT_B;
-      const bool real = i < fr_n;
-      const size_t row_off = real ? (size_t)row_token(i) * D : 0;
-      cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
-                       (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
-    }
+#pragma unroll 1
+    for (int i = tid >> 2; i < nfirst; i += NT / 4) row_chunks(i, (tid & 3) * (CPR / 2), CPR / 2);
     cp_async_commit();
   };
 
   if (need_select) {
     // the sweeps read shared memory: scores kept there, or workspace scores
-    // copied back into the idle staging (warp w moves its share)
+    // copied back into the idle staging
     const float* scr = p.s_cap > 0 ? sc_s : scw;
     if (p.reload && big_ok) {
-      const int nv = (nloc + 3) >> 2;
-      const int per_w = (nv + NW - 1) / NW;
-      const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
-      const uint32_t rbar = smem_u32(&bars[SB_RELOAD]);
-      fence_proxy_async_global();  // this thread's score stores, before the copy reads them
-      __syncthreads();
-      if (lane == 0) {
-        if (warp == 0) mbar_arrive_expect_tx(rbar, (uint32_t)nv * 16u);
-        if (v1 > v0) bulk_g2s(smem_u32(big) + v0 * 16, scw + v0 * 4, (uint32_t)(v1 - v0) * 16u, rbar);
-      }
-      if (!mbar_wait_bounded(rbar, 0u, p.wait_ns)) {
-        if (tid == 0) atomicOr(p.status, 2);
-      } else {
-        scr = reinterpret_cast<const float*>(big);
-      }
+      if (reload_scores(scw, nloc, big, smem_u32(&bars[SB_RELOAD]), p.wait_ns)) scr = reinterpret_cast<const float*>(big);
+      else if (tid == 0) atomicOr(p.status, FASA_DEV_TIMEOUT);
     }
-    // first round: the own top-rho list, sent to every CTA
-    const SelRule R1 = local_rule(min(p.rho, nloc), p.cap1, true, scr, nloc, hist, ms);
-    n1 = list_rule(R1, scr, nloc, t0, recv1 + (size_t)crank * p.cap1, p.cap1, ms);
+    // First round: the own top-rho list (or the whole digit-0 bucket at the
+    // threshold when that fits), sent to every CTA
+    const int r1 = min(p.rho, nloc);
+    const int stride1 = p.cap1 + 2;
+    unsigned long long* own1 = recv1 + (size_t)crank * stride1;
+    SelRule R1{0u, INT_MAX};
+    if (r1 < nloc) {
+      if (warp == 0) warp_find_d0(hist, ms->chist, r1, ms);
+      __syncthreads();
+      R1.thr = (uint32_t)ms->dig << 20;
+      if (ms->gt + ms->bucket > p.cap1) R1 = local_rule(r1, p.cap1, true, scr, nloc, hist, ms);
+    }
+    STEP_TRACE(14);
+    n1 = R1.need == INT_MAX ? list_rule_t<false>(R1, scr, nloc, t0, own1 + 2, p.cap1, ms)
+                            : list_rule_any(R1, scr, nloc, t0, own1 + 2, p.cap1, ms);
     STEP_TRACE(3);
     if (spec) {  // gather the listed rows now; the selection only masks them
-      fslot = recv1 + (size_t)crank * p.cap1;
+      fslot = own1 + 2;
       contig = false;
       fr_n = n1;
       fac_start();
     }
-    push_list(recv1, p.cap1, n1, make_int4(n1, nloc > n1 ? 1 : 0, big_ok ? 0 : 1, 0), ms->hdr1,
-              smem_u32(&bars[SB_X1]), crank, C);
-    if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_X1]), 0u, xwait) && tid == 0) atomicOr(p.status, 2);
-    STEP_TRACE(4);
-    if (tid < C) ms->hdr1[tid].x = min(max(ms->hdr1[tid].x, 0), p.cap1);  // (only a timed-out wait leaves stale ones)
+    // the own slot goes to every peer as one bulk copy, completing on the
+    // peer's first-exchange barrier
+    // header: count, cut short, staging unusable, smallest and largest key
+    // listed (every listed key is >= the rule's threshold)
+    if (tid == 0)
+      *slot_hdr(recv1, stride1, crank) =
+          make_int4(n1, (nloc > n1 ? 1 : 0) | (big_ok ? 0 : 2), (int)R1.thr, (int)ms->list_max);
+    fence_proxy_async();  // the slot's generic writes, before the async proxy reads them
     __syncthreads();
-    int total = 0;
-    bool any_unsafe = false;
-    for (int r = 0; r < C; ++r) {
-      total += ms->hdr1[r].x;
-      any_unsafe |= ms->hdr1[r].z != 0;
-    }
+    if (warp == 0 && lane < C && lane != (int)crank)
+      bulk_s2cluster(dsmem_map(smem_u32(own1), (uint32_t)lane), smem_u32(own1), (uint32_t)stride1 * 8u,
+                     dsmem_map(smem_u32(&bars[SB_X1]), (uint32_t)lane));
+    if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_X1]), 0u, xwait) && tid == 0) atomicOr(p.status, FASA_DEV_TIMEOUT);
+    STEP_TRACE(4);
+    // (only a timed-out wait leaves a stale count; the own slot may still be
+    // read by the outgoing copies and is left alone)
+    if (tid < C && tid != (int)crank)
+      slot_hdr(recv1, stride1, tid)->x = min(max(slot_hdr(recv1, stride1, tid)->x, 0), p.cap1);
+    __syncthreads();
+    STEP_TRACE(30);
+    // lane r reads source r's header (every warp, so the result is everywhere)
+    const int4 hd = lane < C ? *slot_hdr(recv1, stride1, lane) : make_int4(0, 0, 0, 0);
+    const int total = __reduce_add_sync(0xffffffffu, hd.x);
+    const bool any_unsafe = __any_sync(0xffffffffu, (hd.y & 2) != 0);
     bool valid = total >= k_eff;
     if (valid) {
-      theta = union_kth(recv1, ms->hdr1, p.cap1, C, k_eff, uh, ms);
-      for (int r = 0; r < C; ++r) {
-        const int4 hd = ms->hdr1[r];
-        if (hd.y && hd.x < k_eff && ms->sel[r] == hd.x) valid = false;
-      }
+      theta = union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms);
+      if (tid == 0) ms->hist_clobbered = 1;
+      // a source that cut its list short (and sent fewer than k) with every
+      // entry selected could have left out a selected token
+      const int selr = lane < C ? ms->sel[lane] : 0;
+      valid = !__any_sync(0xffffffffu, (hd.y & 1) && hd.x < k_eff && selr == hd.x);
     }
     STEP_TRACE(5);
     if (!valid && !any_unsafe) {
-      // Second round: every CTA sends its exact local top-k.  The staging
-      // that receives them must be idle in every CTA first.
       second = true;
-      cp_async_wait<0>();
-      __syncthreads();
-      cluster_sync();
-      const float* scr2 = p.s_cap > 0 ? sc_s : scw;
-      const SelRule R2 = local_rule(min(k_eff, nloc), p.cap2, ms->hist_clobbered == 0, scr2, nloc, hist, ms);
-      const int n2 = list_rule(R2, scr2, nloc, t0, recv2 + (size_t)crank * p.cap2, p.cap2, ms);
-      push_list(recv2, p.cap2, n2, make_int4(n2, nloc > n2 ? 1 : 0, 0, 0), ms->hdr2, smem_u32(&bars[SB_X2]),
-                crank, C);
-      if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_X2]), 0u, xwait) && tid == 0) atomicOr(p.status, 2);
-      if (tid < C) ms->hdr2[tid].x = min(max(ms->hdr2[tid].x, 0), p.cap2);
-      __syncthreads();
-      int total2 = 0;
-      for (int r = 0; r < C; ++r) total2 += ms->hdr2[r].x;
-      if (total2 >= k_eff) theta = union_kth(recv2, ms->hdr2, p.cap2, C, k_eff, uh, ms);
+      theta = second_round(k_eff, nloc, t0, p.cap2, p.s_cap > 0 ? sc_s : scw, hist,
+                           reinterpret_cast<unsigned long long*>(smem + p.off_recv2), ms, smem_u32(&bars[SB_X2]),
+                           crank, C, xwait, p.status);
       STEP_TRACE(6);
     }
-    for (int r = 0; r < (int)crank; ++r) sel_before += ms->sel[r];
-    // the own selection, compact and in token order (the own list is in
-    // token order): warp w takes a contiguous share of the list
-    {
-      const unsigned long long* own = second ? recv2 + (size_t)crank * p.cap2 : recv1 + (size_t)crank * p.cap1;
-      const int n_own = second ? ms->hdr2[crank].x : n1;
+    sel_before = __reduce_add_sync(0xffffffffu, lane < (int)crank ? ms->sel[lane] : 0);
+    // The own selection, compact and in token order (the own list is in
+    // token order), for the gather when the first round's rows were not
+    // gathered already and for the index output: warp w takes a contiguous
+    // share of the list.
+    if (!spec || second || p.idx_out) {
+      const unsigned long long* recv2 = reinterpret_cast<const unsigned long long*>(smem + p.off_recv2);
+      const unsigned long long* own = second ? recv2 + (size_t)crank * (p.cap2 + 2) + 2 : own1 + 2;
+      const int n_own = second ? slot_hdr(recv2, p.cap2 + 2, crank)->x : n1;
       const int per_w = (n_own + NW - 1) / NW;
       const int e0 = min(n_own, warp * per_w), e1 = min(n_own, e0 + per_w);
       int c = 0;
+#pragma unroll 1
       for (int e = e0 + lane; e < e1; e += 32) c += own[e] >= theta;
       c = warp_sum_i(c);
       if (lane == 0) ms->scan2[warp] = c;
@@ -863,12 +1163,13 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
         at += w < warp ? ms->scan2[w] : 0;
         n_sel += ms->scan2[w];
       }
+#pragma unroll 1
       for (int e0b = e0; e0b < e1; e0b += 32) {
         const int e = e0b + lane;
-        const bool s = e < e1 && own[e] >= theta;
-        const unsigned bal = __ballot_sync(0xffffffffu, s);
+        const bool sl = e < e1 && own[e] >= theta;
+        const unsigned bal = __ballot_sync(0xffffffffu, sl);
         const int pos = at + __popc(bal & ((1u << lane) - 1u));
-        if (s && pos < p.rows_cap) rows[pos] = (int)(0xFFFFFFFFu - (uint32_t)own[e]);
+        if (sl && pos < p.rows_cap) rows[pos] = (int)(0xFFFFFFFFu - (uint32_t)own[e]);
         at += __popc(bal);
       }
       if (tid == 0) ms->n_rows = min(n_sel, p.rows_cap);
@@ -900,12 +1201,14 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   // heads per MMA).  q and the softmax weights P are split into bf16 hi + lo
   // parts, so the products keep ~16 mantissa bits.  Lane (gq, tq) holds rows
   // gq, gq + 8 of S^T and head dims gq, gq + 8 of O^T, heads 2tq, 2tq + 1.
-  constexpr int PSTRIDE = D + 4;
   constexpr int KS = D / 16;
-  float* rec = reinterpret_cast<float*>(big);                         // [G][NW][D + 2]
-  float* part = rec + G_MAX * NW * (D + 2);                           // [G][D + 4]
-  float* wts = part + G_MAX * PSTRIDE;                                // [G][NW] + [G]
-  {
+  const int ngrp = (fr_n + GR - 1) / GR;
+  const int nrec = min(NW, ngrp);  // warps that attend rows
+  float* rec = reinterpret_cast<float*>(big);  // [G][NW][D + 2]
+  float* wts = rec + G_MAX * NW * (D + 2);     // [G][NW] + [G]
+  cp_async_wait<0>();  // the CTA-wide first groups
+  __syncthreads();
+  if (warp < nrec) {
     const float qs = 1.4426950408889634f * rsqrtf((float)D);
     const int gq = lane >> 2, tq = lane & 3;
     uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo]
@@ -929,24 +1232,6 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     const uint32_t k_row = kr * ROWB, v_row = vr * ROWB;
     const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
     const int wst = p.fac_wst;
-    const int ngrp = (fr_n + GR - 1) / GR;
-    auto grp_issue = [&](int g, int s) {
-      if (g * GR < fr_n) {
-        const uint32_t st0 = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
-        for (int c = lane; c < GR * 2 * CPR; c += 32) {
-          const int rr = c / (2 * CPR), rem = c - rr * (2 * CPR);
-          const int which = rem >= CPR, ch = rem - which * CPR;
-          const int i = g * GR + rr;
-          const bool real = i < fr_n;
-          const size_t row_off = real ? (size_t)row_token(i) * D : 0;
-          cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
-                           (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
-        }
-      }
-      cp_async_commit();
-    };
-    cp_async_wait<0>();  // the CTA-wide first groups
-    __syncthreads();
     int it = 0;
     for (int g = warp; g < ngrp; g += NW, ++it) {
       const int s = wst == 2 ? (it & 1) : 0;
@@ -978,12 +1263,12 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       }
       const float n0 = fmaxf(m0, x0), n1m = fmaxf(m1, x1);
       // every row so far may be masked: then nothing is rescaled or added
-      const float c0 = n0 == -CUDART_INF_F ? 1.f : exp2f(m0 - n0);
-      const float c1 = n1m == -CUDART_INF_F ? 1.f : exp2f(m1 - n1m);
-      const float p0 = n0 == -CUDART_INF_F ? 0.f : exp2f(s0 - n0);
-      const float p2 = n0 == -CUDART_INF_F ? 0.f : exp2f(s2 - n0);
-      const float p1 = n1m == -CUDART_INF_F ? 0.f : exp2f(s1 - n1m);
-      const float p3 = n1m == -CUDART_INF_F ? 0.f : exp2f(s3 - n1m);
+      const float c0 = n0 == -CUDART_INF_F ? 1.f : ex2_approx(m0 - n0);
+      const float c1 = n1m == -CUDART_INF_F ? 1.f : ex2_approx(m1 - n1m);
+      const float p0 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s0 - n0);
+      const float p2 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s2 - n0);
+      const float p1 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s1 - n1m);
+      const float p3 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s3 - n1m);
       l0 = l0 * c0 + p0 + p2;
       l1 = l1 * c1 + p1 + p3;
       m0 = n0;
@@ -1015,7 +1300,12 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
         mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
       }
       __syncwarp();  // the slot and the P tile are free again
-      grp_issue(g + wst * NW, s);  // commits a group even when empty: the waits count groups
+      // the warp's next group after the ones in flight: two lanes per row,
+      // each half of its chunks (commits a group even when empty: the waits
+      // count groups)
+      const int gn = g + wst * NW;
+      if (gn < ngrp) row_chunks(gn * GR + (lane >> 1), (lane & 1) * CPR, CPR);
+      cp_async_commit();
     }
     cp_async_wait<0>();
 #pragma unroll
@@ -1023,8 +1313,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    __syncthreads();  // every warp is done with its slots: `big` takes the warp records
-    STEP_TRACE(8);
+    __syncwarp();
+    // the warp's record, once every warp is done with its slots
+    asm volatile("bar.sync 1, %0;" ::"r"(nrec * 32) : "memory");
     if (big_ok) {
       const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll
@@ -1050,88 +1341,97 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
         }
       }
     }
-    __syncthreads();
   }
-  // merge the warps' records per head into this CTA's record part[g] =
-  // (o[0..D), m, l): the head's maximum and the warp weights exp2(m_w - M)
-  // once, then one multiply-add per warp and element
-  if (big_ok) {
-    if (tid < G) {
-      const int g = tid;
-      float M = -CUDART_INF_F;
-      for (int r = 0; r < NW; ++r) M = fmaxf(M, rec[(g * NW + r) * (D + 2) + D]);
-      for (int r = 0; r < NW; ++r) {
-        const float m_r = rec[(g * NW + r) * (D + 2) + D];
-        wts[g * NW + r] = m_r != -CUDART_INF_F ? exp2f(m_r - M) : 0.f;
-      }
-      wts[G * NW + g] = M;
+  __syncthreads();
+  STEP_TRACE(8);
+  // ---------------------------------------------------------------- combine
+  // The G*D outputs are cut into C slices of sl float4 groups (the last one
+  // shorter).  The records of the warps that attended rows are merged per
+  // head -- the head's maximum and the warp weights exp2(m_w - M) once, then
+  // one multiply-add per warp and element; no rows: m = -inf, l = 0 -- and
+  // written straight into the combine slots: slice r with (m, l) of every
+  // head goes to slot r of the staging (CTA r's share; this CTA's own share
+  // into its receive slot), each slot then one bulk copy to CTA r, which
+  // finishes slice r.
+  const int ngrp4 = G * (D / 4);
+  const int sl = (ngrp4 + C - 1) / C;
+  const int cs = p.comb_slot;  // bytes: sl float4, then G (m, l) float2 (padded)
+  const float inv_sl = 1.f / (float)sl;
+  unsigned char* crcv = smem + p.off_comb;      // [C][cs], slot r from CTA r
+  unsigned char* csnd = smem + p.off_comb_snd;  // [C][cs], slot r for CTA r
+  if (big_ok && tid < G) {
+    const int g = tid;
+    float M = -CUDART_INF_F;
+#pragma unroll 1
+    for (int r = 0; r < nrec; ++r) M = fmaxf(M, rec[(g * NW + r) * (D + 2) + D]);
+#pragma unroll 1
+    for (int r = 0; r < nrec; ++r) {
+      const float m_r = rec[(g * NW + r) * (D + 2) + D];
+      wts[g * NW + r] = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
     }
-    __syncthreads();
-    for (int x = tid; x < G * (D + 2); x += NT) {
-      const int g = x / (D + 2), e = x - g * (D + 2);
-      float val = wts[G * NW + g];
+    wts[G * NW + g] = M;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int x = tid; x < G * (D + 2); x += NT) {
+    const int g = x / (D + 2), e = x - g * (D + 2);
+    float val = e == D ? -CUDART_INF_F : 0.f;
+    if (big_ok) {
+      val = wts[G * NW + g];
       if (e != D) {
         float acc = 0.f;
-        for (int r = 0; r < NW; ++r) {
+#pragma unroll 1
+        for (int r = 0; r < nrec; ++r) {
           const float w = wts[g * NW + r];
           if (w != 0.f) acc += w * rec[(g * NW + r) * (D + 2) + e];
         }
         val = acc;
       }
-      part[g * PSTRIDE + e] = val;
     }
-    __syncthreads();
+    if (e < D) {
+      const int q = g * (D / 4) + (e >> 2);
+      const int r = __float2int_rz(((float)q + 0.5f) * inv_sl);  // q / sl, exact for these sizes
+      unsigned char* dst = (r == (int)crank ? crcv : csnd) + r * cs;
+      *reinterpret_cast<float*>(dst + (q - r * sl) * 16 + (e & 3) * 4) = val;
+    } else {
+#pragma unroll 1
+      for (int r = 0; r < C; ++r)
+        *reinterpret_cast<float*>((r == (int)crank ? crcv : csnd) + r * cs + sl * 16 + g * 8 + (e - D) * 4) = val;
+    }
   }
-
-  // ---------------------------------------------------------------- combine
-  // Each CTA cuts its record into the C output slices (runs of 4-element
-  // groups of the G*D outputs) and stores each slice, with (m, l) of every
-  // head, into the shared memory of the CTA that finishes it, then arrives on
-  // that CTA's barrier.
-  const int ngrp4 = G * (D / 4);
-  const int sl = (ngrp4 + C - 1) / C;
-  float4* recv_o = reinterpret_cast<float4*>(smem + p.off_comb);  // [C][sl]
-  float2* recv_ml = reinterpret_cast<float2*>(recv_o + C * sl);    // [C][G]
-  const uint32_t recv_o_l = smem_u32(recv_o), recv_ml_l = smem_u32(recv_ml);
-  for (int q = tid; q < ngrp4; q += NT) {
-    const int r = ((q + 1) * C - 1) / ngrp4;  // the CTA whose slice holds group q
-    const int q0r = (ngrp4 * r) / C;
-    const int g = q / (D / 4), e4 = q - g * (D / 4);
-    const float4 v = big_ok ? *reinterpret_cast<const float4*>(part + g * PSTRIDE + e4 * 4)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    dsmem_st_v4f(dsmem_map(recv_o_l + ((int)crank * sl + q - q0r) * 16, (uint32_t)r), v.x, v.y, v.z, v.w);
-  }
-  for (int x = tid; x < C * G; x += NT) {
-    const int r = x / G, g = x - r * G;
-    const float mm = big_ok ? part[g * PSTRIDE + D] : -CUDART_INF_F;
-    const float ll = big_ok ? part[g * PSTRIDE + D + 1] : 0.f;
-    dsmem_st_v2f(dsmem_map(recv_ml_l + ((int)crank * G + g) * 8, (uint32_t)r), mm, ll);
-  }
+  fence_proxy_async();  // the staging's generic writes, before the async proxy reads them
   __syncthreads();
-  if (tid < C) mbar_arrive_remote(dsmem_map(smem_u32(&bars[SB_COMB]), (uint32_t)tid));
-  // first half of the final cluster barrier: this CTA touches no peer's
-  // shared memory after this point
-  cluster_arrive();
-  STEP_TRACE(9);
-  if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_COMB]), 0u, xwait) && tid == 0) atomicOr(p.status, 2);
+  STEP_TRACE(28);
+  if (warp == 0 && lane < C && lane != (int)crank)
+    bulk_s2cluster(dsmem_map(smem_u32(crcv + crank * cs), (uint32_t)lane), smem_u32(csnd + lane * cs), (uint32_t)cs,
+                   dsmem_map(smem_u32(&bars[SB_COMB]), (uint32_t)lane));
+  STEP_TRACE(29);
+  if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_COMB]), 0u, xwait) && tid == 0) atomicOr(p.status, FASA_DEV_TIMEOUT);
   STEP_TRACE(10);
+  // First half of the final cluster barrier, once every copy into this CTA
+  // has landed: when the barrier completes, every CTA's outgoing copies have
+  // finished reading its shared memory, and no peer touches it any more.
+  cluster_arrive_relaxed();
+  STEP_TRACE(9);
 
   // Finish this CTA's slice: lpg lanes per output group (the power of two
   // >= C), lane r taking CTA r's record, reduced with width-lpg shuffles.
-  const int q0 = (ngrp4 * (int)crank) / C, q1 = (ngrp4 * ((int)crank + 1)) / C;
+  const int q0 = min(ngrp4, (int)crank * sl), q1 = min(ngrp4, q0 + sl);
   const int lpg = C <= 1 ? 1 : 1 << (32 - __clz(C - 1));
   const int gpw = 32 / lpg;
+#pragma unroll 1
   for (int qw = q0 + gpw * warp; qw < q1; qw += gpw * NW) {  // warp-uniform bound
     const int q = qw + lane / lpg, r = lane & (lpg - 1);
     const bool okq = q < q1 && r < C;
     const int g = okq ? q / (D / 4) : 0, e4 = okq ? q - g * (D / 4) : 0;
-    const float2 ml = okq ? recv_ml[r * G + g] : make_float2(-CUDART_INF_F, 0.f);
+    const float2 ml =
+        okq ? *reinterpret_cast<const float2*>(crcv + r * cs + sl * 16 + g * 8) : make_float2(-CUDART_INF_F, 0.f);
     float M = ml.x;
     for (int o = lpg >> 1; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, lpg));
-    const float w = (ml.x != -CUDART_INF_F) ? exp2f(ml.x - M) : 0.f;
+    const float w = (ml.x != -CUDART_INF_F) ? ex2_approx(ml.x - M) : 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (w != 0.f) {
-      const float4 v = recv_o[r * sl + q - q0];
+      const float4 v = *reinterpret_cast<const float4*>(crcv + r * cs + (q - q0) * 16);
       acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
     }
     float L = w * ml.y;
@@ -1160,15 +1460,17 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     int* io = p.idx_out + (size_t)unit * p.budget;
     if (!need_select) {
       if (crank == 0)
+#pragma unroll 1
         for (int i = tid; i < p.budget; i += NT) io[i] = i < k_eff ? i : -1;
     } else {
-      const int n_own = ms->n_rows;
+      const int n_own = ms->n_rows;  // in token order
+#pragma unroll 1
       for (int i = tid; i < n_own; i += NT)
         if (sel_before + i < p.budget) io[sel_before + i] = rows[i];
     }
   }
   if (p.count_out && crank == 0 && tid == 0) p.count_out[unit] = k_eff;
-  if (bad) atomicOr(p.status, 1);
+  if (bad) atomicOr(p.status, FASA_DEV_BAD_INPUT);
   STEP_TRACE(11);
   cluster_wait();
 }

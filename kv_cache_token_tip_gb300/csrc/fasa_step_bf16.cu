@@ -68,6 +68,14 @@ cudaError_t launch_step_bf16(const StepParams& p, int head_dim, int C, cudaStrea
   return cudaErrorInvalidValue;
 }
 
+#ifdef FASA_PHASE_TRACE
+// Tracing builds: where the step kernel stores its phase timestamps.
+extern "C" int fasa_debug_set_trace(void* buf) {
+  unsigned long long* p = reinterpret_cast<unsigned long long*>(buf);
+  return (int)cudaMemcpyToSymbol(g_step_trace, &p, sizeof(p));
+}
+#endif
+
 int max_active_clusters_step_bf16(int head_dim, int C, int smem_bytes) {
   if (head_dim == 128) return max_clusters_d<128>(C, smem_bytes);
   if (head_dim == 64) return max_clusters_d<64>(C, smem_bytes);
