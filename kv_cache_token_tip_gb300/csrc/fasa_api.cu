@@ -36,6 +36,7 @@ int cuda_fail(cudaError_t e) {
 
 constexpr int SMEM_LIMIT = 232448;  // 227 KB per CTA
 constexpr int S_CAP_MAX = 8192;     // scores per CTA kept in shared memory
+constexpr int STEP_MIN_C = 8;       // smallest cluster the single-exchange step kernel serves
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -333,7 +334,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   const double e = (double)k / C;
   int rho = C == 1 ? k : (int)ceil(e + 4.0 * sqrt(e) + 4.0);
   rho = std::max(1, std::min(rho, chunkT));
-  const int cap1 = align_up(rho + std::max(32, rho / 4), 16);
+  const int cap1 = align_up(rho + std::max(64, rho / 4), 16);
   const int cap2 = C == 1 ? 0 : align_up(k + std::max(32, k / 8), 16);
   const int s_cap = chunkT <= S_CAP_MAX ? chunkT : 0;
   const int rows_cap = std::min(k, std::max(cap1, cap2));
@@ -369,15 +370,16 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   if (room <= 0) return FASA_ERR_UNSUPPORTED;
   // after TIP: FAC slots (then the P tiles), the second-round slots (written
   // only once every CTA drained its gathers), the warp records
-  auto fac_slots = [&](int wst) { return wst * NW * 2 * GR * D * ES; };
-  const int pt_bytes = NW * G_MAX * PTS * 4;
-  const int rec_bytes = (G_MAX * NW * (D + 2) + G_MAX * NW + G_MAX) * 4;
+  auto fac_slots = [&](int wst) { return wst * FNW * 2 * GR * D * ES; };
+  const int pt_bytes = FNW * G_MAX * PTS * 4;
+  const int rec_bytes = (G_MAX * FNW * (D + 2) + G_MAX * FNW + G_MAX) * 4;
   const int recv2_bytes = C == 1 ? 0 : C * (cap2 + 2) * 8;
   // TIP staging: the whole range at once (no refill) with the smallest tile
   // that needs at most ST_MAX_STAGES stages, else a ring of at least two
   // stages holding up to 128 KB.  Warp w scores the 128-token units w,
-  // w + NW, ...; in a ring, stages x (units per tile) must be a multiple of
-  // NW so that every warp meets the same stages in every round of ns tiles
+  // w + W, ...; in a ring, stages x (units per tile) must be a multiple of
+  // the W scoring warps so that every warp meets the same stages in every
+  // round of ns tiles
   // and so waits on each of their phases in order (a parity wait on a
   // barrier two phases behind would pass at once).
   const int fc_tok = nfc * 2 * ES;  // bytes per token over all planes
@@ -389,17 +391,21 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
       stages = st;
     }
   }
-  for (int t = 1024; t >= TIP_UNIT && !tile; t /= 2) {
-    const int step = std::max(1, NW / (t / TIP_UNIT));  // stage counts that keep the rounds aligned
-    int best = 0;
-    for (int st = std::max(2, step); st <= ST_MAX_STAGES; st += step) {
-      if (st % step != 0) continue;
-      if (st * t * fc_tok > std::min(room, std::max(131072, 2 * t * fc_tok))) break;
-      best = st;
-    }
-    if (best) {
-      tile = t;
-      stages = best;
+  int tip_warps = SNW;
+  for (int tw = SNW; tw >= FNW && !tile; tw /= 2) {  // fewer scoring warps when no ring aligns for all
+    for (int t = 1024; t >= TIP_UNIT && !tile; t /= 2) {
+      const int step = std::max(1, tw / (t / TIP_UNIT));  // stage counts that keep the rounds aligned
+      int best = 0;
+      for (int st = std::max(2, step); st <= ST_MAX_STAGES; st += step) {
+        if (st % step != 0) continue;
+        if (st * t * fc_tok > std::min(room, std::max(131072, 2 * t * fc_tok))) break;
+        best = st;
+      }
+      if (best) {
+        tile = t;
+        stages = best;
+        tip_warps = tw;
+      }
     }
   }
   if (!tile) return FASA_ERR_UNSUPPORTED;
@@ -410,7 +416,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   for (int w = 2; w >= 1 && !wst; --w)
     if (fac_slots(w) + pt_bytes <= room) wst = w;
   if (!wst) return FASA_ERR_UNSUPPORTED;
-  const int spec = (C > 1 && cap1 <= wst * NW * GR) ? 1 : 0;
+  const int spec = (C > 1 && cap1 <= wst * FNW * GR) ? 1 : 0;
   const int reload = (s_cap == 0 && !spec && chunkT * 4 <= room) ? 1 : 0;
   int big = std::max(tip_bytes, fac_slots(wst) + pt_bytes);
   big = std::max(big, std::max(rec_bytes, recv2_bytes));
@@ -419,6 +425,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.s_cap = s_cap;
   p.tip_tile = tile;
   p.tip_stages = stages;
+  p.tip_warps = tip_warps;
   p.rho = rho;
   p.cap1 = cap1;
   p.cap2 = cap2;
@@ -454,9 +461,12 @@ void fill_step(StepParams& p, const fasa_dims_t* d, int32_t budget) {
 bool step_kernel_applies(const fasa_dims_t* d) { return d->dtype == FASA_BF16; }
 
 // Plans (and launches) the step kernel.  Cluster size: the override, else
-// the largest C <= 16 for which every unit's cluster is resident at once,
-// else (several waves) the smallest C that launches.  FASA_ERR_UNSUPPORTED:
-// no plan; the caller then uses the general cluster kernel.
+// the largest C <= 16 for which every unit's cluster is resident at once.
+// The kernel serves plans of at least STEP_MIN_C CTAs per unit -- few units
+// at small batch, where the step is one latency-bound chain; with fewer,
+// larger CTAs (batched or multi-wave shapes) each CTA's lists and row
+// gathers are long and the general cluster kernel is faster.
+// FASA_ERR_UNSUPPORTED: no plan here; the caller then uses the cluster kernel.
 int step_plan_and_launch(StepParams& p, const fasa_dims_t* d, void* ws, size_t ws_bytes, bool launch,
                          size_t* ws_need, int* C_out, cudaStream_t stream) {
   DevInfo di;
@@ -480,17 +490,14 @@ int step_plan_and_launch(StepParams& p, const fasa_dims_t* d, void* ws, size_t w
     return n;
   };
   if (d->reserved > 0) {
+    if (d->reserved < STEP_MIN_C) return FASA_ERR_UNSUPPORTED;
     if (plan_step(p, d, d->reserved, &need, di.smem_optin) != FASA_OK) return FASA_ERR_UNSUPPORTED;
     if (capacity(d->reserved) < 1) return FASA_ERR_UNSUPPORTED;
     C = d->reserved;
   } else {
-    for (int c = C_MAX; c >= 1 && !C; --c) {
+    for (int c = C_MAX; c >= STEP_MIN_C && !C; --c) {
       if (plan_step(p, d, c, &need, di.smem_optin) != FASA_OK) continue;
       if (capacity(c) >= units) C = c;
-    }
-    for (int c = 1; c <= 4 && !C; ++c) {
-      if (plan_step(p, d, c, &need, di.smem_optin) != FASA_OK) continue;
-      if (capacity(c) >= 1) C = c;
     }
     if (!C) return FASA_ERR_UNSUPPORTED;
     if (plan_step(p, d, C, &need, di.smem_optin) != FASA_OK) return FASA_ERR_UNSUPPORTED;

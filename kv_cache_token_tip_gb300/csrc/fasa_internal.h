@@ -71,6 +71,9 @@ struct Params {
 };
 
 // The bf16 fused-step kernel (fasa_step.cuh): its plan and arguments.
+constexpr int SNT = 512;           // threads of a step CTA
+constexpr int SNW = SNT / 32;      // its warps
+constexpr int FNW = 8;             // warps that attend rows (one 16-row group slot set each)
 constexpr int ST_MAX_STAGES = 12;  // TIP stage mbarriers [0, 12)
 constexpr int ST_BARS = 16;        // + two selection exchanges, the combine, the score reload
 constexpr int ST_MISC_BYTES = 1024;
@@ -101,6 +104,7 @@ struct StepParams {
   int s_cap;       // scores per CTA kept in shared memory (0: workspace)
   int tip_tile;    // tokens per TIP stage (multiple of TIP_UNIT)
   int tip_stages;  // TIP ring depth (>= the CTA's tiles: no refill)
+  int tip_warps;   // warps that score TIP units (SNW, or 8 for some rings)
   int rho;         // first-round list length per CTA
   int cap1, cap2;  // receive slots per source CTA, first and second round
   int spec;        // gather the first-round list before the selection is final

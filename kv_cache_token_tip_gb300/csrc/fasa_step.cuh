@@ -51,8 +51,8 @@ constexpr int SB_RELOAD = 15;      // score reload from the workspace
 
 struct StepMisc {
   int dig, gt, bucket, pad0;  // radix digit search result
-  int scan[NW];
-  int scan2[NW];
+  int scan[SNW];
+  int scan2[SNW];
   int tip_fail;
   int big_unsafe;       // a TIP copy did not land in time: shared staging is not reused
   int nfc;              // this head's dominant-FC count
@@ -85,7 +85,7 @@ __device__ unsigned long long* g_step_trace;
   do {                                                                                                \
     if ((threadIdx.x & 31) == 0 && g_step_trace) {                                                    \
       unsigned long long* tr_ =                                                                       \
-          g_step_trace + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * NW + (threadIdx.x >> 5)) * 64; \
+          g_step_trace + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * SNW + (threadIdx.x >> 5)) * 64; \
       tr_[(i)] = global_timer_ns();                                                                   \
       tr_[32 + (i)] = clock64();                                                                      \
     }                                                                                                 \
@@ -117,24 +117,53 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
   return incl - v;
 }
 
+// Exclusive prefix sum over the SNT threads of the CTA (thread order); every
+// thread calls it.  `scratch` holds SNW ints.
+__device__ __forceinline__ int block_scan_s(int x, int* scratch, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < SNW; ++w) {
+    const int s = scratch[w];
+    before += (w < warp) ? s : 0;
+    tot += s;
+  }
+  __syncthreads();
+  total = tot;
+  return before + incl - x;
+}
+
 // Finds the digit holding the k_rem-th largest key in a histogram of NB bins
 // (bins counted from the top).  out[0] = digit, out[1] = keys in larger
 // digits, out[2] = keys in the digit.  Every thread must call it.
 template <int NB>
 __device__ __forceinline__ void find_digit(const uint32_t* hist, int k_rem, int* scan, int* out) {
-  constexpr int M = NB / NT;
-  static_assert(M >= 4 && NB % NT == 0 && M % 4 == 0, "bins per thread");
+  constexpr int M = NB / SNT;
+  static_assert(M >= 1 && NB % SNT == 0, "bins per thread");
   const int tid = threadIdx.x;
   const int base = NB - (tid + 1) * M;
-  const uint4* h4 = reinterpret_cast<const uint4*>(hist + base);
   int tsum = 0;
+  if constexpr (M % 4 == 0) {
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist + base);
 #pragma unroll 1
-  for (int q = 0; q < M / 4; ++q) {
-    const uint4 v = h4[q];
-    tsum += (int)(v.x + v.y + v.z + v.w);
+    for (int q = 0; q < M / 4; ++q) {
+      const uint4 v = h4[q];
+      tsum += (int)(v.x + v.y + v.z + v.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < M; ++i) tsum += (int)hist[base + i];
   }
   int total;
-  int run = block_excl_scan(tsum, scan, total);
+  int run = block_scan_s(tsum, scan, total);
   if (run < k_rem && k_rem <= run + tsum) {  // the digit is among this thread's bins
 #pragma unroll 1
     for (int i = M - 1; i >= 0; --i) {
@@ -214,10 +243,10 @@ __device__ __noinline__ SelRule local_rule(int r, int cap, bool hist_ok, const f
   if (!hist_ok) {
     uint4* z = reinterpret_cast<uint4*>(hist);
 #pragma unroll 1
-    for (int i = tid; i < HLOC_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < HLOC_BINS / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 #pragma unroll 1
-    for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
+    for (int tl = tid * 4; tl < nloc; tl += SNT * 4) {
       uint32_t key[4];
       bool ok[4];
       keys4(scr, tl, nloc, key, ok);
@@ -239,10 +268,10 @@ __device__ __noinline__ SelRule local_rule(int r, int cap, bool hist_ok, const f
   for (int dg = 1; dg <= 2; ++dg) {
     const int shift = dg == 1 ? 10 : 0;
 #pragma unroll 1
-    for (int i = tid; i < 1024; i += NT) hist[i] = 0u;
+    for (int i = tid; i < 1024; i += SNT) hist[i] = 0u;
     __syncthreads();
 #pragma unroll 1
-    for (int tl = tid * 4; tl < nloc; tl += NT * 4) {
+    for (int tl = tid * 4; tl < nloc; tl += SNT * 4) {
       uint32_t key[4];
       bool ok[4];
       keys4(scr, tl, nloc, key, ok);
@@ -271,7 +300,7 @@ __device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt = (1u << lane) - 1u;
   constexpr bool ties = TIES;
-  const int wlen = (((nloc + NW - 1) / NW) + 3) & ~3;
+  const int wlen = (((nloc + SNW - 1) / SNW) + 3) & ~3;
   const int w0 = min(nloc, warp * wlen), w1 = min(nloc, w0 + wlen);
   int tie_base = 0;
   if constexpr (ties) {
@@ -333,7 +362,7 @@ __device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc
   STEP_TRACE(26);
   int base = 0, total = 0;
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
+  for (int w = 0; w < SNW; ++w) {
     const int c = ms->scan[w];
     base += w < warp ? c : 0;
     total += c;
@@ -395,7 +424,7 @@ __device__ __forceinline__ void push_list(unsigned long long* recv, int stride, 
   const uint32_t slot = smem_u32(recv + (size_t)crank * stride);
   const uint4* src = reinterpret_cast<const uint4*>(recv + (size_t)crank * stride);
 #pragma unroll 1
-  for (int rr = warp; rr < C - 1; rr += NW) {  // warp per destination, lanes over the vectors
+  for (int rr = warp; rr < C - 1; rr += SNW) {  // warp per destination, lanes over the vectors
     const uint32_t r = (uint32_t)(rr + (rr >= (int)crank));
 #pragma unroll 1
     for (int v = lane; v < nvec; v += 32) dsmem_st_v4u32(dsmem_map(slot + v * 16, r), src[v]);
@@ -429,7 +458,7 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
   };
   unsigned long long mx = 0ull, mn = ~0ull;
 #pragma unroll 1
-  for (int f = tid; f < nslots; f += NT) {
+  for (int f = tid; f < nslots; f += SNT) {
     unsigned long long x;
     if (entry(f, x)) {
       mx = max(mx, x);
@@ -441,18 +470,18 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
   }
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(hb);  // [NW] maxima, [NW] minima
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(hb);  // [SNW] maxima, [SNW] minima
   if (lane == 0) {
     red[warp] = mx;
-    red[NW + warp] = mn;
+    red[SNW + warp] = mn;
   }
   __syncthreads();
   mx = red[0];
-  mn = red[NW];
+  mn = red[SNW];
 #pragma unroll
-  for (int w = 1; w < NW; ++w) {
+  for (int w = 1; w < SNW; ++w) {
     mx = max(mx, red[w]);
-    mn = min(mn, red[NW + w]);
+    mn = min(mn, red[SNW + w]);
   }
   __syncthreads();
   STEP_TRACE(16);
@@ -468,11 +497,11 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
     {
       uint4* z = reinterpret_cast<uint4*>(hb);
 #pragma unroll 1
-      for (int i = tid; i < NB / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = tid; i < NB / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
 #pragma unroll 1
-    for (int f = tid; f < nslots; f += NT) {
+    for (int f = tid; f < nslots; f += SNT) {
       unsigned long long x;
       if (entry(f, x) && (shift + nb == 64 || (x >> (shift + nb)) == prefix))
         atomicAdd(&hb[(uint32_t)(x >> shift) & ((1u << nb) - 1u)], 1u);
@@ -488,7 +517,7 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
   }
   const unsigned long long theta = shift == 64 ? 0ull : (prefix << shift);
 #pragma unroll 1
-  for (int r = warp; r < C; r += NW) {
+  for (int r = warp; r < C; r += SNW) {
     int c = 0;
 #pragma unroll 1
     for (int i = lane; i < slot_hdr(recv, stride, r)->x; i += 32) c += recv[(size_t)r * stride + 2 + i] >= theta;
@@ -563,19 +592,24 @@ __device__ __forceinline__ unsigned long long union_select(const unsigned long l
   hi = __reduce_max_sync(0xffffffffu, hi);
   const uint32_t span = hi - lo;  // keys lie in [lo, hi]
   const int shift = max(0, (32 - __clz((int)(span | 1u))) - 11);
+  // wps warps per source (at least one): a source's entries are split over
+  // its warps' lanes
+  const int wps = max(1, SNW / C);
+  const int sw = warp / wps, sl_ = (warp - sw * wps) * 32 + lane, sstride = wps * 32;
   {
     uint4* z = reinterpret_cast<uint4*>(hb);
 #pragma unroll 1
-    for (int i = tid; i < NB / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < NB / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < C_MAX) ms->sel[tid] = 0;
     if (tid == 0) ms->bkt_n = 0;
   }
   __syncthreads();
 #pragma unroll 1
-  for (int r = warp; r < C; r += NW) {
+  for (int r = sw; r < C; r += SNW / wps) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
 #pragma unroll 1
-    for (int i = lane; i < n; i += 32) atomicAdd(&hb[((uint32_t)(e[i] >> 32) - lo) >> shift], 1u);
+    for (int i = sl_; i < n; i += sstride) atomicAdd(&hb[((uint32_t)(e[i] >> 32) - lo) >> shift], 1u);
   }
   __syncthreads();
   find_digit<NB>(hb, k, ms->scan, &ms->dig);
@@ -583,12 +617,12 @@ __device__ __forceinline__ unsigned long long union_select(const unsigned long l
   const int k_rem = k - ms->gt, nbk = ms->bucket;
   if (nbk > 32) return union_kth(recv, stride, cap, C, k, hb, ms);  // (uniform)
 #pragma unroll 1
-  for (int r = warp; r < C; r += NW) {
+  for (int r = sw; r < C; r += SNW / wps) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
     int above = 0;
 #pragma unroll 1
-    for (int i = lane; i < n; i += 32) {
+    for (int i = sl_; i < n; i += sstride) {
       const unsigned long long x = e[i];
       const uint32_t b = ((uint32_t)(x >> 32) - lo) >> shift;
       above += b > bs;
@@ -599,7 +633,7 @@ __device__ __forceinline__ unsigned long long union_select(const unsigned long l
       }
     }
     above = warp_sum_i(above);
-    if (lane == 0) ms->sel[r] = above;
+    if (lane == 0 && above) atomicAdd(&ms->sel[r], above);
   }
   __syncthreads();
   if (warp == 0) {
@@ -648,7 +682,7 @@ __device__ __noinline__ bool reload_scores(const float* scw, int nloc, unsigned 
                                            uint64_t wait_ns) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = (nloc + 3) >> 2;
-  const int per_w = (nv + NW - 1) / NW;
+  const int per_w = (nv + SNW - 1) / SNW;
   const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
   fence_proxy_async_global();  // this thread's score stores, before the copy reads them
   __syncthreads();
@@ -686,7 +720,7 @@ __device__ __noinline__ float append_own_token(const unsigned long long* turns, 
   __syncthreads();
   auto dom_at = [&](int j) { return min(max(dom[j], 0), D / 2 - 1); };
 #pragma unroll 1
-  for (int j = tid; j < nfc; j += NT) {
+  for (int j = tid; j < nfc; j += SNT) {
     const float2 kp = scratch[dom_at(j)];
     kdw[(size_t)j * KDOM_BLOCK * 2] = __float2bfloat16_rn(kp.x);
     kdw[(size_t)j * KDOM_BLOCK * 2 + 1] = __float2bfloat16_rn(kp.y);
@@ -739,7 +773,7 @@ __device__ __noinline__ unsigned long long second_round(int k_eff, int nloc, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant__ StepParams p) {
+__global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant__ StepParams p) {
   using T = __nv_bfloat16;
   constexpr int ES = 2;
   constexpr int KB = KDOM_BLOCK;         // k_dom tokens per block
@@ -794,11 +828,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     kn = __halves2bfloat162(knp[0], knp[1]);
     vn = __halves2bfloat162(vnp[0], vnp[1]);
   }
-  constexpr int QPAIRS = (G_MAX * D / 2 + NT - 1) / NT;
+  constexpr int QPAIRS = (G_MAX * D / 2 + SNT - 1) / SNT;
   T qv0[QPAIRS], qv1[QPAIRS];
 #pragma unroll
   for (int k = 0; k < QPAIRS; ++k) {
-    const int x = tid + k * NT;
+    const int x = tid + k * SNT;
     qv0[k] = qv1[k] = T(0.f);
     if (x < G * (D / 2)) {
       const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D + 2 * x;
@@ -830,7 +864,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   }
   {
     uint4* z = reinterpret_cast<uint4*>(hist);
-    for (int i = tid; i < HLOC_BINS / 4; i += NT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < HLOC_BINS / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   // The barrier inits were fenced at cluster scope above; the matching wait
   // (after TIP) comes before any peer touches this CTA's shared memory.  A
@@ -909,7 +943,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   // ------------------------------------------------------------ query prep
 #pragma unroll 1
   for (int k = 0; k < QPAIRS; ++k) {
-    const int x = tid + k * NT;
+    const int x = tid + k * SNT;
     if (x < G * (D / 2)) {
       const int i = x & (D / 2 - 1);
       const float2 c = rope_cos_sin(turns[i], m_pos);
@@ -945,7 +979,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   STEP_TRACE(1);
 
   // ---------------------------------------------------------------- TIP scan
-  // Warp w scores the 128-token units w, w + NW, ...; a unit lies in one
+  // Warp w scores the 128-token units w, w + W, ... (W = p.tip_warps); a unit lies in one
   // stage.  In a refilled ring each unit's warp counts itself done with the
   // stage, and the warp that completes the stage refills it.  A wait that
   // runs out stops the warp and, through ms->tip_fail, the others.
@@ -961,7 +995,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   const bool ring = ntiles > ns;
   const uint32_t blk_bytes = (uint32_t)nfc * FCB;
   int tip_fail = 0;
-  for (int u = warp; u < nunits; u += NW) {
+  const int tip_stride = p.tip_warps;
+  for (int u = warp; warp < tip_stride && u < nunits; u += tip_stride) {  // (warps >= tip_warps score nothing)
     const int it = u / upt, s = it % ns;
     const uint32_t parity = (uint32_t)(it / ns) & 1u;
     int stop = lane == 0 ? *reinterpret_cast<volatile int*>(&ms->tip_fail) : 0;
@@ -1043,7 +1078,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     return rows[i];
   };
   // Gathers chunks [c0, c0 + nc) of row i's K then V (CPR chunks each) into
-  // its group's slot: group g belongs to warp g % NW, its slot (g / NW) mod
+  // its group's slot: group g belongs to warp g % FNW, its slot (g / FNW) mod
   // fac_wst (the slots are reused in turn); chunk c of a row sits at
   // chunk position c ^ (row & 7) so the eight rows an ldmatrix reads fall in
   // distinct banks.  Rows past fr_n are zero-filled: the tensor cores
@@ -1051,7 +1086,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   auto row_chunks = [&](int i, int c0, int nc) {
     const int g = i / GR, rr = i & (GR - 1);
     const uint32_t st0 =
-        smem_u32(big) + (uint32_t)((g % NW) * p.fac_wst + (g / NW) % p.fac_wst) * GSLOT_B + rr * ROWB;
+        smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B + rr * ROWB;
     const bool real = i < fr_n;
     const size_t off = real ? (size_t)row_token(i) * D : 0;
 #pragma unroll 1
@@ -1064,9 +1099,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   // the first fac_wst groups of every warp, issued by the whole CTA: four
   // threads per row, each a quarter of its chunks
   auto fac_start = [&]() {
-    const int nfirst = min((fr_n + GR - 1) / GR * GR, p.fac_wst * NW * GR);
+    const int nfirst = min((fr_n + GR - 1) / GR * GR, p.fac_wst * FNW * GR);
 #pragma unroll 1
-    for (int i = tid >> 2; i < nfirst; i += NT / 4) row_chunks(i, (tid & 3) * (CPR / 2), CPR / 2);
+    for (int i = tid >> 2; i < nfirst; i += SNT / 4) row_chunks(i, (tid & 3) * (CPR / 2), CPR / 2);
     cp_async_commit();
   };
 
@@ -1150,7 +1185,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       const unsigned long long* recv2 = reinterpret_cast<const unsigned long long*>(smem + p.off_recv2);
       const unsigned long long* own = second ? recv2 + (size_t)crank * (p.cap2 + 2) + 2 : own1 + 2;
       const int n_own = second ? slot_hdr(recv2, p.cap2 + 2, crank)->x : n1;
-      const int per_w = (n_own + NW - 1) / NW;
+      const int per_w = (n_own + SNW - 1) / SNW;
       const int e0 = min(n_own, warp * per_w), e1 = min(n_own, e0 + per_w);
       int c = 0;
 #pragma unroll 1
@@ -1159,7 +1194,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       if (lane == 0) ms->scan2[warp] = c;
       __syncthreads();
       int at = 0, n_sel = 0;
-      for (int w = 0; w < NW; ++w) {
+      for (int w = 0; w < SNW; ++w) {
         at += w < warp ? ms->scan2[w] : 0;
         n_sel += ms->scan2[w];
       }
@@ -1203,9 +1238,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   // gq, gq + 8 of S^T and head dims gq, gq + 8 of O^T, heads 2tq, 2tq + 1.
   constexpr int KS = D / 16;
   const int ngrp = (fr_n + GR - 1) / GR;
-  const int nrec = min(NW, ngrp);  // warps that attend rows
-  float* rec = reinterpret_cast<float*>(big);  // [G][NW][D + 2]
-  float* wts = rec + G_MAX * NW * (D + 2);     // [G][NW] + [G]
+  const int nrec = min(FNW, ngrp);  // warps that attend rows
+  float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
+  float* wts = rec + G_MAX * FNW * (D + 2);     // [G][FNW] + [G]
   cp_async_wait<0>();  // the CTA-wide first groups
   __syncthreads();
   if (warp < nrec) {
@@ -1233,7 +1268,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
     const int wst = p.fac_wst;
     int it = 0;
-    for (int g = warp; g < ngrp; g += NW, ++it) {
+    for (int g = warp; g < ngrp; g += FNW, ++it) {
       const int s = wst == 2 ? (it & 1) : 0;
       if (it > 0) {
         if (wst == 2) cp_async_wait<1>();
@@ -1303,7 +1338,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       // the warp's next group after the ones in flight: two lanes per row,
       // each half of its chunks (commits a group even when empty: the waits
       // count groups)
-      const int gn = g + wst * NW;
+      const int gn = g + wst * FNW;
       if (gn < ngrp) row_chunks(gn * GR + (lane >> 1), (lane & 1) * CPR, CPR);
       cp_async_commit();
     }
@@ -1322,22 +1357,22 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
       for (int mt = 0; mt < KS; ++mt) {
         const int dd = mt * 16 + gq;
         if (h0 < G) {
-          rec[(h0 * NW + warp) * (D + 2) + dd] = oc[mt][0];
-          rec[(h0 * NW + warp) * (D + 2) + dd + 8] = oc[mt][2];
+          rec[(h0 * FNW + warp) * (D + 2) + dd] = oc[mt][0];
+          rec[(h0 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][2];
         }
         if (h1 < G) {
-          rec[(h1 * NW + warp) * (D + 2) + dd] = oc[mt][1];
-          rec[(h1 * NW + warp) * (D + 2) + dd + 8] = oc[mt][3];
+          rec[(h1 * FNW + warp) * (D + 2) + dd] = oc[mt][1];
+          rec[(h1 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][3];
         }
       }
       if (gq == 0) {
         if (h0 < G) {
-          rec[(h0 * NW + warp) * (D + 2) + D] = m0;
-          rec[(h0 * NW + warp) * (D + 2) + D + 1] = l0;
+          rec[(h0 * FNW + warp) * (D + 2) + D] = m0;
+          rec[(h0 * FNW + warp) * (D + 2) + D + 1] = l0;
         }
         if (h1 < G) {
-          rec[(h1 * NW + warp) * (D + 2) + D] = m1;
-          rec[(h1 * NW + warp) * (D + 2) + D + 1] = l1;
+          rec[(h1 * FNW + warp) * (D + 2) + D] = m1;
+          rec[(h1 * FNW + warp) * (D + 2) + D + 1] = l1;
         }
       }
     }
@@ -1363,27 +1398,27 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     const int g = tid;
     float M = -CUDART_INF_F;
 #pragma unroll 1
-    for (int r = 0; r < nrec; ++r) M = fmaxf(M, rec[(g * NW + r) * (D + 2) + D]);
+    for (int r = 0; r < nrec; ++r) M = fmaxf(M, rec[(g * FNW + r) * (D + 2) + D]);
 #pragma unroll 1
     for (int r = 0; r < nrec; ++r) {
-      const float m_r = rec[(g * NW + r) * (D + 2) + D];
-      wts[g * NW + r] = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
+      const float m_r = rec[(g * FNW + r) * (D + 2) + D];
+      wts[g * FNW + r] = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
     }
-    wts[G * NW + g] = M;
+    wts[G * FNW + g] = M;
   }
   __syncthreads();
 #pragma unroll 1
-  for (int x = tid; x < G * (D + 2); x += NT) {
+  for (int x = tid; x < G * (D + 2); x += SNT) {
     const int g = x / (D + 2), e = x - g * (D + 2);
     float val = e == D ? -CUDART_INF_F : 0.f;
     if (big_ok) {
-      val = wts[G * NW + g];
+      val = wts[G * FNW + g];
       if (e != D) {
         float acc = 0.f;
 #pragma unroll 1
         for (int r = 0; r < nrec; ++r) {
-          const float w = wts[g * NW + r];
-          if (w != 0.f) acc += w * rec[(g * NW + r) * (D + 2) + e];
+          const float w = wts[g * FNW + r];
+          if (w != 0.f) acc += w * rec[(g * FNW + r) * (D + 2) + e];
         }
         val = acc;
       }
@@ -1420,7 +1455,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
   const int lpg = C <= 1 ? 1 : 1 << (32 - __clz(C - 1));
   const int gpw = 32 / lpg;
 #pragma unroll 1
-  for (int qw = q0 + gpw * warp; qw < q1; qw += gpw * NW) {  // warp-uniform bound
+  for (int qw = q0 + gpw * warp; qw < q1; qw += gpw * SNW) {  // warp-uniform bound
     const int q = qw + lane / lpg, r = lane & (lpg - 1);
     const bool okq = q < q1 && r < C;
     const int g = okq ? q / (D / 4) : 0, e4 = okq ? q - g * (D / 4) : 0;
@@ -1461,11 +1496,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_step_kernel(const __grid_constant_
     if (!need_select) {
       if (crank == 0)
 #pragma unroll 1
-        for (int i = tid; i < p.budget; i += NT) io[i] = i < k_eff ? i : -1;
+        for (int i = tid; i < p.budget; i += SNT) io[i] = i < k_eff ? i : -1;
     } else {
       const int n_own = ms->n_rows;  // in token order
 #pragma unroll 1
-      for (int i = tid; i < n_own; i += NT)
+      for (int i = tid; i < n_own; i += SNT)
         if (sel_before + i < p.budget) io[sel_before + i] = rows[i];
     }
   }

@@ -26,7 +26,7 @@ cudaError_t prepare_step() {
 cudaLaunchConfig_t step_config(int C, int units, int smem, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)C, (unsigned)units, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.blockDim = dim3(SNT, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
