@@ -402,8 +402,9 @@ def run_gpu(args):
     import torch
     from kv_cache_token_tip_gb300 import build as kbuild
     kbuild.build()
-    from kv_cache_token_tip_gb300 import (dims_for, fasa_apply_rope_q, fasa_cluster_size, fasa_decode_step,
-                                          fasa_dense_attention, fasa_device_status, fasa_workspace_size)
+    from kv_cache_token_tip_gb300 import (FASA_KERNEL_SINGLE_EXCHANGE, dims_for, fasa_apply_rope_q,
+                                          fasa_cluster_size, fasa_decode_step, fasa_dense_attention,
+                                          fasa_device_status, fasa_step_kernel, fasa_workspace_size)
 
     rank, world, local, pg = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -637,6 +638,8 @@ def run_gpu(args):
     achieved_gbs = per_step / sec_per_step / 1e9
     clocks = clk.summary()
     C = fasa_cluster_size(dims)
+    kernel_name = (f"fasa_step_kernel<{cfg.head_dim}>" if fasa_step_kernel(dims) == FASA_KERNEL_SINGLE_EXCHANGE
+                   else f"fasa_cluster_kernel<{cfg.dtype},{cfg.head_dim}>")
     line = None
     if args.cpu_baseline and rank == 0 and world == 1:
         cb = run_oracle_leg(cfg, args.cpu_seconds)
@@ -707,7 +710,7 @@ def run_gpu(args):
                                 if kk in model},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),
-                         "peak_kind": peak_kind, "kernel": f"fasa_cluster_kernel<{cfg.dtype},{cfg.head_dim}>"},
+                         "peak_kind": peak_kind, "kernel": kernel_name},
             "dense": {"us_per_step": round(dense_sec * 1e6, 3),
                       "achieved_gbs": round(model["dense_total"] * layers / dense_sec / 1e9, 1),
                       "sparse_vs_dense_speedup": round(dense_sec / sec_per_step, 3)},

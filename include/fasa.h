@@ -343,6 +343,15 @@ int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile);
 /* Cluster size (CTAs per (b, KV head)) the fused kernels use on this device. */
 int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas);
 
+/* Which fused kernel serves fasa_decode_step (and the _append and _noalloc
+ * forms) for these dims on this device: FASA_KERNEL_SINGLE_EXCHANGE (bf16
+ * caches, clusters of 8 or more CTAs per unit: one list exchange, a verified
+ * union top-k, one combine exchange) or FASA_KERNEL_CLUSTER (every other
+ * plan: the radix-select cluster kernel).  Both compute the same step; the
+ * selected set and the output agree up to the documented rounding. */
+enum { FASA_KERNEL_CLUSTER = 0, FASA_KERNEL_SINGLE_EXCHANGE = 1 };
+int fasa_step_kernel(const fasa_dims_t* dims, int32_t* kernel);
+
 #ifdef __cplusplus
 }
 #endif

@@ -695,6 +695,22 @@ int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas) {
   return FASA_OK;
 }
 
+int fasa_step_kernel(const fasa_dims_t* dims, int32_t* kernel) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!kernel) return FASA_ERR_INVALID_ARG;
+  *kernel = FASA_KERNEL_CLUSTER;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, 1);
+    int C = 0;
+    st = step_plan_and_launch(sp, dims, nullptr, 0, false, nullptr, &C, nullptr);
+    if (st == FASA_OK) *kernel = FASA_KERNEL_SINGLE_EXCHANGE;
+    else if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
+  return FASA_OK;
+}
+
 int fasa_apply_rope_q(const void* q, const int32_t* pos, float* q_rot, const fasa_dims_t* dims,
                       fasa_stream_t stream) {
   int st = check_dims(dims);

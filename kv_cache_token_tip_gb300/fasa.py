@@ -21,7 +21,7 @@ EXPORTS = [
     "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention", "fasa_dense_attention",
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
     "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
-    "fasa_select_dominant_fcs", "fasa_compound_agreement", "fasa_test_fault_injection",
+    "fasa_select_dominant_fcs", "fasa_compound_agreement", "fasa_test_fault_injection", "fasa_step_kernel",
 ]
 
 
@@ -76,6 +76,7 @@ def lib():
             "fasa_max_budget": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
             "fasa_workspace_size": ([dp, i32, ctypes.POINTER(sz)], ctypes.c_int),
             "fasa_cluster_size": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
+            "fasa_step_kernel": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
             "fasa_apply_rope_q": ([vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_build_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_append_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
@@ -167,6 +168,17 @@ def fasa_workspace_size(dims: FasaDims, budget: int) -> int:
 def fasa_cluster_size(dims: FasaDims) -> int:
     out = ctypes.c_int32(0)
     _check("fasa_cluster_size", lib().fasa_cluster_size(ctypes.byref(dims), ctypes.byref(out)))
+    return out.value
+
+
+FASA_KERNEL_CLUSTER, FASA_KERNEL_SINGLE_EXCHANGE = 0, 1
+
+
+def fasa_step_kernel(dims: FasaDims) -> int:
+    """Which fused kernel serves fasa_decode_step for these dims on this
+    device (FASA_KERNEL_CLUSTER or FASA_KERNEL_SINGLE_EXCHANGE)."""
+    out = ctypes.c_int32(0)
+    _check("fasa_step_kernel", lib().fasa_step_kernel(ctypes.byref(dims), ctypes.byref(out)))
     return out.value
 
 

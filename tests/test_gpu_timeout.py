@@ -1,0 +1,97 @@
+"""The bounded device waits of the fused step (GPU).
+
+A step whose TIP stage barrier is armed for a copy that is never issued
+(fasa_test_fault_injection) must end by itself once the wait bound runs out,
+report FASA_DEV_TIMEOUT in the device status word, and leave the stream and
+the context usable: the next step, with the defaults restored, gives the
+same result as a step before the fault.  Nothing here faults the GPU: the
+wait that runs out is on a shared-memory barrier no copy targets.
+"""
+
+import time
+
+import numpy as np
+import pytest
+
+from tests.gpu_util import build_kdom, ensure_built
+from workload import configs, gpu_gen
+
+pytestmark = pytest.mark.gpu
+
+SHORT_NS = 2_000_000   # 2 ms: far above a clean step (tens of microseconds)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    ensure_built()
+
+
+def _setup():
+    import torch
+    from kv_cache_token_tip_gb300 import FASA_KERNEL_SINGLE_EXCHANGE, dims_for, fasa_step_kernel, fasa_workspace_size
+    cfg = configs.CONFIGS["llama3_8b_ctx32k"]
+    dims = dims_for(cfg)
+    # the fault hook acts on the single-exchange kernel's TIP staging
+    assert fasa_step_kernel(dims) == FASA_KERNEL_SINGLE_EXCHANGE
+    L = gpu_gen.make_layer(cfg, 0)
+    kd = build_kdom(L, dims)
+    n = fasa_workspace_size(dims, cfg.budget)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda") if n else None
+    return cfg, dims, L, kd, ws
+
+
+def _step(cfg, dims, L, kd, ws):
+    import torch
+    from kv_cache_token_tip_gb300 import fasa_decode_step
+    out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    idx = torch.full((cfg.batch, cfg.n_kv_heads, cfg.budget), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((cfg.batch, cfg.n_kv_heads), -1, dtype=torch.int32, device="cuda")
+    fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, cnt, ws, dims)
+    return out, idx, cnt
+
+
+def test_short_wait_bound_alone_changes_nothing():
+    from kv_cache_token_tip_gb300 import fasa_device_status, fasa_test_fault_injection
+    cfg, dims, L, kd, ws = _setup()
+    fasa_device_status()
+    out0, idx0, cnt0 = _step(cfg, dims, L, kd, ws)
+    assert fasa_device_status() == 0
+    try:
+        fasa_test_fault_injection(wait_limit_ns=SHORT_NS)
+        out1, idx1, cnt1 = _step(cfg, dims, L, kd, ws)
+        st = fasa_device_status()
+    finally:
+        fasa_test_fault_injection()
+    assert st == 0
+    assert np.array_equal(idx1.cpu().numpy(), idx0.cpu().numpy())
+    assert np.array_equal(cnt1.cpu().numpy(), cnt0.cpu().numpy())
+    assert np.array_equal(out1.cpu().numpy(), out0.cpu().numpy())
+
+
+def test_unissued_tip_copy_times_out_and_the_stream_stays_usable():
+    import torch
+    from kv_cache_token_tip_gb300 import FASA_DEV_TIMEOUT, fasa_device_status, fasa_test_fault_injection
+    cfg, dims, L, kd, ws = _setup()
+    fasa_device_status()
+    out0, idx0, cnt0 = _step(cfg, dims, L, kd, ws)
+    assert fasa_device_status() == 0
+    try:
+        fasa_test_fault_injection(wait_limit_ns=SHORT_NS, drop_tip_tile=0)
+        t0 = time.perf_counter()
+        _step(cfg, dims, L, kd, ws)
+        st = fasa_device_status()          # synchronises the stream
+        elapsed = time.perf_counter() - t0
+    finally:
+        fasa_test_fault_injection()
+    assert st & FASA_DEV_TIMEOUT, f"status {st}"
+    # the copy wait, the drain and the peer exchanges are each bounded:
+    # the launch ends within a small multiple of the bound
+    assert elapsed < 2.0, f"faulted step took {elapsed:.3f} s"
+    # the context and the stream still work, and the next clean step is
+    # unaffected by the barrier state the faulted one left behind
+    out2, idx2, cnt2 = _step(cfg, dims, L, kd, ws)
+    assert fasa_device_status() == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(idx2.cpu().numpy(), idx0.cpu().numpy())
+    assert np.array_equal(cnt2.cpu().numpy(), cnt0.cpu().numpy())
+    assert np.array_equal(out2.cpu().numpy(), out0.cpu().numpy())

@@ -57,11 +57,14 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     import ctypes
-    from kv_cache_token_tip_gb300 import dims_for, lib
+    from kv_cache_token_tip_gb300 import dims_for, fasa_workspace_size, lib
     cfg = configs.CONFIGS["llama3_8b_b4_ctx128k"].with_(batch=5)   # 5*8*131072*4 B = 20 MiB > 16 MiB
     dims = dims_for(cfg, cluster_ctas=4)
-    P_ = 0x10000
-    st = lib().fasa_decode_step_noalloc(P_, P_, P_, P_, P_, P_, P_, cfg.budget, P_, None, None,
+    # the size check must come first: with the plan's workspace beyond the
+    # scratch, the call returns before it looks at (or launches on) any
+    # pointer, so null pointers are safe here
+    assert fasa_workspace_size(dims, cfg.budget) > (16 << 20)
+    st = lib().fasa_decode_step_noalloc(None, None, None, None, None, None, None, cfg.budget, None, None, None,
                                         ctypes.byref(dims), None)
     assert st == 3   # FASA_ERR_WORKSPACE, before any launch
 
