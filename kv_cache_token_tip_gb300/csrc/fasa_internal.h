@@ -76,7 +76,7 @@ constexpr int SNW = SNT / 32;      // its warps
 constexpr int FNW = 8;             // warps that attend rows (one 16-row group slot set each)
 constexpr int ST_MAX_STAGES = 12;  // TIP stage mbarriers [0, 12)
 constexpr int ST_BARS = 16;        // + two selection exchanges, the combine, the score reload
-constexpr int ST_MISC_BYTES = 1024;
+constexpr int ST_MISC_BYTES = 1152;
 constexpr int UH_BINS = 256;       // histogram of the union's 8-bit digits
 constexpr int TIP_UNIT = 128;      // tokens per warp step of TIP (32 lanes x 4)
 

@@ -49,13 +49,21 @@ constexpr int SB_COMB = 14;        // partial records for the combine (the peers
 constexpr int SB_RELOAD = 15;      // score reload from the workspace
 
 
+// The unit's length and this CTA's token range, planned by the issuing warp
+// and read by every thread after the set-up barrier.
+struct StepHdr {
+  int len, m_pos, t_new, bad;  // tokens attended, query position, appended index (-1: none), bad input
+  int t0, nloc, nloc_s, ntiles;  // range start and size, tokens streamed, TIP tiles
+  int nfc, pad[3];               // this head's dominant-FC count
+};
+
 struct StepMisc {
+  StepHdr hdr;
   int dig, gt, bucket, pad0;  // radix digit search result
   int scan[SNW];
   int scan2[SNW];
   int tip_fail;
   int big_unsafe;       // a TIP copy did not land in time: shared staging is not reused
-  int nfc;              // this head's dominant-FC count
   int hist_clobbered;   // the digit-0 histogram was overwritten by later digits
   uint32_t tip_done[ST_MAX_STAGES];
   int tip_last[ST_MAX_STAGES];
@@ -484,7 +492,6 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
     mn = min(mn, red[SNW + w]);
   }
   __syncthreads();
-  STEP_TRACE(16);
   const unsigned long long diff = mx ^ mn;
   int shift = diff ? 64 - __clzll((long long)diff) : 0;  // bits below `shift` are still open
   unsigned long long prefix = shift == 64 ? 0ull : (mx >> shift);
@@ -507,9 +514,7 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
         atomicAdd(&hb[(uint32_t)(x >> shift) & ((1u << nb) - 1u)], 1u);
     }
     __syncthreads();
-    if (pass < 3) STEP_TRACE(17 + 2 * pass);
     find_digit<NB>(hb, k_rem, ms->scan, res);
-    if (pass < 3) STEP_TRACE(18 + 2 * pass);
     ++pass;
     k_rem -= res[1];
     prefix = (prefix << nb) | (unsigned long long)res[0];
@@ -525,14 +530,14 @@ __device__ __noinline__ unsigned long long union_kth(const unsigned long long* r
     if (lane == 0) ms->sel[r] = c;
   }
   __syncthreads();
-  STEP_TRACE(23);
   return theta;
 }
 
-// Warp 0: the digit-0 bin (key >> 20) holding the r-th largest key, read
-// from the 64-bin coarse histogram (key >> 26) and then the 64 fine bins of
-// the coarse bin found, one warp scan each.  Writes ms->dig / gt (keys in
-// larger bins) / bucket.  1 <= r <= the histogram's total.
+// One warp: the bin of a 4096-bin histogram (hist; fine bin f lies in coarse
+// bin f >> 6 of chist) holding the r-th largest entry, read from the 64
+// coarse bins and then the 64 fine bins of the coarse bin found, one warp
+// scan each.  Writes ms->dig / gt (entries in larger bins) / bucket.
+// 1 <= r <= the histogram's total.
 __device__ __forceinline__ void warp_find_d0(const uint32_t* hist, const uint32_t* chist, int r, StepMisc* ms) {
   const int lane = threadIdx.x & 31;
   int base = 0, above = 0;
@@ -570,15 +575,16 @@ __device__ __forceinline__ void warp_find_d0(const uint32_t* hist, const uint32_
 // smallest and largest key it listed; values are distinct): exactly k
 // entries are >= theta (the caller guarantees the union holds at least k).
 // One pass bins every entry by its key's offset from the smallest key,
-// shifted to at most 2048 bins (hb); the bin holding the k-th entry is
-// found; a second pass counts each source's entries in higher bins and
-// gathers that bin's entries, which one warp ranks.  A bin of more than 32
-// entries (dense or tied keys) falls back to the radix search.  Stores per
-// source the count of its entries >= theta in ms->sel.  A warp sweeps whole
-// sources.  Every thread calls it.
-__device__ __forceinline__ unsigned long long union_select(const unsigned long long* recv, int stride, int cap,
-                                                           int C, int k, uint32_t* hb, StepMisc* ms) {
-  constexpr int NB = 2048;
+// shifted to at most 4096 fine bins (hb) and 64 coarse bins of 64 fine ones
+// (ch); warp 0 finds the bin holding the k-th entry, coarse level first; a
+// second pass counts each source's entries in higher bins and gathers that
+// bin's entries, which one warp ranks; theta goes to ms->theta.  A bin of
+// more than 32 entries (dense or tied keys; ms->bucket > 32 on return) is
+// left to the caller's radix search.  hb, ch, ms->sel and ms->bkt_n arrive
+// cleared.  Stores per source the count of its entries >= theta in ms->sel.
+// Warps 0..nuw-1 call it (named barrier 4).
+__device__ __forceinline__ void union_select(const unsigned long long* recv, int stride, int cap, int C, int k,
+                                             uint32_t* hb, uint32_t* ch, StepMisc* ms, int nuw) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // lane r reads source r's header
   if (lane < C) {
@@ -591,33 +597,32 @@ __device__ __forceinline__ unsigned long long union_select(const unsigned long l
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
   const uint32_t span = hi - lo;  // keys lie in [lo, hi]
-  const int shift = max(0, (32 - __clz((int)(span | 1u))) - 11);
+  const int shift = max(0, (32 - __clz((int)(span | 1u))) - 12);
   // wps warps per source (at least one): a source's entries are split over
   // its warps' lanes
-  const int wps = max(1, SNW / C);
+  const int wps = max(1, nuw / C);
   const int sw = warp / wps, sl_ = (warp - sw * wps) * 32 + lane, sstride = wps * 32;
-  {
-    uint4* z = reinterpret_cast<uint4*>(hb);
 #pragma unroll 1
-    for (int i = tid; i < NB / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid < C_MAX) ms->sel[tid] = 0;
-    if (tid == 0) ms->bkt_n = 0;
-  }
-  __syncthreads();
-#pragma unroll 1
-  for (int r = sw; r < C; r += SNW / wps) {
+  for (int r = sw; r < C; r += nuw / wps) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
 #pragma unroll 1
-    for (int i = sl_; i < n; i += sstride) atomicAdd(&hb[((uint32_t)(e[i] >> 32) - lo) >> shift], 1u);
+    for (int i = sl_; i < n; i += sstride) {
+      const uint32_t bin = ((uint32_t)(e[i] >> 32) - lo) >> shift;
+      atomicAdd(&hb[bin], 1u);
+      atomicAdd(&ch[bin >> 6], 1u);
+    }
   }
-  __syncthreads();
-  find_digit<NB>(hb, k, ms->scan, &ms->dig);
+  named_bar_sync(4, nuw * 32);
+  STEP_TRACE(25);
+  if (warp == 0) warp_find_d0(hb, ch, k, ms);
+  named_bar_sync(4, nuw * 32);
+  STEP_TRACE(31);
   const uint32_t bs = (uint32_t)ms->dig;
   const int k_rem = k - ms->gt, nbk = ms->bucket;
-  if (nbk > 32) return union_kth(recv, stride, cap, C, k, hb, ms);  // (uniform)
+  if (nbk > 32) return;  // (uniform) the caller runs the radix search
 #pragma unroll 1
-  for (int r = sw; r < C; r += SNW / wps) {
+  for (int r = sw; r < C; r += nuw / wps) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
     int above = 0;
@@ -635,19 +640,19 @@ __device__ __forceinline__ unsigned long long union_select(const unsigned long l
     above = warp_sum_i(above);
     if (lane == 0 && above) atomicAdd(&ms->sel[r], above);
   }
-  __syncthreads();
+  named_bar_sync(4, nuw * 32);
+  STEP_TRACE(6);
   if (warp == 0) {
     const unsigned long long x = lane < nbk ? ms->bkt[lane] : 0ull;  // (lanes >= nbk hold 0: never larger)
     int rank = 0;  // entries of the bin larger than x
-#pragma unroll
-    for (int i = 0; i < 32; ++i) rank += __shfl_sync(0xffffffffu, x, i) > x;
+#pragma unroll 1
+    for (int i = 0; i < nbk; ++i) rank += ms->bkt[i] > x;
     if (lane < nbk) {
       if (rank == k_rem - 1) ms->theta = x;
       if (rank < k_rem) atomicAdd(&ms->sel[ms->bkt_src[lane]], 1);
     }
   }
-  __syncthreads();
-  return ms->theta;
+  named_bar_sync(4, nuw * 32);
 }
 
 // ----------------------------------------------------------- rare paths
@@ -802,125 +807,23 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   unsigned char* big = smem + p.off_big;
 
   STEP_TRACE(0);
+  constexpr int QW = 8;  // query warps
+  constexpr int QPAIRS = (G_MAX * D / 2 + QW * 32 - 1) / (QW * 32);
   const int nfc_max = p.n_tip, tt = p.tip_tile, ns = p.tip_stages;
-  // barriers first: their fence must not wait for the loads below
-  if (warp == 0 && lane < ST_BARS && (lane < ns || lane >= ST_MAX_STAGES)) {
-    // X1 and COMB complete when the C - 1 peers' bulk copies have landed
-    // (their bytes are expected here, with the one local arrival); X2 takes
-    // one arrival per CTA
-    mbar_init(smem_u32(&bars[lane]), lane == SB_X2 ? (uint32_t)C : 1u);
-    fence_mbar_init();
-    if (lane == SB_X1) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * (p.cap1 + 2) * 8));
-    if (lane == SB_COMB) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * p.comb_slot));
-  }
-  // small inputs: every load is in flight during the rest of the set-up, and
-  // the query pairs stay in their stored form until used
   const bool append = (p.flags & F_APPEND) != 0;
-  bool bad = false;
-  int len = p.seq_lens[b];
-  int m_pos = append ? 0 : p.pos[b];
-  const int dom_i = tid < nfc_max ? p.dom_fc[h * nfc_max + tid] : 0;
-  const int dom_hi = (warp == 0 && lane + 32 < nfc_max) ? p.dom_fc[h * nfc_max + lane + 32] : 0;
-  __nv_bfloat162 kn = __float2bfloat162_rn(0.f), vn = kn;
-  if (append && tid < D / 2) {  // (element-aligned inputs: two 2-byte loads each)
-    const T* knp = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D + 2 * tid;
-    const T* vnp = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D + 2 * tid;
-    kn = __halves2bfloat162(knp[0], knp[1]);
-    vn = __halves2bfloat162(vnp[0], vnp[1]);
-  }
-  constexpr int QPAIRS = (G_MAX * D / 2 + SNT - 1) / SNT;
-  T qv0[QPAIRS], qv1[QPAIRS];
-#pragma unroll
-  for (int k = 0; k < QPAIRS; ++k) {
-    const int x = tid + k * SNT;
-    qv0[k] = qv1[k] = T(0.f);
-    if (x < G * (D / 2)) {
-      const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D + 2 * x;
-      qv0[k] = qg[0];
-      qv1[k] = qg[1];
-    }
-  }
-
-  // ---------------------------------------------------------------- set-up
-  // the RoPE table goes to shared memory (each thread reads its own entry
-  // later; per-thread indices into kernel parameters would serialize)
-  unsigned long long* turns = reinterpret_cast<unsigned long long*>(uh);  // [D/2]
-  if (tid < D / 2) turns[tid] = p.rope_turns[tid];
-  if (warp == 0) {
-    if (lane < ST_MAX_STAGES) {
-      ms->tip_done[lane] = 0u;
-      ms->tip_last[lane] = -1;
-    }
-    if (lane < C_MAX) ms->sel[lane] = 0;
-    ms->chist[lane] = 0u;
-    ms->chist[lane + 32] = 0u;
-    if (lane == 0) {
-      ms->tip_fail = 0;
-      ms->big_unsafe = 0;
-      ms->hist_clobbered = 0;
-      ms->n_rows = 0;
-      ms->list_max = 0u;
-    }
-  }
-  {
-    uint4* z = reinterpret_cast<uint4*>(hist);
-    for (int i = tid; i < HLOC_BINS / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  // The barrier inits were fenced at cluster scope above; the matching wait
-  // (after TIP) comes before any peer touches this CTA's shared memory.  A
-  // relaxed arrive does not wait for this thread's loads still in flight.
-  cluster_arrive_relaxed();
-  __syncthreads();
-  STEP_TRACE(12);
-
-  int nfc = nfc_max;
-  if (warp == 0) {  // this head's count: the entries before the first negative one
-    const unsigned b0 = __ballot_sync(0xffffffffu, lane < nfc_max && dom_i < 0);
-    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && dom_hi < 0);
-    nfc = b0 ? __ffs(b0) - 1 : (b1 ? 31 + __ffs(b1) : nfc_max);
-    nfc = max(nfc, 1);  // an empty set uses slot 0 (reported below)
-    if (lane == 0) ms->nfc = nfc;
-  }
-  if (len < 0 || len > p.T_max) {
-    bad = true;
-    len = min(max(len, 0), p.T_max);
-  }
-  // F_APPEND: the step's own token goes to index t_new = len, the query sits
-  // at that position, and the step attends len + 1 tokens (a full cache
-  // cannot take the token: reported, not appended)
-  int t_new = -1;
-  if (append) {
-    m_pos = len;
-    if (len < p.T_max) {
-      t_new = len;
-      len += 1;
-    } else {
-      bad = true;
-    }
-  }
-  const int k_eff = min(p.budget, len);
-  const bool need_select = len > p.budget;
-  // contiguous token range of this CTA, its start aligned to a k_dom block
-  const int chunk = ((len + C - 1) / C + KB - 1) / KB * KB;
-  const int t0 = min(len, (int)crank * chunk);
-  const int t1 = min(len, t0 + chunk);
-  const int nloc = t1 - t0;
-  // K_dom is streamed up to the new token, which its CTA scores from registers
-  const bool own_new = t_new >= t0 && t_new < t1;
-  const int nloc_s = own_new ? t_new - t0 : nloc;
-  const int t1s = t0 + nloc_s;
-
-  // ---------------------------------------------------------------- TIP loads
   // k_dom is [.., T_max/KB, n_tip, KB, 2]: a tile of whole blocks is one
   // contiguous range (one bulk copy); a head using fewer planes takes the
   // leading nfc planes of each block, packed in the stage
-  const int ntiles = need_select ? (nloc_s + tt - 1) / tt : 0;
   const uint32_t stage_bytes = (uint32_t)(tt / KB) * nfc_max * FCB;
   const T* kd_unit = reinterpret_cast<const T*>(p.k_dom) + (size_t)unit * nfc_max * p.T_max * 2;
+  // the unit's length and this CTA's range (warp 1 plans them; every thread
+  // reads them after the set-up barrier)
+  int len = 0, m_pos = 0, t_new = -1, t0 = 0, nloc = 0, nloc_s = 0, ntiles = 0, nfc = 1;
+  bool bad = false;
   auto tip_issue = [&](int it) {  // one thread per tile; nfc is this head's count
-    const int s = it % ns;
+    const int s = it < ns ? it : it % ns;
     const int tau0 = t0 + it * tt;
-    const int nblk = (min(tt, t1s - tau0) + KB - 1) / KB;
+    const int nblk = (min(tt, t0 + nloc_s - tau0) + KB - 1) / KB;
     const uint32_t blk_bytes = (uint32_t)nfc * FCB;
     const uint32_t bar = smem_u32(&bars[s]);
     mbar_arrive_expect_tx(bar, (uint32_t)nblk * blk_bytes);
@@ -937,37 +840,189 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     }
     ms->tip_last[s] = it;
   };
-  if (warp == 0 && lane < min(ns, ntiles)) tip_issue(lane);  // one stage per lane
-  STEP_TRACE(13);
 
-  // ------------------------------------------------------------ query prep
-#pragma unroll 1
-  for (int k = 0; k < QPAIRS; ++k) {
-    const int x = tid + k * SNT;
-    if (x < G * (D / 2)) {
-      const int i = x & (D / 2 - 1);
-      const float2 c = rope_cos_sin(turns[i], m_pos);
-      const float x0 = __bfloat162float(qv0[k]), x1 = __bfloat162float(qv1[k]);
-      *reinterpret_cast<float2*>(&qrot[2 * x]) = make_float2(x0 * c.x - x1 * c.y, x0 * c.y + x1 * c.x);
+  // ---------------------------------------------------------------- set-up
+  // Split so that the TIP copies go out as soon as the unit's length and FC
+  // table are in: warp 1 loads them, plans this CTA's token range and issues
+  // the copies; meanwhile warp 0 initialises the barriers and the scratch
+  // (a release fence waits for its thread's loads, so warp 0 loads nothing
+  // before it) and the other warps load the query and clear the histogram.
+  if (warp == 0) {
+    if (lane < ST_BARS && (lane < ns || lane >= ST_MAX_STAGES)) {
+      // X1 and COMB complete when the C - 1 peers' bulk copies have landed
+      // (their bytes are expected here, with the one local arrival); X2
+      // takes one arrival per CTA
+      mbar_init(smem_u32(&bars[lane]), lane == SB_X2 ? (uint32_t)C : 1u);
+      fence_mbar_init();
+      if (lane == SB_X1) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * (p.cap1 + 2) * 8));
+      if (lane == SB_COMB) mbar_arrive_expect_tx(smem_u32(&bars[lane]), (uint32_t)((C - 1) * p.comb_slot));
     }
-  }
-  __syncthreads();
-  nfc = ms->nfc;
-  if (tid < nfc) {  // q-bar: the group sum of the rotated query on the dominant FCs
-    int i = dom_i;
-    if (i < 0 || i >= D / 2) {
+    if (lane < ST_MAX_STAGES) {
+      ms->tip_done[lane] = 0u;
+      ms->tip_last[lane] = -1;
+    }
+    if (lane < C_MAX) ms->sel[lane] = 0;
+    ms->chist[lane] = 0u;
+    ms->chist[lane + 32] = 0u;
+    if (lane == 0) {
+      ms->tip_fail = 0;
+      ms->big_unsafe = 0;
+      ms->hist_clobbered = 0;
+      ms->n_rows = 0;
+      ms->list_max = 0u;
+    }
+    STEP_TRACE(16);
+    named_bar_arrive(2, 64);  // barriers and stage records ready for warp 1
+  } else if (warp == 1) {
+    len = p.seq_lens[b];
+    m_pos = append ? 0 : p.pos[b];
+    const int d0 = lane < nfc_max ? p.dom_fc[h * nfc_max + lane] : 0;
+    const int d1 = lane + 32 < nfc_max ? p.dom_fc[h * nfc_max + lane + 32] : 0;
+    // this head's count: the entries before the first negative one (an
+    // empty set uses slot 0, reported below)
+    const unsigned b0 = __ballot_sync(0xffffffffu, lane < nfc_max && d0 < 0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && d1 < 0);
+    nfc = max(b0 ? __ffs(b0) - 1 : (b1 ? 31 + __ffs(b1) : nfc_max), 1);
+    if (len < 0 || len > p.T_max) {
       bad = true;
-      i = min(max(i, 0), D / 2 - 1);
+      len = min(max(len, 0), p.T_max);
     }
-    float a0 = 0.f, a1 = 0.f;
-    for (int g = 0; g < G; ++g) {
-      a0 += qrot[g * D + 2 * i];
-      a1 += qrot[g * D + 2 * i + 1];
+    // F_APPEND: the step's own token goes to index t_new = len, the query
+    // sits at that position, and the step attends len + 1 tokens (a full
+    // cache cannot take the token: reported, not appended)
+    if (append) {
+      m_pos = len;
+      if (len < p.T_max) {
+        t_new = len;
+        len += 1;
+      } else {
+        bad = true;
+      }
     }
-    qbar[2 * tid] = a0;
-    qbar[2 * tid + 1] = a1;
+    // contiguous token range of this CTA, its start aligned to a k_dom
+    // block; K_dom is streamed up to the new token, which its CTA scores
+    // from registers
+    const int chunk = ((len + C - 1) / C + KB - 1) / KB * KB;
+    t0 = min(len, (int)crank * chunk);
+    nloc = min(len, t0 + chunk) - t0;
+    nloc_s = t_new >= t0 && t_new < t0 + nloc ? t_new - t0 : nloc;
+    ntiles = len > p.budget ? (nloc_s + tt - 1) / tt : 0;
+    STEP_TRACE(20);
+    if (lane == 0) {
+      StepHdr& hd = ms->hdr;
+      hd.len = len;
+      hd.m_pos = m_pos;
+      hd.t_new = t_new;
+      hd.bad = bad;
+      hd.t0 = t0;
+      hd.nloc = nloc;
+      hd.nloc_s = nloc_s;
+      hd.ntiles = ntiles;
+      hd.nfc = nfc;
+    }
+    named_bar_sync(2, 64);
+    STEP_TRACE(21);
+    if (lane < min(ns, ntiles)) tip_issue(lane);  // one stage per lane
+    STEP_TRACE(13);
   }
+  // Warps 2..9 (the query warps) rotate the G query heads and form q-bar
+  // while warp 1 waits for the length and issues the copies: that code runs
+  // before the TIP data streams into the SM (instruction fetches compete
+  // with it).  Each query warp copies its share of the RoPE table to shared
+  // memory first (per-thread indices into kernel parameters serialize
+  // within a warp).
+  unsigned long long* turns = reinterpret_cast<unsigned long long*>(uh);  // [D/2]
+  if (warp >= 2 && warp < 2 + QW) {
+    const int qt = tid - 64;
+    const int l0 = p.seq_lens[b];
+    const int mp = append ? min(max(l0, 0), p.T_max) : p.pos[b];
+    T qv0[QPAIRS], qv1[QPAIRS];
+#pragma unroll
+    for (int k = 0; k < QPAIRS; ++k) {
+      const int x = qt + k * QW * 32;
+      qv0[k] = qv1[k] = T(0.f);
+      if (x < G * (D / 2)) {
+        const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)h * G) * D + 2 * x;
+        qv0[k] = qg[0];
+        qv1[k] = qg[1];
+      }
+    }
+    // q-bar threads: entry qt of the FC table, and (warps 2, 3) the count
+    const int dq = qt < nfc_max ? p.dom_fc[h * nfc_max + qt] : 0;
+    constexpr int TPQ = D / 2 / QW;
+    static_assert(TPQ >= 1 && TPQ * QW == D / 2, "RoPE table share per query warp");
+    if (lane < TPQ) turns[(warp - 2) * TPQ + lane] = p.rope_turns[(warp - 2) * TPQ + lane];
+    named_bar_sync(3, QW * 32);  // the table is complete
+#pragma unroll 1
+    for (int k = 0; k < QPAIRS; ++k) {
+      const int x = qt + k * QW * 32;
+      if (x < G * (D / 2)) {
+        const int i = x & (D / 2 - 1);
+        const float2 c = rope_cos_sin(turns[i], mp);
+        const float x0 = __bfloat162float(qv0[k]), x1 = __bfloat162float(qv1[k]);
+        *reinterpret_cast<float2*>(&qrot[2 * x]) = make_float2(x0 * c.x - x1 * c.y, x0 * c.y + x1 * c.x);
+      }
+    }
+    STEP_TRACE(22);
+    named_bar_sync(3, QW * 32);  // the rotated query is complete
+    if (warp < 4) {  // q-bar: the group sum of the rotated query on the dominant FCs
+      const int e0 = lane < nfc_max ? p.dom_fc[h * nfc_max + lane] : 0;
+      const int e1 = lane + 32 < nfc_max ? p.dom_fc[h * nfc_max + lane + 32] : 0;
+      const unsigned b0 = __ballot_sync(0xffffffffu, lane < nfc_max && e0 < 0);
+      const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < nfc_max && e1 < 0);
+      const int nq = max(b0 ? __ffs(b0) - 1 : (b1 ? 31 + __ffs(b1) : nfc_max), 1);
+      if (qt < nq) {
+        int i = dq;
+        if (i < 0 || i >= D / 2) {
+          bad = true;
+          i = min(max(i, 0), D / 2 - 1);
+        }
+        float a0 = 0.f, a1 = 0.f;
+        for (int g = 0; g < G; ++g) {
+          a0 += qrot[g * D + 2 * i];
+          a1 += qrot[g * D + 2 * i + 1];
+        }
+        qbar[2 * qt] = a0;
+        qbar[2 * qt + 1] = a1;
+      }
+    }
+    STEP_TRACE(17);
+  }
+  __nv_bfloat162 kn = __float2bfloat162_rn(0.f), vn = kn;
+  if (append && tid < D / 2) {  // (element-aligned inputs: two 2-byte loads each)
+    const T* knp = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D + 2 * tid;
+    const T* vnp = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D + 2 * tid;
+    kn = __halves2bfloat162(knp[0], knp[1]);
+    vn = __halves2bfloat162(vnp[0], vnp[1]);
+  }
+  {
+    uint4* z = reinterpret_cast<uint4*>(hist);
+    for (int i = tid; i < HLOC_BINS / 4; i += SNT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  STEP_TRACE(19);
+  // The barrier inits were fenced at cluster scope above; the matching wait
+  // (after TIP) comes before any peer touches this CTA's shared memory.  A
+  // relaxed arrive does not wait for this thread's loads still in flight.
+  cluster_arrive_relaxed();
   __syncthreads();
+  STEP_TRACE(12);
+  {
+    const StepHdr& hd = ms->hdr;
+    len = hd.len;
+    m_pos = hd.m_pos;
+    t_new = hd.t_new;
+    bad = bad || hd.bad != 0;
+    t0 = hd.t0;
+    nloc = hd.nloc;
+    nloc_s = hd.nloc_s;
+    ntiles = hd.ntiles;
+    nfc = hd.nfc;
+  }
+  const int k_eff = min(p.budget, len);
+  const bool need_select = len > p.budget;
+  const int t1 = t0 + nloc;
+  const bool own_new = t_new >= t0 && t_new < t1;
+
   float s_new = 0.f;
   if (own_new)  // (uh: the RoPE table, then this scratch)
     s_new = append_own_token<D>(turns, kn, vn, t_new,
@@ -1077,31 +1132,32 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     if (fslot) return (int)(0xFFFFFFFFu - (uint32_t)fslot[i]);
     return rows[i];
   };
-  // Gathers chunks [c0, c0 + nc) of row i's K then V (CPR chunks each) into
-  // its group's slot: group g belongs to warp g % FNW, its slot (g / FNW) mod
-  // fac_wst (the slots are reused in turn); chunk c of a row sits at
-  // chunk position c ^ (row & 7) so the eight rows an ldmatrix reads fall in
+  // Row gathers: a warp copies RPI rows per instruction, lane l the 16-byte
+  // chunk l % (2 CPR) of its row's K (the first CPR) then V, into the row's
+  // group slot: group g belongs to warp g % FNW, its slot (g / FNW) mod
+  // fac_wst (the slots are reused in turn); chunk c of a row sits at chunk
+  // position c ^ (row & 7) so the eight rows an ldmatrix reads fall in
   // distinct banks.  Rows past fr_n are zero-filled: the tensor cores
   // multiply them by zero weights, which must not meet stale NaNs.
-  auto row_chunks = [&](int i, int c0, int nc) {
+  constexpr int LPR = 2 * CPR;   // lanes per row
+  constexpr int RPI = 32 / LPR;  // rows per warp instruction
+  static_assert(RPI >= 1 && RPI * LPR == 32 && GR % RPI == 0, "row gather lanes");
+  const int g_sub = lane / LPR, g_cc = lane - g_sub * LPR;
+  const int g_kv = g_cc >= CPR ? 1 : 0, g_ch = g_cc - g_kv * CPR;
+  auto row_copy = [&](int i) {  // this lane's chunk of row i
     const int g = i / GR, rr = i & (GR - 1);
-    const uint32_t st0 =
-        smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B + rr * ROWB;
+    const uint32_t dst = smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B +
+                         (uint32_t)(g_kv * GR + rr) * ROWB + (uint32_t)((g_ch ^ (rr & 7)) << 4);
     const bool real = i < fr_n;
     const size_t off = real ? (size_t)row_token(i) * D : 0;
-#pragma unroll 1
-    for (int c = c0; c < c0 + nc; ++c) {
-      const int which = c >= CPR, ch = c - which * CPR;
-      cp_async16_zfill(st0 + which * GR * ROWB + ((ch ^ (rr & 7)) << 4), (which ? Vb : Kb) + off + ch * (16 / ES),
-                       real ? 16u : 0u);
-    }
+    cp_async16_zfill(dst, (g_kv ? Vb : Kb) + off + g_ch * (16 / ES), real ? 16u : 0u);
   };
-  // the first fac_wst groups of every warp, issued by the whole CTA: four
-  // threads per row, each a quarter of its chunks
-  auto fac_start = [&]() {
+  // the first fac_wst groups of every FAC warp, by warps w, w + 1, .. (nw
+  // of them), RPI rows per warp and step
+  auto fac_start = [&](int w, int nw) {
     const int nfirst = min((fr_n + GR - 1) / GR * GR, p.fac_wst * FNW * GR);
 #pragma unroll 1
-    for (int i = tid >> 2; i < nfirst; i += SNT / 4) row_chunks(i, (tid & 3) * (CPR / 2), CPR / 2);
+    for (int i0 = w * RPI; i0 < nfirst; i0 += nw * RPI) row_copy(i0 + g_sub);
     cp_async_commit();
   };
 
@@ -1122,6 +1178,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     if (r1 < nloc) {
       if (warp == 0) warp_find_d0(hist, ms->chist, r1, ms);
       __syncthreads();
+      STEP_TRACE(23);
       R1.thr = (uint32_t)ms->dig << 20;
       if (ms->gt + ms->bucket > p.cap1) R1 = local_rule(r1, p.cap1, true, scr, nloc, hist, ms);
     }
@@ -1129,12 +1186,6 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     n1 = R1.need == INT_MAX ? list_rule_t<false>(R1, scr, nloc, t0, own1 + 2, p.cap1, ms)
                             : list_rule_any(R1, scr, nloc, t0, own1 + 2, p.cap1, ms);
     STEP_TRACE(3);
-    if (spec) {  // gather the listed rows now; the selection only masks them
-      fslot = own1 + 2;
-      contig = false;
-      fr_n = n1;
-      fac_start();
-    }
     // the own slot goes to every peer as one bulk copy, completing on the
     // peer's first-exchange barrier
     // header: count, cut short, staging unusable, smallest and largest key
@@ -1147,22 +1198,57 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     if (warp == 0 && lane < C && lane != (int)crank)
       bulk_s2cluster(dsmem_map(smem_u32(own1), (uint32_t)lane), smem_u32(own1), (uint32_t)stride1 * 8u,
                      dsmem_map(smem_u32(&bars[SB_X1]), (uint32_t)lane));
-    if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_X1]), 0u, xwait) && tid == 0) atomicOr(p.status, FASA_DEV_TIMEOUT);
-    STEP_TRACE(4);
-    // (only a timed-out wait leaves a stale count; the own slot may still be
-    // read by the outgoing copies and is left alone)
-    if (tid < C && tid != (int)crank)
-      slot_hdr(recv1, stride1, tid)->x = min(max(slot_hdr(recv1, stride1, tid)->x, 0), p.cap1);
+    STEP_TRACE(24);
+    // While the lists travel, the listed rows are gathered (the selection
+    // only masks them): by the warps past the first C when at least four
+    // are left over -- the union select then runs on warps 0..C-1 alone --
+    // else by every warp before the wait.
+    if (spec) {
+      fslot = own1 + 2;
+      contig = false;
+      fr_n = n1;
+    }
+    const int nuw = spec && C <= SNW - 4 ? C : SNW;  // warps of the union select
+    if (spec && nuw == SNW) fac_start(warp, SNW);
+    if (warp < nuw) {
+      // clear the union's histograms (the local one is spent; a second
+      // round rebuilds it)
+      uint4* z = reinterpret_cast<uint4*>(hist);
+      for (int i = tid; i < HLOC_BINS / 4; i += nuw * 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (warp == 0) {
+        ms->chist[lane] = 0u;
+        ms->chist[lane + 32] = 0u;
+        if (lane < C_MAX) ms->sel[lane] = 0;
+        if (lane == 0) {
+          ms->bkt_n = 0;
+          ms->hist_clobbered = 1;
+        }
+      }
+      STEP_TRACE(27);
+      if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_X1]), 0u, xwait) && tid == 0)
+        atomicOr(p.status, FASA_DEV_TIMEOUT);
+      STEP_TRACE(4);
+      // (only a timed-out wait leaves a stale count; the own slot may still
+      // be read by the outgoing copies and is left alone)
+      if (tid < C && tid != (int)crank)
+        slot_hdr(recv1, stride1, tid)->x = min(max(slot_hdr(recv1, stride1, tid)->x, 0), p.cap1);
+      named_bar_sync(4, nuw * 32);
+      STEP_TRACE(30);
+      const int total = __reduce_add_sync(0xffffffffu, lane < C ? slot_hdr(recv1, stride1, lane)->x : 0);
+      if (total >= k_eff) union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms->chist, ms, nuw);
+    } else {
+      fac_start(warp - nuw, SNW - nuw);
+    }
     __syncthreads();
-    STEP_TRACE(30);
     // lane r reads source r's header (every warp, so the result is everywhere)
     const int4 hd = lane < C ? *slot_hdr(recv1, stride1, lane) : make_int4(0, 0, 0, 0);
     const int total = __reduce_add_sync(0xffffffffu, hd.x);
     const bool any_unsafe = __any_sync(0xffffffffu, (hd.y & 2) != 0);
     bool valid = total >= k_eff;
     if (valid) {
-      theta = union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms);
-      if (tid == 0) ms->hist_clobbered = 1;
+      // a threshold bin of more than 32 entries (dense or tied keys): the
+      // radix search over the union, by every warp
+      theta = ms->bucket > 32 ? union_kth(recv1, stride1, p.cap1, C, k_eff, hist, ms) : ms->theta;
       // a source that cut its list short (and sent fewer than k) with every
       // entry selected could have left out a selected token
       const int selr = lane < C ? ms->sel[lane] : 0;
@@ -1214,7 +1300,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       fslot = nullptr;
       contig = false;
       fr_n = ms->n_rows;
-      if (big_ok) fac_start();
+      if (big_ok) fac_start(warp, SNW);
     }
   } else {
     // every cached token is attended: rows split evenly over the cluster.
@@ -1224,7 +1310,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     fr_r0 = (k_eff * (int)crank) / C;
     fr_n = (k_eff * ((int)crank + 1)) / C - fr_r0;
     contig = true;
-    if (big_ok) fac_start();
+    if (big_ok) fac_start(warp, SNW);
   }
   if (!big_ok) fr_n = 0;  // nothing was gathered: an empty record
   STEP_TRACE(7);
@@ -1339,7 +1425,10 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       // each half of its chunks (commits a group even when empty: the waits
       // count groups)
       const int gn = g + wst * FNW;
-      if (gn < ngrp) row_chunks(gn * GR + (lane >> 1), (lane & 1) * CPR, CPR);
+      if (gn < ngrp) {
+#pragma unroll 4
+        for (int r = 0; r < GR; r += RPI) row_copy(gn * GR + r + g_sub);
+      }
       cp_async_commit();
     }
     cp_async_wait<0>();
