@@ -1195,9 +1195,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
           make_int4(n1, (nloc > n1 ? 1 : 0) | (big_ok ? 0 : 2), (int)R1.thr, (int)ms->list_max);
     fence_proxy_async();  // the slot's generic writes, before the async proxy reads them
     __syncthreads();
-    if (warp == 0 && lane < C && lane != (int)crank)
-      bulk_s2cluster(dsmem_map(smem_u32(own1), (uint32_t)lane), smem_u32(own1), (uint32_t)stride1 * 8u,
-                     dsmem_map(smem_u32(&bars[SB_X1]), (uint32_t)lane));
+    if (lane == 0 && warp < C && warp != (int)crank)  // warp r sends to CTA r
+      bulk_s2cluster(dsmem_map(smem_u32(own1), (uint32_t)warp), smem_u32(own1), (uint32_t)stride1 * 8u,
+                     dsmem_map(smem_u32(&bars[SB_X1]), (uint32_t)warp));
     STEP_TRACE(24);
     // While the lists travel, the listed rows are gathered (the selection
     // only masks them): by the warps past the first C when at least four
@@ -1326,7 +1326,6 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   const int ngrp = (fr_n + GR - 1) / GR;
   const int nrec = min(FNW, ngrp);  // warps that attend rows
   float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
-  float* wts = rec + G_MAX * FNW * (D + 2);     // [G][FNW] + [G]
   cp_async_wait<0>();  // the CTA-wide first groups
   __syncthreads();
   if (warp < nrec) {
@@ -1471,43 +1470,36 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   // ---------------------------------------------------------------- combine
   // The G*D outputs are cut into C slices of sl float4 groups (the last one
   // shorter).  The records of the warps that attended rows are merged per
-  // head -- the head's maximum and the warp weights exp2(m_w - M) once, then
-  // one multiply-add per warp and element; no rows: m = -inf, l = 0 -- and
-  // written straight into the combine slots: slice r with (m, l) of every
-  // head goes to slot r of the staging (CTA r's share; this CTA's own share
-  // into its receive slot), each slot then one bulk copy to CTA r, which
-  // finishes slice r.
+  // head -- each thread takes the head's maximum M over the records and the
+  // weights exp2(m_w - M) itself, then one multiply-add per warp; no rows:
+  // m = -inf, l = 0 -- and written straight into the combine slots: slice r
+  // with (m, l) of every head goes to slot r of the staging (CTA r's share;
+  // this CTA's own share into its receive slot), each slot then one bulk
+  // copy to CTA r (issued by warp r), which finishes slice r.
   const int ngrp4 = G * (D / 4);
   const int sl = (ngrp4 + C - 1) / C;
   const int cs = p.comb_slot;  // bytes: sl float4, then G (m, l) float2 (padded)
   const float inv_sl = 1.f / (float)sl;
   unsigned char* crcv = smem + p.off_comb;      // [C][cs], slot r from CTA r
   unsigned char* csnd = smem + p.off_comb_snd;  // [C][cs], slot r for CTA r
-  if (big_ok && tid < G) {
-    const int g = tid;
-    float M = -CUDART_INF_F;
-#pragma unroll 1
-    for (int r = 0; r < nrec; ++r) M = fmaxf(M, rec[(g * FNW + r) * (D + 2) + D]);
-#pragma unroll 1
-    for (int r = 0; r < nrec; ++r) {
-      const float m_r = rec[(g * FNW + r) * (D + 2) + D];
-      wts[g * FNW + r] = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
-    }
-    wts[G * FNW + g] = M;
-  }
-  __syncthreads();
 #pragma unroll 1
   for (int x = tid; x < G * (D + 2); x += SNT) {
     const int g = x / (D + 2), e = x - g * (D + 2);
     float val = e == D ? -CUDART_INF_F : 0.f;
-    if (big_ok) {
-      val = wts[G * FNW + g];
-      if (e != D) {
+    if (big_ok && nrec > 0) {
+      const float* rg = rec + g * FNW * (D + 2);
+      float M = -CUDART_INF_F;
+#pragma unroll 1
+      for (int r = 0; r < nrec; ++r) M = fmaxf(M, rg[r * (D + 2) + D]);
+      if (e == D) {
+        val = M;
+      } else {  // (e == D + 1: the record's l)
         float acc = 0.f;
 #pragma unroll 1
         for (int r = 0; r < nrec; ++r) {
-          const float w = wts[g * FNW + r];
-          if (w != 0.f) acc += w * rec[(g * FNW + r) * (D + 2) + e];
+          const float m_r = rg[r * (D + 2) + D];
+          const float w = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
+          acc = fmaf(w, rg[r * (D + 2) + e], acc);
         }
         val = acc;
       }
@@ -1526,9 +1518,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   fence_proxy_async();  // the staging's generic writes, before the async proxy reads them
   __syncthreads();
   STEP_TRACE(28);
-  if (warp == 0 && lane < C && lane != (int)crank)
-    bulk_s2cluster(dsmem_map(smem_u32(crcv + crank * cs), (uint32_t)lane), smem_u32(csnd + lane * cs), (uint32_t)cs,
-                   dsmem_map(smem_u32(&bars[SB_COMB]), (uint32_t)lane));
+  if (lane == 0 && warp < C && warp != (int)crank)
+    bulk_s2cluster(dsmem_map(smem_u32(crcv + crank * cs), (uint32_t)warp), smem_u32(csnd + warp * cs), (uint32_t)cs,
+                   dsmem_map(smem_u32(&bars[SB_COMB]), (uint32_t)warp));
   STEP_TRACE(29);
   if (!mbar_wait_cluster_bounded(smem_u32(&bars[SB_COMB]), 0u, xwait) && tid == 0) atomicOr(p.status, FASA_DEV_TIMEOUT);
   STEP_TRACE(10);
