@@ -324,6 +324,10 @@ int plan_and_launch(Params& p, const fasa_dims_t* d, int flags, void* ws, size_t
 // staging, the second-round receive slots and the warp records.
 //
 // Returns FASA_OK, or FASA_ERR_UNSUPPORTED when it does not fit in `limit`.
+// floor(2^32 / d) (0xffffffff for d = 1): q = mulhi(n, m) is n / d or one
+// less for every n < 2^31, which one comparison corrects.
+uint32_t div_magic(uint32_t d) { return d <= 1 ? 0xffffffffu : (uint32_t)((1ull << 32) / d); }
+
 int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit) {
   const int D = d->head_dim, G = d->n_q_heads / d->n_kv_heads, nfc = d->n_tip, k = p.budget;
   constexpr int ES = 2;
@@ -434,6 +438,15 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.rows_cap = rows_cap;
   p.reload = reload;
   p.comb_slot = comb_slot;
+  p.comb_sl = sl;
+  p.comb_inv_sl = 1.f / (float)sl;
+  p.c_magic = div_magic((uint32_t)C);
+  p.tt_magic = div_magic((uint32_t)tile);
+  // with a first-round gather and at least four warps left over, the union
+  // select runs on warps 0..C-1 while the rest gather
+  p.u_nuw = (spec && C <= SNW - 4) ? C : SNW;
+  p.u_wps = std::max(1, p.u_nuw / C);
+  p.u_inv_wps = 1.f / (float)p.u_wps;
   p.off_recv2 = p.off_big;
   p.off_pt = p.off_big + fac_slots(wst);
   p.smem_total = p.off_big + big;

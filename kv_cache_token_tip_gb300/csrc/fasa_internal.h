@@ -112,6 +112,14 @@ struct StepParams {
   int rows_cap;    // capacity of the own-selection list
   int reload;      // copy workspace scores back into shared memory for the sweeps
   int comb_slot;   // bytes of one combine slot: an output slice and every head's (m, l)
+  int comb_sl;     // float4 groups of the output per slice (ceil(G D / 4 / C))
+  float comb_inv_sl;  // 1 / comb_sl (rounded)
+  // divisions by the cluster size and the TIP tile as a multiply-high by
+  // floor(2^32 / divisor) (0xffffffff for 1) and one correction step
+  uint32_t c_magic, tt_magic;
+  // the union select: warps taking part, and warps per source list
+  int u_nuw, u_wps;
+  float u_inv_wps;
   int off_bar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb, off_comb_snd,
       off_big, off_recv2, off_pt, smem_total;
 };

@@ -87,16 +87,16 @@ struct SelRule {
 
 #ifdef FASA_PHASE_TRACE
 // Tracing builds: lane 0 of every warp stores globaltimer (ns) in slot i and
-// clock64 in slot 32 + i of its 64-slot record; 32 slots per warp.
+// clock64 in slot 64 + i of its 128-slot record; 64 slots per warp.
 __device__ unsigned long long* g_step_trace;
-#define STEP_TRACE(i)                                                                                 \
-  do {                                                                                                \
-    if ((threadIdx.x & 31) == 0 && g_step_trace) {                                                    \
-      unsigned long long* tr_ =                                                                       \
-          g_step_trace + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * SNW + (threadIdx.x >> 5)) * 64; \
-      tr_[(i)] = global_timer_ns();                                                                   \
-      tr_[32 + (i)] = clock64();                                                                      \
-    }                                                                                                 \
+#define STEP_TRACE(i)                                                                                  \
+  do {                                                                                                 \
+    if ((threadIdx.x & 31) == 0 && g_step_trace) {                                                     \
+      unsigned long long* tr_ =                                                                        \
+          g_step_trace + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * SNW + (threadIdx.x >> 5)) * 128; \
+      tr_[(i)] = global_timer_ns();                                                                    \
+      tr_[64 + (i)] = clock64();                                                                       \
+    }                                                                                                  \
   } while (0)
 #else
 #define STEP_TRACE(i) \
@@ -105,6 +105,13 @@ __device__ unsigned long long* g_step_trace;
 #endif
 
 __device__ __forceinline__ int warp_sum_i(int v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// n / d for 0 <= n < 2^31 with m = floor(2^32 / d) (0xffffffff for d = 1):
+// the multiply-high is n / d or one less.
+__device__ __forceinline__ int div_magic(int n, int d, uint32_t m) {
+  int q = (int)__umulhi((uint32_t)n, m);
+  return q + (n - q * d >= d ? 1 : 0);
+}
 
 // 2^x by the hardware approximation (relative error ~2^-22; -inf -> +0):
 // the softmax weights need far less than that.
@@ -137,13 +144,9 @@ __device__ __forceinline__ int block_scan_s(int x, int* scratch, int& total) {
   }
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
-  int before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < SNW; ++w) {
-    const int s = scratch[w];
-    before += (w < warp) ? s : 0;
-    tot += s;
-  }
+  const int cw = lane < SNW ? scratch[lane] : 0;  // lane w: warp w's sum
+  const int tot = __reduce_add_sync(0xffffffffu, cw);
+  const int before = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0);
   __syncthreads();
   total = tot;
   return before + incl - x;
@@ -364,17 +367,15 @@ __device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc
       for (int t = 0; t < 4; ++t) cnt += sel[t];
     }
   }
+  STEP_TRACE(46);
   cnt = warp_sum_i(cnt);
   if (lane == 0) ms->scan[warp] = cnt;
   __syncthreads();
   STEP_TRACE(26);
-  int base = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < SNW; ++w) {
-    const int c = ms->scan[w];
-    base += w < warp ? c : 0;
-    total += c;
-  }
+  const int cw = lane < SNW ? ms->scan[lane] : 0;  // lane w: warp w's count
+  const int total = __reduce_add_sync(0xffffffffu, cw);
+  int base = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0);
+  STEP_TRACE(47);
   int tb = tie_base;
   uint32_t kmax = 0u;
 #pragma unroll 1
@@ -399,6 +400,7 @@ __device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc
         kmax = max(kmax, key[t]);
       }
   }
+  STEP_TRACE(48);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0 && kmax) atomicMax(&ms->list_max, kmax);
   __syncthreads();
@@ -584,7 +586,8 @@ __device__ __forceinline__ void warp_find_d0(const uint32_t* hist, const uint32_
 // cleared.  Stores per source the count of its entries >= theta in ms->sel.
 // Warps 0..nuw-1 call it (named barrier 4).
 __device__ __forceinline__ void union_select(const unsigned long long* recv, int stride, int cap, int C, int k,
-                                             uint32_t* hb, uint32_t* ch, StepMisc* ms, int nuw) {
+                                             uint32_t* hb, uint32_t* ch, StepMisc* ms, int nuw, int wps,
+                                             float inv_wps) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // lane r reads source r's header
   if (lane < C) {
@@ -596,14 +599,17 @@ __device__ __forceinline__ void union_select(const unsigned long long* recv, int
   }
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
+  STEP_TRACE(40);
   const uint32_t span = hi - lo;  // keys lie in [lo, hi]
   const int shift = max(0, (32 - __clz((int)(span | 1u))) - 12);
   // wps warps per source (at least one): a source's entries are split over
-  // its warps' lanes
-  const int wps = max(1, nuw / C);
-  const int sw = warp / wps, sl_ = (warp - sw * wps) * 32 + lane, sstride = wps * 32;
+  // its warps' lanes; warp / wps by the rounded reciprocal (exact: both
+  // are at most 16)
+  const int sw = __float2int_rz(((float)warp + 0.5f) * inv_wps);
+  const int sl_ = (warp - sw * wps) * 32 + lane, sstride = wps * 32;
+  const int sources_step = wps == 1 ? nuw : __float2int_rz(((float)nuw + 0.5f) * inv_wps);  // nuw / wps
 #pragma unroll 1
-  for (int r = sw; r < C; r += nuw / wps) {
+  for (int r = sw; r < C; r += sources_step) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
 #pragma unroll 1
@@ -613,16 +619,18 @@ __device__ __forceinline__ void union_select(const unsigned long long* recv, int
       atomicAdd(&ch[bin >> 6], 1u);
     }
   }
+  STEP_TRACE(42);
   named_bar_sync(4, nuw * 32);
   STEP_TRACE(25);
   if (warp == 0) warp_find_d0(hb, ch, k, ms);
+  STEP_TRACE(43);
   named_bar_sync(4, nuw * 32);
   STEP_TRACE(31);
   const uint32_t bs = (uint32_t)ms->dig;
   const int k_rem = k - ms->gt, nbk = ms->bucket;
   if (nbk > 32) return;  // (uniform) the caller runs the radix search
 #pragma unroll 1
-  for (int r = sw; r < C; r += nuw / wps) {
+  for (int r = sw; r < C; r += sources_step) {
     const unsigned long long* e = recv + (size_t)r * stride + 2;
     const int n = min(slot_hdr(recv, stride, r)->x, cap);
     int above = 0;
@@ -640,6 +648,7 @@ __device__ __forceinline__ void union_select(const unsigned long long* recv, int
     above = warp_sum_i(above);
     if (lane == 0 && above) atomicAdd(&ms->sel[r], above);
   }
+  STEP_TRACE(44);
   named_bar_sync(4, nuw * 32);
   STEP_TRACE(6);
   if (warp == 0) {
@@ -652,6 +661,7 @@ __device__ __forceinline__ void union_select(const unsigned long long* recv, int
       if (rank < k_rem) atomicAdd(&ms->sel[ms->bkt_src[lane]], 1);
     }
   }
+  STEP_TRACE(45);
   named_bar_sync(4, nuw * 32);
 }
 
@@ -902,11 +912,11 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     // contiguous token range of this CTA, its start aligned to a k_dom
     // block; K_dom is streamed up to the new token, which its CTA scores
     // from registers
-    const int chunk = ((len + C - 1) / C + KB - 1) / KB * KB;
+    const int chunk = (div_magic(len + C - 1, C, p.c_magic) + KB - 1) / KB * KB;
     t0 = min(len, (int)crank * chunk);
     nloc = min(len, t0 + chunk) - t0;
     nloc_s = t_new >= t0 && t_new < t0 + nloc ? t_new - t0 : nloc;
-    ntiles = len > p.budget ? (nloc_s + tt - 1) / tt : 0;
+    ntiles = len > p.budget ? div_magic(nloc_s + tt - 1, tt, p.tt_magic) : 0;
     STEP_TRACE(20);
     if (lane == 0) {
       StepHdr& hd = ms->hdr;
@@ -1208,7 +1218,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       contig = false;
       fr_n = n1;
     }
-    const int nuw = spec && C <= SNW - 4 ? C : SNW;  // warps of the union select
+    const int nuw = p.u_nuw;  // warps of the union select
     if (spec && nuw == SNW) fac_start(warp, SNW);
     if (warp < nuw) {
       // clear the union's histograms (the local one is spent; a second
@@ -1235,7 +1245,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       named_bar_sync(4, nuw * 32);
       STEP_TRACE(30);
       const int total = __reduce_add_sync(0xffffffffu, lane < C ? slot_hdr(recv1, stride1, lane)->x : 0);
-      if (total >= k_eff) union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms->chist, ms, nuw);
+      if (total >= k_eff) union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms->chist, ms, nuw, p.u_wps, p.u_inv_wps);
     } else {
       fac_start(warp - nuw, SNW - nuw);
     }
@@ -1279,11 +1289,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       c = warp_sum_i(c);
       if (lane == 0) ms->scan2[warp] = c;
       __syncthreads();
-      int at = 0, n_sel = 0;
-      for (int w = 0; w < SNW; ++w) {
-        at += w < warp ? ms->scan2[w] : 0;
-        n_sel += ms->scan2[w];
-      }
+      const int cw = lane < SNW ? ms->scan2[lane] : 0;  // lane w: warp w's count
+      const int n_sel = __reduce_add_sync(0xffffffffu, cw);
+      int at = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0);
 #pragma unroll 1
       for (int e0b = e0; e0b < e1; e0b += 32) {
         const int e = e0b + lane;
@@ -1477,9 +1485,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   // this CTA's own share into its receive slot), each slot then one bulk
   // copy to CTA r (issued by warp r), which finishes slice r.
   const int ngrp4 = G * (D / 4);
-  const int sl = (ngrp4 + C - 1) / C;
+  const int sl = p.comb_sl;  // ceil(ngrp4 / C)
   const int cs = p.comb_slot;  // bytes: sl float4, then G (m, l) float2 (padded)
-  const float inv_sl = 1.f / (float)sl;
+  const float inv_sl = p.comb_inv_sl;
   unsigned char* crcv = smem + p.off_comb;      // [C][cs], slot r from CTA r
   unsigned char* csnd = smem + p.off_comb_snd;  // [C][cs], slot r for CTA r
 #pragma unroll 1
