@@ -403,8 +403,9 @@ def run_gpu(args):
     from kv_cache_token_tip_gb300 import build as kbuild
     kbuild.build()
     from kv_cache_token_tip_gb300 import (FASA_KERNEL_SINGLE_EXCHANGE, dims_for, fasa_apply_rope_q,
-                                          fasa_cluster_size, fasa_decode_step, fasa_dense_attention,
-                                          fasa_device_status, fasa_step_kernel, fasa_workspace_size)
+                                          fasa_cluster_size, fasa_decode_step, fasa_decode_step_split,
+                                          fasa_dense_attention, fasa_device_status, fasa_step_kernel,
+                                          fasa_workspace_size)
 
     rank, world, local, pg = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -428,13 +429,27 @@ def run_gpu(args):
     if args.replicas > 0:  # profiling runs only: fewer replicas may fit in L2
         R = args.replicas
     reps = make_replicas(cfg, R, dims)
+    split = args.fasa_m and not args.append
     if args.fasa_m:
-        # FASA-M placement: the K/V caches move to page-locked host memory
-        # (read in place by the row gather over the host link); K_dom stays
+        # FASA-M placement ("Hardware-Aware Variants"): the values and the
+        # keys' non-dominant FC pairs (K^nondom) in page-locked host memory,
+        # the dominant key cache K_dom on the GPU.  The split step moves only
+        # the selected rows' K^nondom and V over the host link and rebuilds
+        # each key with its K_dom pairs.  (The dense comparison, and the
+        # append step, read whole keys from host memory.)
+        from kv_cache_token_tip_gb300 import fasa_build_knondom
+        ndp = cfg.head_dim // 2 - cfg.n_tip
         for L, _ in reps:
+            if split:
+                L.knd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.context, 2 * ndp), dtype=L.k.dtype,
+                                    pin_memory=True)
+                fasa_build_knondom(L.k, L.dom_fc, None, L.knd, dims)
+                torch.cuda.synchronize()
             L.k = L.k.cpu().pin_memory()
             L.v = L.v.cpu().pin_memory()
         torch.cuda.empty_cache()
+        if fasa_device_status():
+            raise RuntimeError("K^nondom build reported bad input")
     B, Hq, H, d, k = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.budget
     ws_bytes = fasa_workspace_size(dims, k)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
@@ -461,6 +476,9 @@ def run_gpu(args):
             kn, vn, lens_m1 = app[i % R]
             fasa_decode_step_append(L.q, kn, vn, lens_m1, L.k, L.v, kd, L.dom_fc, kl, outs[i % R],
                                     None, None, ws, dims, stream=stream)
+        elif split:
+            fasa_decode_step_split(L.q, L.pos, L.knd, L.v, kd, L.dom_fc, L.seq_lens, kl, outs[i % R],
+                                   None, None, ws, dims, stream=stream)
         else:
             fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, kl, outs[i % R],
                              None, None, ws, dims, stream=stream)
@@ -688,12 +706,24 @@ def run_gpu(args):
                        "layers": layers,
                        "entry": "fasa_decode_step_append (each step stores its own token)" if args.append
                                 else "fasa_decode_step",
-                       "kv_placement": "pinned host memory (FASA-M): selected rows cross the host link"
-                                       if args.fasa_m else "device memory",
+                       "kv_placement": ("FASA-M split keys: K^nondom and V in pinned host memory, K_dom on "
+                                        "the GPU; the selected rows' K^nondom and V cross the host link"
+                                        if split else
+                                        "pinned host memory (FASA-M): selected rows cross the host link"
+                                        if args.fasa_m else "device memory"),
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": per_step,
-            **({"fasa_m": {"link_bytes_per_step": int(round(model["fac"] * layers)),
-                           "link_gbs": round(model["fac"] * layers / sec_per_step / 1e9, 1),
+            **({"fasa_m": {"key_layout": "split" if split else "whole keys",
+                           # per selected row: d - 2 N_tip key elements and d value
+                           # elements over the link (whole keys: 2 d)
+                           "link_bytes_per_step": int(round(model["fac"] * layers * (
+                               (2 * cfg.head_dim - 2 * cfg.n_tip) / (2 * cfg.head_dim) if split else 1.0))),
+                           "link_bytes_whole_keys": int(round(model["fac"] * layers)),
+                           "pages_formula_bytes": int(cfg.batch * cfg.n_kv_heads * cfg.budget
+                                                      * (2 * cfg.head_dim - 2 * cfg.n_tip) * cfg.elem_bytes),
+                           "link_gbs": round(model["fac"] * layers * (
+                               (2 * cfg.head_dim - 2 * cfg.n_tip) / (2 * cfg.head_dim) if split else 1.0)
+                               / sec_per_step / 1e9, 1),
                            "hbm_bytes_not_held_per_replica": int(2 * reps[0][0].k.numel()
                                                                  * reps[0][0].k.element_size()),
                            # what one layer's step keeps in HBM (the library allocates

@@ -209,6 +209,38 @@ int fasa_decode_step(const void* q, const int32_t* pos,
                      const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
+ * FASA-M with split keys (same page, "Hardware-Aware Variants", FASA-M: the
+ * dominant key dims C_key^dom stay on the GPU, the non-dominant ones
+ * C_key^nondom and the values in CPU memory; after TIP only K^nondom_T and
+ * V_T cross the link, and the keys are rebuilt with K^dom_T).
+ *
+ * fasa_build_knondom writes C_key^nondom: for every token tau < seq_lens[b]
+ * (all tau < T_max when seq_lens is NULL), the FC pairs of
+ * k_cache[b,h,tau,:] outside the head's dominant set, in FC order:
+ * k_nondom[b,h,tau, 2p : 2p+2] = the p-th such pair, p < d/2 - N_tip
+ * (row stride d - 2 N_tip elements, stored dtype).  k_nondom may be
+ * page-locked host memory.  Every head must use exactly N_tip distinct FCs
+ * (no negative entries): another table sets FASA_DEV_BAD_INPUT and leaves
+ * the head's rows unwritten.  Nothing to do when N_tip = d/2.
+ *
+ * fasa_decode_step_split is fasa_decode_step with k_nondom in place of
+ * k_cache: the FAC gathers, per selected token, its k_nondom row (d - 2 N_tip
+ * elements) and its V row (d elements) -- typically from host memory -- and
+ * its N_tip dominant pairs from k_dom.  Same selection; the output equals
+ * the whole-key step's up to the summation order of q . k.  bf16 caches and
+ * N_tip a multiple of 4 (FASA_ERR_UNSUPPORTED otherwise); the FC table as
+ * for fasa_build_knondom (FASA_DEV_BAD_INPUT otherwise).
+ */
+int fasa_build_knondom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens,
+                       void* k_nondom, const fasa_dims_t* dims, fasa_stream_t stream);
+int fasa_decode_step_split(const void* q, const int32_t* pos,
+                           const void* k_nondom, const void* v_cache, const void* k_dom,
+                           const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget,
+                           float* out, int32_t* idx_out, int32_t* count_out,
+                           void* workspace, size_t workspace_bytes,
+                           const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
  * fasa_decode_step with the new token's cache maintenance fused in (the
  * FASA pages, "Hardware-Aware Variants": FASA-C keeps the dominant key cache
  * alongside the KV cache, so each decode step adds its own token to both).

@@ -593,6 +593,64 @@ __global__ void build_kdom_kernel(const T* K, const int* dom, const int* lens, T
   }
 }
 
+// K^nondom (FASA-M split keys): per token, the key's FC pairs outside the
+// head's dominant set, in FC order: [unit][T_max][d/2 - n] pairs.  A table
+// that is not n distinct FCs in range is reported (the layout cannot hold
+// it) and its row left unwritten.
+template <typename T>
+__global__ void build_knondom_kernel(const T* K, const int* dom, const int* lens, T* knd, int Hkv, int T_max, int D,
+                                     int n, int* status) {
+  using P = typename Pair<T>::type;
+  __shared__ uint8_t order[64];  // the non-dominant FCs in order
+  __shared__ int ok_s;
+  const int unit = blockIdx.y;
+  const int b = unit / Hkv, h = unit - b * Hkv;
+  const int npairs = D / 2, ndp = npairs - n;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t m0 = 0u, m1 = 0u;
+    bool ok = true;
+    for (int j = lane; j < n; j += 32) {
+      const int i = dom[h * n + j];
+      if (i < 0 || i >= npairs) ok = false;
+      else if (i < 32) m0 |= 1u << i;
+      else m1 |= 1u << (i - 32);
+    }
+    m0 = __reduce_or_sync(0xffffffffu, m0);
+    m1 = __reduce_or_sync(0xffffffffu, m1);
+    ok = __all_sync(0xffffffffu, ok) && __popc(m0) + __popc(m1) == n;
+    for (int f = lane; f < npairs; f += 32) {
+      const bool dm = f < 32 ? ((m0 >> f) & 1u) != 0u : ((m1 >> (f - 32)) & 1u) != 0u;
+      if (!dm) {
+        const int rank = f < 32 ? __popc(~m0 & ((1u << f) - 1u)) : __popc(~m0) + __popc(~m1 & ((1u << (f - 32)) - 1u));
+        if (rank < ndp) order[rank] = (uint8_t)f;
+      }
+    }
+    if (lane == 0) {
+      ok_s = ok;
+      if (!ok && blockIdx.x == 0) atomicOr(status, 1);
+    }
+  }
+  __syncthreads();
+  if (!ok_s) return;
+  int len = T_max;
+  if (lens) {
+    len = lens[b];
+    if (len < 0 || len > T_max) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, 1);
+      len = min(max(len, 0), T_max);
+    }
+  }
+  // thread x: pair x % ndp of token x / ndp of this block's tokens
+  const int tok0 = blockIdx.x * 64;
+  for (int x = threadIdx.x; x < 64 * ndp; x += blockDim.x) {
+    const int tau = tok0 + x / ndp, j = x - (x / ndp) * ndp;
+    if (tau >= len) continue;
+    const P* row = reinterpret_cast<const P*>(K + ((size_t)unit * T_max + tau) * D);
+    reinterpret_cast<P*>(knd)[((size_t)unit * T_max + tau) * ndp + j] = row[order[j]];
+  }
+}
+
 template <typename T>
 __global__ void append_kdom_kernel(const T* k_new, const int* dom, const int* tok_pos, T* kd, int Hkv, int T_max,
                                    int D, int n, int* status) {
@@ -616,6 +674,55 @@ __global__ void append_kdom_kernel(const T* k_new, const int* dom, const int* to
     }
     dst[(size_t)j * KDOM_BLOCK] = row[i];
   }
+}
+
+// fasa_decode_step and fasa_decode_step_split: keys whole in k_cache, or
+// (ksplit) their non-dominant pairs there and the dominant ones in k_dom.
+int decode_step_impl(const void* q, const int32_t* pos, const void* k_cache, const void* v_cache, const void* k_dom,
+                     const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget, float* out, int32_t* idx_out,
+                     int32_t* count_out, void* workspace, size_t workspace_bytes, const fasa_dims_t* dims,
+                     fasa_stream_t stream, bool ksplit) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q || !pos || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
+    return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  if (ksplit && (dims->dtype != FASA_BF16 || dims->n_tip % 4 != 0)) return FASA_ERR_UNSUPPORTED;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, budget);
+    sp.q = q;
+    sp.pos = pos;
+    sp.k_cache = k_cache;
+    sp.v_cache = v_cache;
+    sp.k_dom = k_dom;
+    sp.dom_fc = dom_fc;
+    sp.seq_lens = seq_lens;
+    sp.out = out;
+    sp.idx_out = idx_out;
+    sp.count_out = count_out;
+    if (ksplit) sp.flags |= F_KSPLIT;
+    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.q = q;
+  p.pos = pos;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_dom = k_dom;
+  p.dom_fc = dom_fc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.idx_out = idx_out;
+  p.count_out = count_out;
+  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC;
+  if (idx_out || count_out) flags |= F_IDX_OUT;
+  if (ksplit) flags |= F_KSPLIT;
+  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -772,6 +879,30 @@ int fasa_build_kdom(const void* k_cache, const int32_t* dom_fc, const int32_t* s
   return e == cudaSuccess ? FASA_OK : cuda_fail(e);
 }
 
+int fasa_build_knondom(const void* k_cache, const int32_t* dom_fc, const int32_t* seq_lens, void* k_nondom,
+                       const fasa_dims_t* dims, fasa_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!k_cache || !dom_fc || !k_nondom) return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(k_nondom)) return FASA_ERR_INVALID_ARG;
+  if (dims->n_tip >= dims->head_dim / 2) return FASA_OK;  // no non-dominant pairs
+  DevInfo di;
+  st = device_info(&di);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(ceil_div(dims->t_max, 64), dims->batch * dims->n_kv_heads);
+  if (dims->dtype == FASA_F32)
+    build_knondom_kernel<float><<<grid, 256, 0, s>>>((const float*)k_cache, dom_fc, seq_lens, (float*)k_nondom,
+                                                     dims->n_kv_heads, dims->t_max, dims->head_dim, dims->n_tip,
+                                                     di.status);
+  else
+    build_knondom_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)k_cache, dom_fc, seq_lens,
+                                                             (__nv_bfloat16*)k_nondom, dims->n_kv_heads,
+                                                             dims->t_max, dims->head_dim, dims->n_tip, di.status);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FASA_OK : cuda_fail(e);
+}
+
 int fasa_append_kdom(const void* k_new, const int32_t* dom_fc, const int32_t* tok_pos, void* k_dom,
                      const fasa_dims_t* dims, fasa_stream_t stream) {
   int st = check_dims(dims);
@@ -870,44 +1001,16 @@ int fasa_decode_step(const void* q, const int32_t* pos, const void* k_cache, con
                      const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget, float* out, int32_t* idx_out,
                      int32_t* count_out, void* workspace, size_t workspace_bytes, const fasa_dims_t* dims,
                      fasa_stream_t stream) {
-  int st = check_dims(dims);
-  if (st) return st;
-  if (!q || !pos || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
-    return FASA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
-  if (step_kernel_applies(dims)) {
-    StepParams sp;
-    fill_step(sp, dims, budget);
-    sp.q = q;
-    sp.pos = pos;
-    sp.k_cache = k_cache;
-    sp.v_cache = v_cache;
-    sp.k_dom = k_dom;
-    sp.dom_fc = dom_fc;
-    sp.seq_lens = seq_lens;
-    sp.out = out;
-    sp.idx_out = idx_out;
-    sp.count_out = count_out;
-    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
-                              reinterpret_cast<cudaStream_t>(stream));
-    if (st != FASA_ERR_UNSUPPORTED) return st;
-  }
-  Params p;
-  fill_common(p, dims, budget, nullptr);
-  p.q = q;
-  p.pos = pos;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.k_dom = k_dom;
-  p.dom_fc = dom_fc;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.idx_out = idx_out;
-  p.count_out = count_out;
-  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC;
-  if (idx_out || count_out) flags |= F_IDX_OUT;
-  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return decode_step_impl(q, pos, k_cache, v_cache, k_dom, dom_fc, seq_lens, budget, out, idx_out, count_out,
+                          workspace, workspace_bytes, dims, stream, false);
+}
+
+int fasa_decode_step_split(const void* q, const int32_t* pos, const void* k_nondom, const void* v_cache,
+                           const void* k_dom, const int32_t* dom_fc, const int32_t* seq_lens, int32_t budget,
+                           float* out, int32_t* idx_out, int32_t* count_out, void* workspace, size_t workspace_bytes,
+                           const fasa_dims_t* dims, fasa_stream_t stream) {
+  return decode_step_impl(q, pos, k_nondom, v_cache, k_dom, dom_fc, seq_lens, budget, out, idx_out, count_out,
+                          workspace, workspace_bytes, dims, stream, true);
 }
 
 int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new, const int32_t* seq_lens,

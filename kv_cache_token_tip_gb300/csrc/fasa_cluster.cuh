@@ -61,6 +61,7 @@ struct Misc {
   uint32_t tip_done[4];  // per TIP stage: warps done with it so far (monotonic)
   int tip_last[4];       // per TIP stage: last tile issued into it (-1: none)
   int nfc;               // this head's dominant-FC count (its leading valid entries)
+  uint8_t fac_pair[64];  // F_KSPLIT: the FC of each pair position of a FAC key row
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc scratch too small");
 
@@ -153,6 +154,62 @@ __device__ __forceinline__ float2 rope_cos_sin(unsigned long long turns, int m) 
   float s, c;
   sincospif(x, &s, &c);
   return make_float2(c, s);
+}
+
+// FASA-M split keys ("FASA: Frequency-aware Sparse Attention", "Hardware-
+// Aware Variants": the dominant key dims stay in device memory, the others
+// sit with V in host memory).  A key's FAC row is laid out as its
+// non-dominant FC pairs in FC order (the k_nondom row, ndp = d/2 - n pairs),
+// then its n dominant pairs in the order of the head's FC table (from
+// K_dom); the query is laid out alike, so q . k is unchanged.  One warp
+// fills fac_pair[p] = the FC whose pair sits at position p of that row.
+// Returns (every lane) whether the table holds n distinct FCs in range --
+// the only tables the split layout can represent.
+__device__ __forceinline__ bool split_pairs(const int* dom, int n, int npairs, uint8_t* fac_pair) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m0 = 0u, m1 = 0u;
+  bool ok = true;
+  for (int j = lane; j < n; j += 32) {
+    const int i = dom[j];
+    if (i < 0 || i >= npairs) {
+      ok = false;
+    } else if (i < 32) {
+      m0 |= 1u << i;
+    } else {
+      m1 |= 1u << (i - 32);
+    }
+  }
+  m0 = __reduce_or_sync(0xffffffffu, m0);
+  m1 = __reduce_or_sync(0xffffffffu, m1);
+  ok = __all_sync(0xffffffffu, ok) && __popc(m0) + __popc(m1) == n;
+  const int ndp = npairs - n;
+  for (int f = lane; f < npairs; f += 32) {
+    const bool dominant = f < 32 ? ((m0 >> f) & 1u) != 0u : ((m1 >> (f - 32)) & 1u) != 0u;
+    if (!dominant) {
+      const int rank = f < 32 ? __popc(~m0 & ((1u << f) - 1u))
+                              : __popc(~m0) + __popc(~m1 & ((1u << (f - 32)) - 1u));
+      if (rank < ndp) fac_pair[rank] = (uint8_t)f;
+    }
+  }
+  for (int j = lane; j < n; j += 32) fac_pair[ndp + j] = (uint8_t)min(max(dom[j], 0), npairs - 1);
+  return ok;
+}
+
+// 16-byte chunk ch of the split FAC row of token t (bf16): chunks below
+// ndp / 4 from the token's k_nondom row (ndp pairs, a multiple of four),
+// the others four dominant pairs from the unit's K_dom.  Zero-filled when
+// the row is not real (t must still lie in the unit).
+__device__ __forceinline__ void split_key_chunk(uint32_t dst, const __nv_bfloat16* knd_unit,
+                                                const __nv_bfloat16* kd_unit, int ndp, int n, int t, int ch,
+                                                bool real) {
+  if (4 * ch < ndp) {
+    cp_async16_zfill(dst, knd_unit + (size_t)t * 2 * ndp + ch * 8, real ? 16u : 0u);
+  } else {
+    const __nv_bfloat16* src =
+        kd_unit + ((size_t)(t / KDOM_BLOCK) * n + (4 * ch - ndp)) * KDOM_BLOCK * 2 + (t % KDOM_BLOCK) * 2;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) cp_async4_zfill(dst + 4u * u, src + u * KDOM_BLOCK * 2, real ? 4u : 0u);
+  }
 }
 
 // Loads EPL consecutive elements of a K or V row from shared memory as fp32.
@@ -295,7 +352,7 @@ __device__ __forceinline__ void tip_tile(const unsigned char* st, int ntok, int 
 enum : int { KIND_STEP = 0, KIND_DENSE = 1, KIND_STAGE = 2 };
 
 __host__ __device__ constexpr int kind_flags(int kind, int flags) {
-  return kind == KIND_STEP ? (flags & (F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT | F_APPEND))
+  return kind == KIND_STEP ? (flags & (F_ROPE | F_TIP | F_SELECT | F_FAC | F_IDX_OUT | F_APPEND | F_KSPLIT))
          : kind == KIND_DENSE ? F_DENSE
                               : flags;
 }
@@ -466,6 +523,10 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   };
   if (tid == 0)
     for (int it = 0; it < min(ns, ntiles); ++it) tip_issue(it);
+  // F_KSPLIT: the FAC key rows' pair order (the last warp; read after the
+  // barriers that follow)
+  if (ES == 2 && (flags & F_KSPLIT) && warp == NW - 1)
+    bad = !split_pairs(p.dom_fc + h * nfc_max, nfc_max, D / 2, ms->fac_pair) || bad;
 
   // ------------------------------------------------------------ query prep
 #pragma unroll
@@ -611,8 +672,19 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   const uint2* fr_pairs = nullptr;
   int fr_n = 0, fr_r0 = 0;
   bool fr_contig = true, fac_started = false;
-  const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * D;
+  // F_KSPLIT (bf16): k_cache holds the keys' non-dominant pairs (ndp per token)
+  const bool ksplit = ES == 2 && (flags & F_KSPLIT) != 0;
+  const int ndp = D / 2 - p.n_tip;
+  const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * (ksplit ? 2 * ndp : D);
   const T* Vb = reinterpret_cast<const T*>(p.v_cache) + (size_t)unit * p.T_max * D;
+  const __nv_bfloat16* kd16 = reinterpret_cast<const __nv_bfloat16*>(p.k_dom) + (size_t)unit * p.n_tip * p.T_max * 2;
+  // one 16-byte chunk of row i (token tok) into dst: V, or K whole or split
+  auto kv_chunk = [&](uint32_t dst, int which, int ch, int tok, bool real) {
+    if (ksplit && !which)
+      split_key_chunk(dst, reinterpret_cast<const __nv_bfloat16*>(Kb), kd16, ndp, p.n_tip, tok, ch, real);
+    else
+      cp_async16_zfill(dst, (which ? Vb : Kb) + (size_t)tok * D + ch * (16 / ES), real ? 16u : 0u);
+  };
   auto row_token = [&](int i) -> int {
     if (fr_contig) return fr_r0 + i;
     if (fr_pairs) return (int)(fr_pairs[i].y & 0x7FFFFFFFu);
@@ -662,9 +734,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         const int which = rem >= CPR, ch = rem - which * CPR;
         const int i = g * GR + rr;
         const bool real = i < fr_n;
-        const size_t row_off = real ? (size_t)row_token(i) * D : 0;
-        cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
-                         (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
+        kv_chunk(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16), which, ch, real ? row_token(i) : 0,
+                 real);
       }
     }
     cp_async_commit();
@@ -681,9 +752,8 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         const int g = i / GR, rr = i - g * GR;  // group g: warp g % NW, slot g / NW
         const uint32_t st0 = smem_u32(big) + (uint32_t)((g % NW) * p.fac_wst + g / NW) * GSLOT_B;
         const bool real = i < fr_n;
-        const size_t row_off = real ? (size_t)row_token(i) * D : 0;
-        cp_async16_zfill(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16),
-                         (which ? Vb : Kb) + row_off + ch * (16 / ES), real ? 16u : 0u);
+        kv_chunk(st0 + which * GR * ROWB + rr * ROWB + ((ch ^ (rr & 7)) * 16), which, ch, real ? row_token(i) : 0,
+                 real);
       }
       cp_async_commit();
     } else {
@@ -1209,8 +1279,9 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           const int d0 = ks * 16 + 2 * tq + hb * 8;
-          const float x0 = gq < G ? qrot[gq * D + d0] * qs : 0.f;
-          const float x1 = gq < G ? qrot[gq * D + d0 + 1] * qs : 0.f;
+          const int ds = ksplit ? 2 * ms->fac_pair[d0 >> 1] : d0;  // the key rows' pair order
+          const float x0 = gq < G ? qrot[gq * D + ds] * qs : 0.f;
+          const float x1 = gq < G ? qrot[gq * D + ds + 1] * qs : 0.f;
           split_bf16(x0, x1, qb[ks][hb][0], qb[ks][hb][1]);
         }
       float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1

@@ -31,6 +31,8 @@ enum : int {
   F_IDX_IN = 1 << 6,   // selected rows come from p.idx_in / p.count_in
   F_DENSE = 1 << 7,    // attention over every cached row
   F_APPEND = 1 << 8,   // step: first append the new token (k_new, v_new) at index len
+  F_KSPLIT = 1 << 9,   // keys in two parts (FASA-M): k_cache holds each token's non-dominant
+                       // FC pairs (row of d - 2 n_tip elements), k_dom the dominant ones
 };
 
 struct Params {

@@ -73,6 +73,7 @@ struct StepMisc {
   int bkt_n;            // entries gathered from the union's threshold bucket
   unsigned long long theta;
   uint32_t chist[64];   // coarse histogram of the score keys (key >> 26)
+  uint8_t fac_pair[64];  // F_KSPLIT: the FC of each pair position of a FAC key row
   unsigned long long bkt[32];
   int bkt_src[32];
 };
@@ -998,6 +999,8 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     }
     STEP_TRACE(17);
   }
+  if ((p.flags & F_KSPLIT) && warp == SNW - 1)
+    bad = !split_pairs(p.dom_fc + h * nfc_max, nfc_max, D / 2, ms->fac_pair) || bad;
   __nv_bfloat162 kn = __float2bfloat162_rn(0.f), vn = kn;
   if (append && tid < D / 2) {  // (element-aligned inputs: two 2-byte loads each)
     const T* knp = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D + 2 * tid;
@@ -1130,7 +1133,10 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   bool second = false;  // the second exchange decided the selection
   int sel_before = 0;   // selected tokens of the lower-ranked CTAs
   const bool spec = p.spec != 0 && big_ok;
-  const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * D;
+  // F_KSPLIT: k_cache holds the keys' non-dominant pairs (ndp per token)
+  const bool ksplit = (p.flags & F_KSPLIT) != 0;
+  const int ndp = D / 2 - nfc_max;
+  const T* Kb = reinterpret_cast<const T*>(p.k_cache) + (size_t)unit * p.T_max * (ksplit ? 2 * ndp : D);
   const T* Vb = reinterpret_cast<const T*>(p.v_cache) + (size_t)unit * p.T_max * D;
   // FAC rows: fr_n rows, contiguous tokens fr_r0.. or a list -- the
   // first-round list itself (masked by theta) or the compact own selection
@@ -1159,8 +1165,11 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const uint32_t dst = smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B +
                          (uint32_t)(g_kv * GR + rr) * ROWB + (uint32_t)((g_ch ^ (rr & 7)) << 4);
     const bool real = i < fr_n;
-    const size_t off = real ? (size_t)row_token(i) * D : 0;
-    cp_async16_zfill(dst, (g_kv ? Vb : Kb) + off + g_ch * (16 / ES), real ? 16u : 0u);
+    const int tok = real ? row_token(i) : 0;
+    if (ksplit && !g_kv)
+      split_key_chunk(dst, Kb, kd_unit, ndp, nfc_max, tok, g_ch, real);
+    else
+      cp_async16_zfill(dst, (g_kv ? Vb : Kb) + (size_t)tok * D + g_ch * (16 / ES), real ? 16u : 0u);
   };
   // the first fac_wst groups of every FAC warp, by warps w, w + 1, .. (nw
   // of them), RPI rows per warp and step
@@ -1345,8 +1354,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         const int d0 = ks * 16 + 2 * tq + hb * 8;
-        const float x0 = gq < G ? qrot[gq * D + d0] * qs : 0.f;
-        const float x1 = gq < G ? qrot[gq * D + d0 + 1] * qs : 0.f;
+        const int ds = ksplit ? 2 * ms->fac_pair[d0 >> 1] : d0;  // the key rows' pair order
+        const float x0 = gq < G ? qrot[gq * D + ds] * qs : 0.f;
+        const float x1 = gq < G ? qrot[gq * D + ds + 1] * qs : 0.f;
         split_bf16(x0, x1, qb[ks][hb][0], qb[ks][hb][1]);
       }
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1

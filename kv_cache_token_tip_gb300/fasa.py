@@ -22,6 +22,7 @@ EXPORTS = [
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
     "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
     "fasa_select_dominant_fcs", "fasa_compound_agreement", "fasa_test_fault_injection", "fasa_step_kernel",
+    "fasa_build_knondom", "fasa_decode_step_split",
 ]
 
 
@@ -79,6 +80,9 @@ def lib():
             "fasa_step_kernel": ([dp, ctypes.POINTER(i32)], ctypes.c_int),
             "fasa_apply_rope_q": ([vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_build_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_build_knondom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
+            "fasa_decode_step_split": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
+                                       ctypes.c_int),
             "fasa_append_kdom": ([vp, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_tip_score": ([vp, vp, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_topk_select": ([vp, vp, i32, vp, vp, dp, vp], ctypes.c_int),
@@ -193,6 +197,31 @@ def fasa_build_kdom(k_cache, dom_fc, seq_lens, k_dom, dims: FasaDims, stream=Non
         _ptr(k_cache, _store_dtypes(), "k_cache"), _ptr(dom_fc, _i32(), "dom_fc"),
         _ptr(seq_lens, _i32(), "seq_lens"), _ptr(k_dom, _store_dtypes(), "k_dom"),
         ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_build_knondom(k_cache, dom_fc, seq_lens, k_nondom, dims: FasaDims, stream=None):
+    """The non-dominant key pairs of every token, in FC order (FASA-M split
+    keys); k_cache and k_nondom may live in page-locked host memory."""
+    _check("fasa_build_knondom", lib().fasa_build_knondom(
+        _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens"), _ptr(k_nondom, _store_dtypes(), "k_nondom", True),
+        ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_decode_step_split(q, pos, k_nondom, v_cache, k_dom, dom_fc, seq_lens, budget: int, out,
+                           idx_out=None, count_out=None, workspace=None, dims: FasaDims = None, stream=None):
+    """fasa_decode_step with the keys split: non-dominant pairs in k_nondom,
+    dominant ones in k_dom (FASA-M)."""
+    ws_bytes = 0
+    if workspace is not None and not isinstance(workspace, int):
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fasa_decode_step_split", lib().fasa_decode_step_split(
+        _ptr(q, _store_dtypes(), "q", True), _ptr(pos, _i32(), "pos", True),
+        _ptr(k_nondom, _store_dtypes(), "k_nondom", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
+        _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"),
+        _ptr(seq_lens, _i32(), "seq_lens", True), int(budget), _ptr(out, _f32(), "out", True),
+        _ptr(idx_out, _i32(), "idx_out", True), _ptr(count_out, _i32(), "count_out", True),
+        _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
 
 
 def fasa_append_kdom(k_new, dom_fc, tok_pos, k_dom, dims: FasaDims, stream=None):

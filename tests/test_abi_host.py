@@ -89,6 +89,19 @@ def test_null_and_misaligned_pointers_rejected(L):
     assert L.fasa_device_status(None, None) == 1
 
 
+def test_split_step_arguments_rejected_before_launch(L):
+    """FASA-M split keys: bf16 and N_tip a multiple of 4 only (the K^nondom
+    row must be whole 16-byte chunks), checked on the host."""
+    P = 0x10000  # never dereferenced: validation fails first
+    sp = L.fasa_decode_step_split
+    assert sp(P, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims(n_tip=6)), None) == 2
+    assert sp(P, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims(dtype=0)), None) == 2
+    assert sp(None, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
+    assert sp(P, P, P + 8, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
+    assert L.fasa_build_knondom(P, P, None, P + 2, ctypes.byref(_dims()), None) == 1
+    assert L.fasa_build_knondom(P, None, None, P, ctypes.byref(_dims()), None) == 1
+
+
 def test_calibration_arguments_rejected_before_launch(L):
     """The calibration entry points validate on the host: dims, null and
     misaligned pointers, K < 1, n_tip outside 1..d/2, a missing or short

@@ -4,13 +4,36 @@ pages).  The step reads the caches only in the row gather, so the results
 must equal the all-device run bit for bit; the append step must also land
 its row in host memory."""
 
+import types
+
 import numpy as np
 import pytest
 
-from tests.gpu_util import build_kdom, ensure_built
+import oracle as O
+from tests import parity as P
+from tests.gpu_util import build_kdom, ensure_built, oracle_unit
 from workload import configs, gpu_gen
 
 pytestmark = pytest.mark.gpu
+
+
+def _check_units(L, cfg, out, idx, cnt, units=None, budget=None):
+    """Each (batch, KV head) unit of a step's results against the oracle on
+    the stored inputs of layer-like L: the selected set (near-tie rule) and
+    the output over that set."""
+    k = cfg.budget if budget is None else budget
+    G = cfg.group
+    out, idx, cnt = (np.asarray(t.cpu().numpy() if hasattr(t, "cpu") else t) for t in (out, idx, cnt))
+    if units is None:
+        units = [(b, h) for b in range(cfg.batch) for h in range(cfg.n_kv_heads)]
+    for b, h in units:
+        ref = oracle_unit(L, b, h, k)
+        n = int(L.seq_lens_host[b])
+        assert cnt[b, h] == min(k, n)
+        mine = idx[b, h, :cnt[b, h]]
+        P.check_selection(mine, ref["scores"], k)
+        fac = O.focused_attention_unit(ref["q_rot"], ref["K"], ref["V"], mine)
+        P.check_output(out[b, h * G:(h + 1) * G], fac, cfg.dtype)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,17 +64,25 @@ def test_step_and_dense_with_host_caches(name, over):
     for K, V in ((L.k, L.v), (Kh, Vh)):
         out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
         idx = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.budget), dtype=torch.int32, device="cuda")
-        fasa_decode_step(L.q, L.pos, K, V, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, None, ws, dims)
+        cnt = torch.empty((cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device="cuda")
+        fasa_decode_step(L.q, L.pos, K, V, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, cnt, ws, dims)
         q_rot = torch.empty_like(out)
         fasa_apply_rope_q(L.q, L.pos, q_rot, dims)
         dense = torch.empty_like(out)
         fasa_dense_attention(q_rot, K, V, L.seq_lens, dense, dims)
         assert fasa_device_status() == 0
-        res.append((out.cpu(), idx.cpu(), dense.cpu()))
+        res.append((out.cpu(), idx.cpu(), dense.cpu(), cnt.cpu()))
+    # the host-placement run against the oracle, unit by unit
+    _check_units(L, cfg, res[1][0], res[1][1], res[1][3])
+    G = cfg.group
+    for b, h in ((0, 0), (cfg.batch - 1, cfg.n_kv_heads - 1)):
+        ref = oracle_unit(L, b, h, cfg.budget)
+        full = O.focused_attention_unit(ref["q_rot"], ref["K"], ref["V"], np.arange(int(L.seq_lens_host[b])))
+        P.check_output(res[1][2].numpy()[b, h * G:(h + 1) * G], full, cfg.dtype)
+    # and bit for bit the device-placement run
     assert torch.equal(res[0][1], res[1][1])
     assert torch.equal(res[0][0], res[1][0])
     assert torch.equal(res[0][2], res[1][2])
-    assert np.all(np.isfinite(res[1][0].numpy()))
 
 
 def test_append_step_with_host_caches():
@@ -73,10 +104,18 @@ def test_append_step_with_host_caches():
     outs = []
     for K, V, kd in ((Kd, Vd, kd_dev), (Kh, Vh, kd_host_run)):
         out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
-        fasa_decode_step_append(L.q, kn, vn, L.seq_lens, K, V, kd, L.dom_fc, cfg.budget, out, None, None, ws, dims)
+        idx = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.budget), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device="cuda")
+        fasa_decode_step_append(L.q, kn, vn, L.seq_lens, K, V, kd, L.dom_fc, cfg.budget, out, idx, cnt, ws, dims)
         assert fasa_device_status() == 0
-        outs.append(out.cpu())
-    assert torch.equal(outs[0], outs[1])
+        outs.append((out.cpu(), idx.cpu(), cnt.cpu()))
+    # the host run against the oracle over the appended caches: len + 1
+    # tokens, the query at position len
+    lens = L.seq_lens.cpu().numpy()
+    Lh = types.SimpleNamespace(cfg=cfg, q=L.q, k=Kh, v=Vh, seq_lens_host=lens + 1, pos_host=lens,
+                               dom_fc_host=L.dom_fc_host)
+    _check_units(Lh, cfg, *outs[1])
+    assert torch.equal(outs[0][0], outs[1][0])
     assert torch.equal(kd_dev, kd_host_run)
     assert torch.equal(Kd.cpu(), Kh) and torch.equal(Vd.cpu(), Vh)
 
@@ -140,5 +179,94 @@ def test_step_io_in_host_memory():
         torch.cuda.synchronize()
         assert fasa_device_status() == 0
         res.append((out.cpu(), idx.cpu(), cnt.cpu()))
+    L.seq_lens_host = L.seq_lens.cpu().numpy()
+    L.pos_host = L.pos.cpu().numpy()
+    _check_units(L, cfg, *res[1], units=[(0, 0), (0, 5), (1, 2), (1, 7)])
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+def _nondom_expected(L, cfg):
+    """K^nondom by hand: each token's non-dominant FC pairs in FC order."""
+    B, H, T, d = cfg.batch, cfg.n_kv_heads, cfg.context, cfg.head_dim
+    k16 = L.k.cpu().view(__import__("torch").int16).numpy().reshape(B, H, T, d // 2, 2)
+    out = np.empty((B, H, T, d // 2 - cfg.n_tip, 2), dtype=np.int16)
+    for h in range(H):
+        nd = np.setdiff1d(np.arange(d // 2), L.dom_fc_host[h])
+        out[:, h] = k16[:, h][:, :, nd, :]
+    return out
+
+
+@pytest.mark.parametrize("name,over", [("llama3_8b_ctx32k", dict(context=8192, batch=1)),
+                                       ("qwen25_7b_b8_ctx16k", dict(context=4096))])
+def test_split_keys_against_oracle(name, over):
+    """FASA-M with split keys: K^nondom and V in host memory, K^dom on the
+    GPU.  fasa_build_knondom writes exactly each token's non-dominant pairs;
+    the split step selects the same tokens as the whole-key step and its
+    output matches the oracle unit by unit."""
+    import torch
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_build_knondom, fasa_decode_step, fasa_decode_step_split,
+                                          fasa_device_status)
+    cfg = configs.CONFIGS[name].with_(**over)
+    L = gpu_gen.make_layer(cfg, 0)
+    dims = dims_for(cfg)
+    kd = build_kdom(L, dims)
+    ws = _ws(dims, cfg.budget)
+    ndp = cfg.head_dim // 2 - cfg.n_tip
+    knd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.context, 2 * ndp), dtype=torch.bfloat16).pin_memory()
+    fasa_build_knondom(L.k, L.dom_fc, None, knd, dims)
+    torch.cuda.synchronize()
+    assert fasa_device_status() == 0
+    want = _nondom_expected(L, cfg)
+    assert np.array_equal(knd.view(torch.int16).numpy().reshape(want.shape), want)
+    Vh = L.v.cpu().pin_memory()
+    res = []
+    for split in (False, True):
+        out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+        idx = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.budget), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device="cuda")
+        if split:
+            fasa_decode_step_split(L.q, L.pos, knd, Vh, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, cnt, ws, dims)
+        else:
+            fasa_decode_step(L.q, L.pos, L.k, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, idx, cnt, ws, dims)
+        torch.cuda.synchronize()
+        assert fasa_device_status() == 0
+        res.append((out.cpu(), idx.cpu(), cnt.cpu()))
+    assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+    _check_units(L, cfg, *res[1])
+    P.check_output(res[1][0].numpy(), res[0][0].numpy().astype(np.float64), cfg.dtype)
+
+
+def test_split_keys_cover_both_fused_kernels():
+    """The two cases above run on different fused kernels (the
+    single-exchange kernel and the cluster kernel)."""
+    from kv_cache_token_tip_gb300 import dims_for, fasa_step_kernel
+    kinds = {fasa_step_kernel(dims_for(configs.CONFIGS[n].with_(**o)))
+             for n, o in (("llama3_8b_ctx32k", dict(context=8192, batch=1)),
+                          ("qwen25_7b_b8_ctx16k", dict(context=4096)))}
+    assert len(kinds) == 2
+
+
+def test_split_keys_reject_what_the_layout_cannot_hold():
+    """A per-head FC table with unused slots cannot be split: the build and
+    the step report FASA_DEV_BAD_INPUT; an N_tip that is not a multiple of 4
+    is refused before any launch."""
+    import torch
+    from kv_cache_token_tip_gb300 import (FASA_DEV_BAD_INPUT, FasaError, dims_for, fasa_build_knondom,
+                                          fasa_decode_step_split, fasa_device_status)
+    cfg = configs.CONFIGS["llama3_8b_ctx32k_ragged_ntip"].with_(context=4096)
+    L = gpu_gen.make_layer(cfg, 0)
+    dims = dims_for(cfg)
+    kd = build_kdom(L, dims)
+    ndp = cfg.head_dim // 2 - cfg.n_tip
+    knd = torch.zeros((cfg.batch, cfg.n_kv_heads, cfg.context, 2 * ndp), dtype=torch.bfloat16, device="cuda")
+    fasa_device_status()
+    fasa_build_knondom(L.k, L.dom_fc, None, knd, dims)
+    assert fasa_device_status() & FASA_DEV_BAD_INPUT
+    out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
+    ws = _ws(dims, cfg.budget)
+    fasa_decode_step_split(L.q, L.pos, knd, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, ws, dims)
+    assert fasa_device_status() & FASA_DEV_BAD_INPUT
+    odd = dims_for(configs.CONFIGS["llama3_8b_ctx32k"].with_(context=4096, n_tip=6))
+    with pytest.raises(FasaError):
+        fasa_decode_step_split(L.q, L.pos, knd, L.v, kd, L.dom_fc, L.seq_lens, cfg.budget, out, None, None, ws, odd)
