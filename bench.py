@@ -35,6 +35,7 @@ from workload import configs, synth  # noqa: E402
 METRIC = "FASA decode-step µs and achieved HBM TB/s (TIP+top-k+FAC) at 32K ctx"
 DEFAULT_WORKLOAD = "llama3_8b_ctx32k"
 L2_BYTES = 129 * 1024 * 1024
+TRIAL_S = 2.0  # target length of one timed trial when --steps is not given
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["kv_cache_token_tip_gb300/csrc/fasa_step.cuh",
                   "kv_cache_token_tip_gb300/csrc/fasa_cluster.cuh",
@@ -498,16 +499,24 @@ def run_gpu(args):
     dense_step(0)
     torch.cuda.synchronize()
     chunk = R * max(1, 512 // R)
-    K, W = args.steps, args.warmup
-    KL = K * layers              # timed launches
+    W = args.warmup if args.warmup is not None else max(8, 2048 // layers)
     g_chunk = capture(step, chunk, stream)
-    rem = KL % chunk
-    g_rem = capture(step, rem, stream) if rem else None
     g_warm = capture(step, W * layers, stream) if W else None
     torch.cuda.synchronize()
-    if g_warm is not None:
-        with torch.cuda.stream(stream):
-            g_warm.replay()
+    # the warm-up, timed: without --steps, K is chosen so that one trial
+    # lasts about TRIAL_S (the same K on every rank)
+    wev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    with torch.cuda.stream(stream):
+        wev[0].record(stream)
+        (g_warm if g_warm is not None else g_chunk).replay()
+        wev[1].record(stream)
+    torch.cuda.synchronize()
+    warm_launches = W * layers if g_warm is not None else chunk
+    t_step = max_over_ranks(pg, wev[0].elapsed_time(wev[1])) / 1e3 / warm_launches * layers
+    K = args.steps if args.steps else int(min(200000, max(20, round(TRIAL_S / t_step))))
+    KL = K * layers              # timed launches
+    rem = KL % chunk
+    g_rem = capture(step, rem, stream) if rem else None
     torch.cuda.synchronize()
     status = fasa_device_status(stream)
     if status:
@@ -803,7 +812,7 @@ def run_calibrate(args):
 
     call(0)
     torch.cuda.synchronize()
-    K, W = args.steps, args.warmup
+    K, W = (args.steps or 2000), (args.warmup if args.warmup is not None else 64)
     chunk = R * max(1, 64 // R)
     g_chunk = capture(call, chunk, stream)
     rem = K % chunk
@@ -924,14 +933,15 @@ def run_reference(args):
         return None
     cfg = configs.CONFIGS[args.workload]
     cal = args.calibrate
-    cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps, args.warmup,
+    warm = args.warmup if args.warmup is not None else 3
+    cb = run_oracle_leg(cfg, args.cpu_seconds, args.steps or 10 ** 9, warm,
                         fn="oracle_ca_sample" if cal else "oracle_sample")
     val = cb["bytes"] / cb["seconds"] / 1e12
     per_step = cb["seconds"] / cb["steps_per_proc"]
     line = {
         "impl": "reference",
         "metric": CA_METRIC if cal else METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
-        "steps": cb["steps_per_proc"], "warmup": args.warmup,
+        "steps": cb["steps_per_proc"], "warmup": warm,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, host-generated)",
         "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.n_q_heads,
@@ -953,8 +963,10 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2048)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps per trial (default: as many as fill about %.0f s, at most 200000)" % TRIAL_S)
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps (default: 2048 launches' worth, at least 8 steps)")
     ap.add_argument("--impl", choices=["fasa", "reference"], default="fasa")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -972,7 +984,7 @@ def main(argv=None):
                     help="input replicas rotated through (0: enough to exceed 4x L2, as timing requires; "
                          "a smaller count is for profiler captures)")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
+    if args.warmup is not None and args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
