@@ -349,8 +349,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   off += ST_BARS * 8;
   p.off_misc = off;
   off += ST_MISC_BYTES;
-  p.off_qrot = off;
-  off += G * D * 4;
+  p.off_qrot = off;  // the rotated query, then the FAC's query fragments over it
+  off += std::max(G * D * 4, (D / 16) * 32 * 16);
   p.off_qbar = off;
   off += align_up(2 * nfc * 4, 16);
   p.off_hist = off;

@@ -408,6 +408,63 @@ __device__ __forceinline__ int list_rule_t(SelRule R, const float* scr, int nloc
   return min(total, cap);
 }
 
+// list_rule_t<false> in one sweep: each warp writes its selected entries,
+// in token order, to its own segment of `stage` (scap entries per warp),
+// then copies them to dst at its offset.  Returns -1 (every thread) when a
+// warp selected more than scap entries: the caller then runs the two-pass
+// listing.  Every thread calls it.
+__device__ __forceinline__ int list_rule_1p(SelRule R, const float* scr, int nloc, int t0, unsigned long long* dst,
+                                            int cap, StepMisc* ms, unsigned long long* stage, int scap) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int wlen = (((nloc + SNW - 1) / SNW) + 3) & ~3;
+  const int w0 = min(nloc, warp * wlen), w1 = min(nloc, w0 + wlen);
+  unsigned long long* seg = stage + (size_t)warp * scap;
+  int wc = 0;  // the warp's entries so far
+  uint32_t kmax = 0u;
+#pragma unroll 1
+  for (int tl0 = w0; tl0 < w1; tl0 += 128) {
+    const int tl = tl0 + lane * 4;
+    uint32_t key[4];
+    bool ok[4];
+    keys4(scr, tl, w1, key, ok);
+    bool sel[4];
+    int at = wc, n = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      sel[t] = ok[t] && key[t] >= R.thr;
+      const unsigned bs = __ballot_sync(0xffffffffu, sel[t]);
+      at += __popc(bs & lt);
+      n += __popc(bs);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (sel[t]) {
+        if (at < scap)
+          seg[at] = ((unsigned long long)key[t] << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)(t0 + tl + t));
+        ++at;
+        kmax = max(kmax, key[t]);
+      }
+    wc += n;
+  }
+  STEP_TRACE(46);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    ms->scan[warp] = wc;
+    if (kmax) atomicMax(&ms->list_max, kmax);
+  }
+  if (__syncthreads_or(wc > scap)) return -1;
+  STEP_TRACE(26);
+  const int cw = lane < SNW ? ms->scan[lane] : 0;  // lane w: warp w's count
+  const int total = __reduce_add_sync(0xffffffffu, cw);
+  const int base = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0);
+#pragma unroll 1
+  for (int i = lane; i < wc && base + i < cap; i += 32) dst[base + i] = seg[i];
+  STEP_TRACE(48);
+  __syncthreads();
+  return min(total, cap);
+}
+
 // list_rule_t for any rule, out of line (ties on the threshold key, second round).
 __device__ __noinline__ int list_rule_any(SelRule R, const float* scr, int nloc, int t0, unsigned long long* dst,
                                           int cap, StepMisc* ms) {
@@ -963,6 +1020,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     constexpr int TPQ = D / 2 / QW;
     static_assert(TPQ >= 1 && TPQ * QW == D / 2, "RoPE table share per query warp");
     if (lane < TPQ) turns[(warp - 2) * TPQ + lane] = p.rope_turns[(warp - 2) * TPQ + lane];
+    // F_KSPLIT: the FAC key rows' pair order, needed for the query fragments
+    if ((p.flags & F_KSPLIT) && warp == 2)
+      bad = !split_pairs(p.dom_fc + h * nfc_max, nfc_max, D / 2, ms->fac_pair) || bad;
     named_bar_sync(3, QW * 32);  // the table is complete
 #pragma unroll 1
     for (int k = 0; k < QPAIRS; ++k) {
@@ -997,10 +1057,33 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
         qbar[2 * qt + 1] = a1;
       }
     }
+    // The FAC's query operand, built here once and stored over the rotated
+    // query (the same 4 KB): lane (gq, tq) of an attending warp needs, per
+    // 16-column k-step ks, the log2(e)/sqrt(d)-scaled pairs at columns 2tq
+    // and 2tq + 8 (in the key rows' pair order) of head gq, each split into
+    // bf16 hi + lo.  Item (ks, lane) is one uint4 at [ks][lane].
+    {
+      constexpr int KSQ = D / 16;
+      static_assert(KSQ <= QW && KSQ * 32 * 16 <= G_MAX * D * 4, "query fragments: one item per query thread, "
+                                                                   "within the rotated query's bytes");
+      const float qs = 1.4426950408889634f * rsqrtf((float)D);
+      const int ks = qt >> 5, ln = qt & 31, gq = ln >> 2, tq = ln & 3;
+      uint32_t v[4] = {0u, 0u, 0u, 0u};
+      if (ks < KSQ) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int d0 = ks * 16 + 2 * tq + hb * 8;
+          const int ds = (p.flags & F_KSPLIT) ? 2 * ms->fac_pair[d0 >> 1] : d0;
+          const float x0 = gq < G ? qrot[gq * D + ds] * qs : 0.f;
+          const float x1 = gq < G ? qrot[gq * D + ds + 1] * qs : 0.f;
+          split_bf16(x0, x1, v[2 * hb], v[2 * hb + 1]);
+        }
+      }
+      named_bar_sync(3, QW * 32);  // every read of the rotated query is done
+      if (ks < KSQ) reinterpret_cast<uint4*>(qrot)[ks * 32 + ln] = make_uint4(v[0], v[1], v[2], v[3]);
+    }
     STEP_TRACE(17);
   }
-  if ((p.flags & F_KSPLIT) && warp == SNW - 1)
-    bad = !split_pairs(p.dom_fc + h * nfc_max, nfc_max, D / 2, ms->fac_pair) || bad;
   __nv_bfloat162 kn = __float2bfloat162_rn(0.f), vn = kn;
   if (append && tid < D / 2) {  // (element-aligned inputs: two 2-byte loads each)
     const T* knp = reinterpret_cast<const T*>(p.k_new) + (size_t)unit * D + 2 * tid;
@@ -1202,8 +1285,15 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       if (ms->gt + ms->bucket > p.cap1) R1 = local_rule(r1, p.cap1, true, scr, nloc, hist, ms);
     }
     STEP_TRACE(14);
-    n1 = R1.need == INT_MAX ? list_rule_t<false>(R1, scr, nloc, t0, own1 + 2, p.cap1, ms)
-                            : list_rule_any(R1, scr, nloc, t0, own1 + 2, p.cap1, ms);
+    // one sweep into per-warp segments of the idle staging when it is free
+    // (scores not reloaded there), else the two-pass listing
+    n1 = -1;
+    if (R1.need == INT_MAX && !p.reload && p.smem_total - p.off_big >= SNW * p.cap1 * 8)
+      n1 = list_rule_1p(R1, scr, nloc, t0, own1 + 2, p.cap1, ms, reinterpret_cast<unsigned long long*>(big),
+                        p.cap1);
+    if (n1 < 0)
+      n1 = R1.need == INT_MAX ? list_rule_t<false>(R1, scr, nloc, t0, own1 + 2, p.cap1, ms)
+                              : list_rule_any(R1, scr, nloc, t0, own1 + 2, p.cap1, ms);
     STEP_TRACE(3);
     // the own slot goes to every peer as one bulk copy, completing on the
     // peer's first-exchange barrier
@@ -1346,19 +1436,16 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   cp_async_wait<0>();  // the CTA-wide first groups
   __syncthreads();
   if (warp < nrec) {
-    const float qs = 1.4426950408889634f * rsqrtf((float)D);
     const int gq = lane >> 2, tq = lane & 3;
-    uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo]
+    uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo], built in the set-up
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int d0 = ks * 16 + 2 * tq + hb * 8;
-        const int ds = ksplit ? 2 * ms->fac_pair[d0 >> 1] : d0;  // the key rows' pair order
-        const float x0 = gq < G ? qrot[gq * D + ds] * qs : 0.f;
-        const float x1 = gq < G ? qrot[gq * D + ds + 1] * qs : 0.f;
-        split_bf16(x0, x1, qb[ks][hb][0], qb[ks][hb][1]);
-      }
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint4 f = reinterpret_cast<const uint4*>(qrot)[ks * 32 + lane];
+      qb[ks][0][0] = f.x;
+      qb[ks][0][1] = f.y;
+      qb[ks][1][0] = f.z;
+      qb[ks][1][1] = f.w;
+    }
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1
     float l0 = 0.f, l1 = 0.f;
     float oc[KS][4];
