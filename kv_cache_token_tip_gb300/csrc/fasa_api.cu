@@ -259,6 +259,7 @@ void fill_common(Params& p, const fasa_dims_t* d, int32_t budget, int* status) {
   fill_rope_turns(p, d);
   p.status = status;
   p.wait_ns = g_wait_ns;
+  p.drop_stage = g_drop_tip_tile;
 }
 
 // Plans and launches the cluster kernel.  Cluster size: the explicit

@@ -34,6 +34,7 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "../../include/fasa.h"
 #include "fasa_internal.h"
 #include "fasa_ptx.cuh"
 
@@ -54,6 +55,7 @@ struct Misc {
   int scan[NW];
   int scan2[NW];
   int tip_fail;          // a TIP stage wait ran out
+  int big_unsafe;        // a TIP copy did not land in time: `big` is not reused
   int bx_n;              // bucket entries received from the cluster (remote atomics)
   int bx_fail;           // set remotely by a CTA without a candidate list
   int bx_loc;            // this CTA's bucket entries
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     if (flags & F_SELECT) mbar_init(smem_u32(&bars[7]), 1);  // score reload
     fence_mbar_init();
     ms->tip_fail = 0;
+    ms->big_unsafe = 0;
     ms->bx_n = 0;
     ms->bx_fail = 0;
     ms->bx_loc = 0;
@@ -512,12 +515,14 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const uint32_t bar = smem_u32(&bars[s]);
     mbar_arrive_expect_tx(bar, (uint32_t)nblk * blk_bytes);
     const T* src = kd_unit + (size_t)(tau0 / KB) * nfc_max * KB * 2;
-    if (nfc == nfc_max) {
-      bulk_g2s(smem_u32(big + s * stage_bytes), src, (uint32_t)nblk * blk_bytes, bar);
-    } else {
-      for (int bi = 0; bi < nblk; ++bi)
-        bulk_g2s(smem_u32(big + s * stage_bytes + bi * blk_bytes), src + (size_t)bi * nfc_max * KB * 2, blk_bytes,
-                 bar);
+    if (it != p.drop_stage) {  // (test hook: one tile's copy left unissued)
+      if (nfc == nfc_max) {
+        bulk_g2s(smem_u32(big + s * stage_bytes), src, (uint32_t)nblk * blk_bytes, bar);
+      } else {
+        for (int bi = 0; bi < nblk; ++bi)
+          bulk_g2s(smem_u32(big + s * stage_bytes + bi * blk_bytes), src + (size_t)bi * nfc_max * KB * 2, blk_bytes,
+                   bar);
+      }
     }
     ms->tip_last[s] = it;
   };
@@ -651,14 +656,26 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   }
   if (__syncthreads_or(tip_fail | (ntiles > 0 ? ms->tip_fail : 0))) {
     if (tid == 0) {
-      atomicOr(p.status, 2);
-      // let copies still in flight land before the shared memory is reused
+      atomicOr(p.status, FASA_DEV_TIMEOUT);
+      // let copies still in flight land before the shared memory is reused;
+      // one that does not within one more bound (all stages together) is
+      // reported, and `big` is left alone for the rest of the launch
+      bool drained = true;
+      const uint64_t start = global_timer_ns();
       for (int s = 0; s < ns; ++s)
-        if (ms->tip_last[s] >= 0)
-          mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, p.wait_ns);
+        if (ms->tip_last[s] >= 0) {
+          const uint64_t spent = global_timer_ns() - start;
+          const uint64_t left = spent < p.wait_ns ? p.wait_ns - spent : 1ull;
+          drained &= mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)(ms->tip_last[s] / ns) & 1u, left);
+        }
+      if (!drained) {
+        atomicOr(p.status, FASA_DEV_UNDRAINED);
+        ms->big_unsafe = 1;
+      }
     }
     __syncthreads();
   }
+  const bool big_ok = ms->big_unsafe == 0;
 
   // ----------------------------------------------------- FAC row source
   // The attention rows of this CTA: fr_n rows, either contiguous tokens
@@ -741,6 +758,11 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     cp_async_commit();
   };
   auto fac_start = [&]() {
+    if (!big_ok) {  // nothing is gathered into unsafe staging: an empty record
+      fr_n = 0;
+      fac_started = true;
+      return;
+    }
     if constexpr (ES == 2) {
       // the first p.fac_wst groups of every warp are issued by the whole CTA
       // (a few rows per thread instead of up to 32 per warp); the FAC loop
@@ -781,7 +803,7 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
     const int nv = (nloc + 3) >> 2;  // score vectors (rows are padded to whole vectors)
     const int per_w = (nv + NW - 1) / NW;
     const int v0 = min(nv, warp * per_w), v1 = min(nv, v0 + per_w);
-    const bool reload = (read_sc || p.s_cap == 0) && nv > 0 && nv * 16 <= p.smem_total - p.off_big;
+    const bool reload = big_ok && (read_sc || p.s_cap == 0) && nv > 0 && nv * 16 <= p.smem_total - p.off_big;
     const uint32_t rbar = smem_u32(&bars[7]);
     if (reload) {
       if (!read_sc) fence_proxy_async_global();  // this thread's score stores, before the copy reads them
@@ -1262,7 +1284,13 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
         part[g * PSTRIDE + e] = val;
       }
     };
-    if constexpr (ES == 2) {
+    if (!big_ok) {
+      // the staging may still receive a late TIP copy: an empty record
+      for (int x = tid; x < G * PSTRIDE; x += NT) {
+        const int e = x % PSTRIDE;
+        part[x] = e == D ? -CUDART_INF_F : 0.f;
+      }
+    } else if constexpr (ES == 2) {
       // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
       // flash-decoding pass per warp over its own 16-row groups, no block
       // barriers: QK as S^T = K Q^T (16 rows x 8 heads), PV as O^T = V^T P^T

@@ -59,6 +59,7 @@ struct Params {
   float* out;               // [B,Hq,D] fp32
   int* status;              // device status word
   unsigned long long wait_ns;  // bound of every device wait
+  int drop_stage;           // test hook: this TIP tile's copy is never issued (-1: none)
   // shared-memory layout (bytes), computed by the host
   int s_cap;                // scores kept per CTA in shared memory (0: global)
   int tip_tile;             // tokens per TIP pipeline tile

@@ -26,13 +26,17 @@ def _built(cuda_ok):
     ensure_built()
 
 
-def _setup():
+# the two fused kernels: the single-exchange kernel at the 32K single-sequence
+# shape, the cluster kernel at batch 8 (32 units, clusters of fewer than 8)
+CASES = [("llama3_8b_ctx32k", {}, 1), ("qwen25_7b_b8_ctx16k", dict(context=4096), 0)]
+
+
+def _setup(name="llama3_8b_ctx32k", over=None, kernel=1):
     import torch
-    from kv_cache_token_tip_gb300 import FASA_KERNEL_SINGLE_EXCHANGE, dims_for, fasa_step_kernel, fasa_workspace_size
-    cfg = configs.CONFIGS["llama3_8b_ctx32k"]
+    from kv_cache_token_tip_gb300 import dims_for, fasa_step_kernel, fasa_workspace_size
+    cfg = configs.CONFIGS[name].with_(**(over or {}))
     dims = dims_for(cfg)
-    # the fault hook acts on the single-exchange kernel's TIP staging
-    assert fasa_step_kernel(dims) == FASA_KERNEL_SINGLE_EXCHANGE
+    assert fasa_step_kernel(dims) == kernel
     L = gpu_gen.make_layer(cfg, 0)
     kd = build_kdom(L, dims)
     n = fasa_workspace_size(dims, cfg.budget)
@@ -50,9 +54,10 @@ def _step(cfg, dims, L, kd, ws):
     return out, idx, cnt
 
 
-def test_short_wait_bound_alone_changes_nothing():
+@pytest.mark.parametrize("name,over,kernel", CASES)
+def test_short_wait_bound_alone_changes_nothing(name, over, kernel):
     from kv_cache_token_tip_gb300 import fasa_device_status, fasa_test_fault_injection
-    cfg, dims, L, kd, ws = _setup()
+    cfg, dims, L, kd, ws = _setup(name, over, kernel)
     fasa_device_status()
     out0, idx0, cnt0 = _step(cfg, dims, L, kd, ws)
     assert fasa_device_status() == 0
@@ -68,10 +73,11 @@ def test_short_wait_bound_alone_changes_nothing():
     assert np.array_equal(out1.cpu().numpy(), out0.cpu().numpy())
 
 
-def test_unissued_tip_copy_times_out_and_the_stream_stays_usable():
+@pytest.mark.parametrize("name,over,kernel", CASES)
+def test_unissued_tip_copy_times_out_and_the_stream_stays_usable(name, over, kernel):
     import torch
     from kv_cache_token_tip_gb300 import FASA_DEV_TIMEOUT, fasa_device_status, fasa_test_fault_injection
-    cfg, dims, L, kd, ws = _setup()
+    cfg, dims, L, kd, ws = _setup(name, over, kernel)
     fasa_device_status()
     out0, idx0, cnt0 = _step(cfg, dims, L, kd, ws)
     assert fasa_device_status() == 0
