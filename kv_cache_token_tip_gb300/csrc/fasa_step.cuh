@@ -712,7 +712,7 @@ __device__ __forceinline__ void union_select(const unsigned long long* recv, int
   if (warp == 0) {
     const unsigned long long x = lane < nbk ? ms->bkt[lane] : 0ull;  // (lanes >= nbk hold 0: never larger)
     int rank = 0;  // entries of the bin larger than x
-#pragma unroll 1
+#pragma unroll 8
     for (int i = 0; i < nbk; ++i) rank += ms->bkt[i] > x;
     if (lane < nbk) {
       if (rank == k_rem - 1) ms->theta = x;
@@ -1592,20 +1592,24 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const int g = x / (D + 2), e = x - g * (D + 2);
     float val = e == D ? -CUDART_INF_F : 0.f;
     if (big_ok && nrec > 0) {
+      // (unrolled over the at most FNW records, so the loads overlap)
       const float* rg = rec + g * FNW * (D + 2);
-      float M = -CUDART_INF_F;
-#pragma unroll 1
-      for (int r = 0; r < nrec; ++r) M = fmaxf(M, rg[r * (D + 2) + D]);
+      float mr[FNW], M = -CUDART_INF_F;
+#pragma unroll
+      for (int r = 0; r < FNW; ++r) {
+        mr[r] = r < nrec ? rg[r * (D + 2) + D] : -CUDART_INF_F;
+        M = fmaxf(M, mr[r]);
+      }
       if (e == D) {
         val = M;
       } else {  // (e == D + 1: the record's l)
         float acc = 0.f;
-#pragma unroll 1
-        for (int r = 0; r < nrec; ++r) {
-          const float m_r = rg[r * (D + 2) + D];
-          const float w = m_r != -CUDART_INF_F ? ex2_approx(m_r - M) : 0.f;
-          acc = fmaf(w, rg[r * (D + 2) + e], acc);
-        }
+#pragma unroll
+        for (int r = 0; r < FNW; ++r)
+          if (r < nrec) {
+            const float w = mr[r] != -CUDART_INF_F ? ex2_approx(mr[r] - M) : 0.f;
+            acc = fmaf(w, rg[r * (D + 2) + e], acc);
+          }
         val = acc;
       }
     }
@@ -1648,7 +1652,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const float2 ml =
         okq ? *reinterpret_cast<const float2*>(crcv + r * cs + sl * 16 + g * 8) : make_float2(-CUDART_INF_F, 0.f);
     float M = ml.x;
-    for (int o = lpg >> 1; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, lpg));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1)
+      if (o < lpg) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, lpg));
     const float w = (ml.x != -CUDART_INF_F) ? ex2_approx(ml.x - M) : 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (w != 0.f) {
@@ -1656,7 +1662,9 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
     }
     float L = w * ml.y;
-    for (int o = lpg >> 1; o >= 1; o >>= 1) {
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+      if (o >= lpg) continue;
       L += __shfl_xor_sync(0xffffffffu, L, o, lpg);
       acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o, lpg);
       acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o, lpg);
