@@ -1639,48 +1639,29 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   cluster_arrive_relaxed();
   STEP_TRACE(9);
 
-  // Finish this CTA's slice: lpg lanes per output group (the power of two
-  // >= C), lane r taking CTA r's record, reduced with width-lpg shuffles.
+  // Finish this CTA's slice: one thread per output element (4 per float4
+  // group), each merging the C CTA records of its head with the loads of
+  // all records in flight at once.
   const int q0 = min(ngrp4, (int)crank * sl), q1 = min(ngrp4, q0 + sl);
-  const int lpg = C <= 1 ? 1 : 1 << (32 - __clz(C - 1));
-  const int gpw = 32 / lpg;
 #pragma unroll 1
-  for (int qw = q0 + gpw * warp; qw < q1; qw += gpw * SNW) {  // warp-uniform bound
-    const int q = qw + lane / lpg, r = lane & (lpg - 1);
-    const bool okq = q < q1 && r < C;
-    const int g = okq ? q / (D / 4) : 0, e4 = okq ? q - g * (D / 4) : 0;
-    const float2 ml =
-        okq ? *reinterpret_cast<const float2*>(crcv + r * cs + sl * 16 + g * 8) : make_float2(-CUDART_INF_F, 0.f);
-    float M = ml.x;
+  for (int t = tid; t < 4 * (q1 - q0); t += SNT) {
+    const int q = q0 + (t >> 2), c4 = t & 3;
+    const int g = q / (D / 4), e = (q - g * (D / 4)) * 4 + c4;
+    float mr[C_MAX], M = -CUDART_INF_F;
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-      if (o < lpg) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, lpg));
-    const float w = (ml.x != -CUDART_INF_F) ? ex2_approx(ml.x - M) : 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (w != 0.f) {
-      const float4 v = *reinterpret_cast<const float4*>(crcv + r * cs + (q - q0) * 16);
-      acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+    for (int r = 0; r < C_MAX; ++r) {
+      mr[r] = r < C ? *reinterpret_cast<const float*>(crcv + r * cs + sl * 16 + g * 8) : -CUDART_INF_F;
+      M = fmaxf(M, mr[r]);
     }
-    float L = w * ml.y;
+    float L = 0.f, acc = 0.f;
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) {
-      if (o >= lpg) continue;
-      L += __shfl_xor_sync(0xffffffffu, L, o, lpg);
-      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o, lpg);
-      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o, lpg);
-      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o, lpg);
-      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o, lpg);
-    }
-    if (r == 0 && q < q1) {
-      if (L > 0.f) {
-        const float inv = 1.f / L;
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
+    for (int r = 0; r < C_MAX; ++r)
+      if (r < C && mr[r] != -CUDART_INF_F) {
+        const float w = ex2_approx(mr[r] - M);
+        L = fmaf(w, *reinterpret_cast<const float*>(crcv + r * cs + sl * 16 + g * 8 + 4), L);
+        acc = fmaf(w, *reinterpret_cast<const float*>(crcv + r * cs + (q - q0) * 16 + c4 * 4), acc);
       }
-      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G + g) * D + e4 * 4) = acc;
-    }
+    p.out[((size_t)b * p.Hq + (size_t)h * G + g) * D + e] = L > 0.f ? acc / L : 0.f;
   }
 
   // idx_out / count_out: the selected tokens of every CTA, concatenated in
