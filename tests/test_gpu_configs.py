@@ -130,3 +130,22 @@ def test_step_without_index_output(name):
     assert np.array_equal(o, o_idx)
     for (b, h) in [(0, 0), (cfg.batch - 1, cfg.n_kv_heads - 1)]:
         _check_unit(L, cfg, o, ix, cn, b, h)
+
+
+@pytest.mark.parametrize("over", [dict(dtype="bf16", context=8192, budget=256),
+                                  dict(dtype="bf16", context=8192, budget=256, batch=3)])
+def test_head_dim_64_bf16(over):
+    """bf16 with head_dim 64 (the tiny workload's shape, stored in bf16 at
+    8K tokens): the single-exchange kernel at batch 1 (clusters of 16) and
+    the cluster kernel or the single-exchange kernel at batch 3, every unit
+    against the oracle."""
+    from kv_cache_token_tip_gb300 import dims_for, fasa_step_kernel
+    cfg = configs.CONFIGS["tiny_fp32_ctx1k"].with_(**over)
+    L = gpu_gen.make_layer(cfg, 0)
+    dims = dims_for(cfg)
+    if cfg.batch == 1:
+        assert fasa_step_kernel(dims) == 1
+    o, ix, cn, _ = _run_step(L, cfg, dims)
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            _check_unit(L, cfg, o, ix, cn, b, h)
