@@ -264,6 +264,23 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             const fasa_dims_t* dims, fasa_stream_t stream);
 
 /*
+ * fasa_decode_step_append_split is fasa_decode_step_append over split keys
+ * (FASA-M, as fasa_decode_step_split): the rotated new key's non-dominant
+ * pairs go, in FC order, to k_nondom[b,h,t,:] (row stride d - 2 N_tip, as
+ * fasa_build_knondom writes it), its dominant pairs to k_dom, v_new to
+ * v_cache[b,h,t,:]; then the split step runs over the t + 1 tokens.  The
+ * rows written equal what fasa_build_knondom and fasa_build_kdom would
+ * write from the whole rotated key.  Same restrictions and errors as
+ * fasa_decode_step_split and fasa_decode_step_append.
+ */
+int fasa_decode_step_append_split(const void* q, const void* k_new, const void* v_new,
+                                  const int32_t* seq_lens, void* k_nondom, void* v_cache, void* k_dom,
+                                  const int32_t* dom_fc, int32_t budget,
+                                  float* out, int32_t* idx_out, int32_t* count_out,
+                                  void* workspace, size_t workspace_bytes,
+                                  const fasa_dims_t* dims, fasa_stream_t stream);
+
+/*
  * Offline calibration of the dominant FCs (the FASA pages: "The Functional
  * Sparsity Hypothesis and the Contextual Agreement (CA) Metric", Eq. 4, and
  * the calibration procedure, Algorithm 1).

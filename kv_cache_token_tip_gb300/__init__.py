@@ -14,7 +14,7 @@ from .fasa import (  # noqa: F401
     fasa_dense_attention,
     fasa_device_status, fasa_fc_agreement, fasa_fc_agreement_workspace_size,
     fasa_select_dominant_fcs, fasa_compound_agreement, fasa_test_fault_injection, fasa_step_kernel,
-    fasa_build_knondom, fasa_decode_step_split,
+    fasa_build_knondom, fasa_decode_step_split, fasa_decode_step_append_split,
     fasa_focused_attention, fasa_max_budget, fasa_tip_score, fasa_topk_select, fasa_workspace_size,
     lib, library_path,
 )

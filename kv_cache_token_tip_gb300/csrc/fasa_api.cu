@@ -726,6 +726,59 @@ int decode_step_impl(const void* q, const int32_t* pos, const void* k_cache, con
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+// fasa_decode_step_append and its split-key form (ksplit: k_cache holds the
+// keys' non-dominant pairs; the new token's are written there).
+int decode_append_impl(const void* q, const void* k_new, const void* v_new, const int32_t* seq_lens, void* k_cache,
+                       void* v_cache, void* k_dom, const int32_t* dom_fc, int32_t budget, float* out,
+                       int32_t* idx_out, int32_t* count_out, void* workspace, size_t workspace_bytes,
+                       const fasa_dims_t* dims, fasa_stream_t stream, bool ksplit) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
+    return FASA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
+  if (ksplit && (dims->dtype != FASA_BF16 || dims->n_tip % 4 != 0)) return FASA_ERR_UNSUPPORTED;
+  if (step_kernel_applies(dims)) {
+    StepParams sp;
+    fill_step(sp, dims, budget);
+    sp.flags = F_APPEND | (ksplit ? F_KSPLIT : 0);
+    sp.q = q;
+    sp.pos = seq_lens;
+    sp.k_new = k_new;
+    sp.v_new = v_new;
+    sp.k_cache = k_cache;
+    sp.v_cache = v_cache;
+    sp.k_dom = k_dom;
+    sp.dom_fc = dom_fc;
+    sp.seq_lens = seq_lens;
+    sp.out = out;
+    sp.idx_out = idx_out;
+    sp.count_out = count_out;
+    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (st != FASA_ERR_UNSUPPORTED) return st;
+  }
+  Params p;
+  fill_common(p, dims, budget, nullptr);
+  p.q = q;
+  p.pos = seq_lens;  // the query sits at the new token's position, len
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_dom = k_dom;
+  p.dom_fc = dom_fc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.idx_out = idx_out;
+  p.count_out = count_out;
+  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC | F_APPEND;
+  if (idx_out || count_out) flags |= F_IDX_OUT;
+  if (ksplit) flags |= F_KSPLIT;
+  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 // ============================================================================
@@ -1018,49 +1071,16 @@ int fasa_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache, void* k_dom, const int32_t* dom_fc, int32_t budget,
                             float* out, int32_t* idx_out, int32_t* count_out, void* workspace,
                             size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream) {
-  int st = check_dims(dims);
-  if (st) return st;
-  if (!q || !k_new || !v_new || !k_cache || !v_cache || !k_dom || !dom_fc || !seq_lens || !out || budget < 1)
-    return FASA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_dom) || !aligned16(out)) return FASA_ERR_INVALID_ARG;
-  if (step_kernel_applies(dims)) {
-    StepParams sp;
-    fill_step(sp, dims, budget);
-    sp.flags = F_APPEND;
-    sp.q = q;
-    sp.pos = seq_lens;
-    sp.k_new = k_new;
-    sp.v_new = v_new;
-    sp.k_cache = k_cache;
-    sp.v_cache = v_cache;
-    sp.k_dom = k_dom;
-    sp.dom_fc = dom_fc;
-    sp.seq_lens = seq_lens;
-    sp.out = out;
-    sp.idx_out = idx_out;
-    sp.count_out = count_out;
-    st = step_plan_and_launch(sp, dims, workspace, workspace_bytes, true, nullptr, nullptr,
-                              reinterpret_cast<cudaStream_t>(stream));
-    if (st != FASA_ERR_UNSUPPORTED) return st;
-  }
-  Params p;
-  fill_common(p, dims, budget, nullptr);
-  p.q = q;
-  p.pos = seq_lens;  // the query sits at the new token's position, len
-  p.k_new = k_new;
-  p.v_new = v_new;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.k_dom = k_dom;
-  p.dom_fc = dom_fc;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.idx_out = idx_out;
-  p.count_out = count_out;
-  int flags = F_ROPE | F_TIP | F_SELECT | F_FAC | F_APPEND;
-  if (idx_out || count_out) flags |= F_IDX_OUT;
-  return plan_and_launch(p, dims, flags, workspace, workspace_bytes, true, nullptr, nullptr,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return decode_append_impl(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, dom_fc, budget, out, idx_out,
+                            count_out, workspace, workspace_bytes, dims, stream, false);
+}
+
+int fasa_decode_step_append_split(const void* q, const void* k_new, const void* v_new, const int32_t* seq_lens,
+                                  void* k_nondom, void* v_cache, void* k_dom, const int32_t* dom_fc, int32_t budget,
+                                  float* out, int32_t* idx_out, int32_t* count_out, void* workspace,
+                                  size_t workspace_bytes, const fasa_dims_t* dims, fasa_stream_t stream) {
+  return decode_append_impl(q, k_new, v_new, seq_lens, k_nondom, v_cache, k_dom, dom_fc, budget, out, idx_out,
+                            count_out, workspace, workspace_bytes, dims, stream, true);
 }
 
 int fasa_fc_agreement_workspace_size(const fasa_dims_t* dims, size_t* bytes) {

@@ -571,23 +571,35 @@ __global__ void __launch_bounds__(NT, 1) fasa_cluster_kernel(const __grid_consta
   // position, store key and value at index t_new of the cache and the key's
   // dominant FCs in K_dom, and score it exactly as the TIP loop scores a
   // streamed token (same FC order, same accumulation; stored precision).
+  // With F_KSPLIT the key row is the token's k_nondom row: its non-dominant
+  // pairs in FC order (fac_pair positions below ndp).
   float s_new = 0.f;
   if (own_new) {
     float2* knew = reinterpret_cast<float2*>(stile);  // rotated key pairs, as stored
-    T* Kw = const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D;
+    const bool ksplit_w = ES == 2 && (flags & F_KSPLIT) != 0;
+    const int ndp_w = D / 2 - nfc_max;
+    T* Kw = const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) +
+            ((size_t)unit * p.T_max + t_new) * (ksplit_w ? 2 * ndp_w : D);
     T* Vw = const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D;
     if (tid < D / 2) {  // D / 2 <= NT
       const int i = tid;
       const float x0 = to_f32<T>(kn0), x1 = to_f32<T>(kn1);
       const float2 c = rope_cos_sin(p.rope_turns[i], t_new);
       const T r0 = from_f32<T>(x0 * c.x - x1 * c.y), r1 = from_f32<T>(x0 * c.y + x1 * c.x);
-      Kw[2 * i] = r0;
-      Kw[2 * i + 1] = r1;
+      if (!ksplit_w) {
+        Kw[2 * i] = r0;
+        Kw[2 * i + 1] = r1;
+      }
       Vw[2 * i] = vn0;
       Vw[2 * i + 1] = vn1;
       knew[i] = make_float2(to_f32<T>(r0), to_f32<T>(r1));
     }
     __syncthreads();
+    if (ksplit_w && tid < ndp_w) {
+      const float2 kp = knew[ms->fac_pair[tid]];
+      Kw[2 * tid] = from_f32<T>(kp.x);
+      Kw[2 * tid + 1] = from_f32<T>(kp.y);
+    }
     T* kdw = const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc_max * KB + (t_new % KB)) * 2;
     auto dom_at = [&](int j) { return min(max(p.dom_fc[h * nfc_max + j], 0), D / 2 - 1); };
     for (int j = tid; j < nfc; j += NT) {

@@ -770,13 +770,15 @@ __device__ __noinline__ bool reload_scores(const float* scw, int nloc, unsigned 
 // stored dtype) by position t_new, store key and value vn at index t_new of
 // the caches and the key's dominant FCs in K_dom (slot row kdw), and return
 // (thread 0) the token's TIP score computed exactly as the TIP loop scores a
-// streamed token: same FC order and accumulation, stored precision.
+// streamed token: same FC order and accumulation, stored precision.  With a
+// split key layout (fac_pair non-null) Kw is the token's k_nondom row and
+// takes only the ndp non-dominant pairs, in FC order (fac_pair[0, ndp)).
 // `scratch` holds D/2 float2.  Every thread calls it.
 template <int D>
 __device__ __noinline__ float append_own_token(const unsigned long long* turns, __nv_bfloat162 kn, __nv_bfloat162 vn,
                                                int t_new, __nv_bfloat16* Kw, __nv_bfloat16* Vw, __nv_bfloat16* kdw,
                                                const int* dom, int nfc, const float* qbar, bool score,
-                                               float2* scratch) {
+                                               float2* scratch, const uint8_t* fac_pair, int ndp) {
   using T = __nv_bfloat16;
   const int tid = threadIdx.x;
   if (tid < D / 2) {
@@ -784,13 +786,20 @@ __device__ __noinline__ float append_own_token(const unsigned long long* turns, 
     const float x0 = __low2float(kn), x1 = __high2float(kn);
     const float2 c = rope_cos_sin(turns[i], t_new);
     const T r0 = __float2bfloat16_rn(x0 * c.x - x1 * c.y), r1 = __float2bfloat16_rn(x0 * c.y + x1 * c.x);
-    Kw[2 * i] = r0;
-    Kw[2 * i + 1] = r1;
+    if (!fac_pair) {
+      Kw[2 * i] = r0;
+      Kw[2 * i + 1] = r1;
+    }
     Vw[2 * i] = __low2bfloat16(vn);
     Vw[2 * i + 1] = __high2bfloat16(vn);
     scratch[i] = make_float2(__bfloat162float(r0), __bfloat162float(r1));
   }
   __syncthreads();
+  if (fac_pair && tid < ndp) {
+    const float2 kp = scratch[fac_pair[tid]];
+    Kw[2 * tid] = __float2bfloat16_rn(kp.x);
+    Kw[2 * tid + 1] = __float2bfloat16_rn(kp.y);
+  }
   auto dom_at = [&](int j) { return min(max(dom[j], 0), D / 2 - 1); };
 #pragma unroll 1
   for (int j = tid; j < nfc; j += SNT) {
@@ -1120,13 +1129,18 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   const bool own_new = t_new >= t0 && t_new < t1;
 
   float s_new = 0.f;
-  if (own_new)  // (uh: the RoPE table, then this scratch)
+  if (own_new) {  // (uh: the RoPE table, then this scratch)
+    // a split key layout keeps ndp = D/2 - nfc_max pairs per k_nondom row
+    const bool ksplit_w = (p.flags & F_KSPLIT) != 0;
+    const int krow = ksplit_w ? D - 2 * nfc_max : D;
     s_new = append_own_token<D>(turns, kn, vn, t_new,
-                                const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * D,
+                                const_cast<T*>(reinterpret_cast<const T*>(p.k_cache)) + ((size_t)unit * p.T_max + t_new) * krow,
                                 const_cast<T*>(reinterpret_cast<const T*>(p.v_cache)) + ((size_t)unit * p.T_max + t_new) * D,
                                 const_cast<T*>(kd_unit) + ((size_t)(t_new / KB) * nfc_max * KB + (t_new % KB)) * 2,
                                 p.dom_fc + h * nfc_max, nfc, qbar, need_select,
-                                reinterpret_cast<float2*>(uh) + D / 2);
+                                reinterpret_cast<float2*>(uh) + D / 2, ksplit_w ? ms->fac_pair : nullptr,
+                                D / 2 - nfc_max);
+  }
   STEP_TRACE(1);
 
   // ---------------------------------------------------------------- TIP scan

@@ -22,7 +22,7 @@ EXPORTS = [
     "fasa_decode_step", "fasa_device_status", "fasa_cluster_size", "fasa_decode_step_noalloc",
     "fasa_decode_step_append", "fasa_fc_agreement_workspace_size", "fasa_fc_agreement",
     "fasa_select_dominant_fcs", "fasa_compound_agreement", "fasa_test_fault_injection", "fasa_step_kernel",
-    "fasa_build_knondom", "fasa_decode_step_split",
+    "fasa_build_knondom", "fasa_decode_step_split", "fasa_decode_step_append_split",
 ]
 
 
@@ -94,6 +94,8 @@ def lib():
             "fasa_decode_step_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, dp, vp], ctypes.c_int),
             "fasa_decode_step_append": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
                                         ctypes.c_int),
+            "fasa_decode_step_append_split": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, dp, vp],
+                                              ctypes.c_int),
             "fasa_fc_agreement_workspace_size": ([dp, ctypes.POINTER(sz)], ctypes.c_int),
             "fasa_fc_agreement": ([vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_compound_agreement": ([vp, vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
@@ -287,6 +289,23 @@ def fasa_decode_step_append(q, k_new, v_new, seq_lens, k_cache, v_cache, k_dom, 
         _ptr(q, _store_dtypes(), "q"), _ptr(k_new, _store_dtypes(), "k_new"),
         _ptr(v_new, _store_dtypes(), "v_new"), _ptr(seq_lens, _i32(), "seq_lens"),
         _ptr(k_cache, _store_dtypes(), "k_cache", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
+        _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"), int(budget),
+        _ptr(out, _f32(), "out"), _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
+        _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))
+
+
+def fasa_decode_step_append_split(q, k_new, v_new, seq_lens, k_nondom, v_cache, k_dom, dom_fc, budget: int, out,
+                                  idx_out=None, count_out=None, workspace=None, dims: FasaDims = None, stream=None):
+    """fasa_decode_step_append over split keys: the new token's non-dominant
+    pairs go to its k_nondom row, its dominant pairs to K_dom, v_new to
+    v_cache; then the split step attends over seq_lens[b] + 1 tokens."""
+    ws_bytes = 0
+    if workspace is not None and not isinstance(workspace, int):
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fasa_decode_step_append_split", lib().fasa_decode_step_append_split(
+        _ptr(q, _store_dtypes(), "q"), _ptr(k_new, _store_dtypes(), "k_new"),
+        _ptr(v_new, _store_dtypes(), "v_new"), _ptr(seq_lens, _i32(), "seq_lens"),
+        _ptr(k_nondom, _store_dtypes(), "k_nondom", True), _ptr(v_cache, _store_dtypes(), "v_cache", True),
         _ptr(k_dom, _store_dtypes(), "k_dom"), _ptr(dom_fc, _i32(), "dom_fc"), int(budget),
         _ptr(out, _f32(), "out"), _ptr(idx_out, _i32(), "idx_out"), _ptr(count_out, _i32(), "count_out"),
         _ptr(workspace, None, "workspace"), ws_bytes, ctypes.byref(dims), _stream(stream)))

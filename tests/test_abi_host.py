@@ -31,6 +31,7 @@ def test_header_declares_the_decode_path_calls():
     for name in ("fasa_apply_rope_q", "fasa_tip_score", "fasa_topk_select", "fasa_focused_attention",
                  "fasa_decode_step", "fasa_dense_attention", "fasa_build_kdom", "fasa_append_kdom",
                  "fasa_workspace_size", "fasa_device_status", "fasa_decode_step_append",
+                 "fasa_decode_step_split", "fasa_decode_step_append_split", "fasa_build_knondom",
                  "fasa_fc_agreement", "fasa_compound_agreement", "fasa_select_dominant_fcs"):
         assert name in syms
 
@@ -98,6 +99,11 @@ def test_split_step_arguments_rejected_before_launch(L):
     assert sp(P, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims(dtype=0)), None) == 2
     assert sp(None, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
     assert sp(P, P, P + 8, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
+    ap = L.fasa_decode_step_append_split
+    assert ap(P, P, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims(n_tip=6)), None) == 2
+    assert ap(P, P, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims(dtype=0)), None) == 2
+    assert ap(P, P, P, P, P + 8, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
+    assert ap(P, None, P, P, P, P, P, P, 256, P, None, None, None, 0, ctypes.byref(_dims()), None) == 1
     assert L.fasa_build_knondom(P, P, None, P + 2, ctypes.byref(_dims()), None) == 1
     assert L.fasa_build_knondom(P, None, None, P, ctypes.byref(_dims()), None) == 1
 

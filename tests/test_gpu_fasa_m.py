@@ -237,6 +237,59 @@ def test_split_keys_against_oracle(name, over):
     P.check_output(res[1][0].numpy(), res[0][0].numpy().astype(np.float64), cfg.dtype)
 
 
+@pytest.mark.parametrize("name,over,lens", [("llama3_8b_ctx32k", dict(context=8192, batch=2), (8000, 300)),
+                                            ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2), (4000, 1234))])
+def test_split_keys_append_against_oracle(name, over, lens):
+    """The append step over split keys: the new token's non-dominant pairs
+    land in its k_nondom row (host memory) exactly as fasa_build_knondom
+    would write them from the whole rotated key, its dominant pairs in K_dom
+    and its value in V exactly as the whole-key append writes them; the
+    selection equals the whole-key append step's and the output matches the
+    oracle over the appended caches unit by unit."""
+    import torch
+    from kv_cache_token_tip_gb300 import (dims_for, fasa_build_knondom, fasa_decode_step_append,
+                                          fasa_decode_step_append_split, fasa_device_status)
+    cfg = configs.CONFIGS[name].with_(**over)
+    L = gpu_gen.make_layer(cfg, 0)
+    L.seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    dims = dims_for(cfg)
+    kd_whole = build_kdom(L, dims)
+    kd_split = kd_whole.clone()
+    ws = _ws(dims, cfg.budget)
+    ndp = cfg.head_dim // 2 - cfg.n_tip
+    knd = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.context, 2 * ndp), dtype=torch.bfloat16).pin_memory()
+    fasa_build_knondom(L.k, L.dom_fc, None, knd, dims)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    shape = (cfg.batch, cfg.n_kv_heads, cfg.head_dim)
+    kn = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    vn = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    Kd, Vd = L.k.clone(), L.v.clone()
+    Vh = L.v.cpu().pin_memory()
+    res = []
+    for split in (False, True):
+        out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+        idx = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.budget), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device="cuda")
+        if split:
+            fasa_decode_step_append_split(L.q, kn, vn, L.seq_lens, knd, Vh, kd_split, L.dom_fc, cfg.budget, out, idx,
+                                          cnt, ws, dims)
+        else:
+            fasa_decode_step_append(L.q, kn, vn, L.seq_lens, Kd, Vd, kd_whole, L.dom_fc, cfg.budget, out, idx, cnt,
+                                    ws, dims)
+        torch.cuda.synchronize()
+        assert fasa_device_status() == 0
+        res.append((out.cpu(), idx.cpu(), cnt.cpu()))
+    assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+    assert torch.equal(kd_whole, kd_split)
+    assert torch.equal(Vd.cpu(), Vh)
+    want = _nondom_expected(types.SimpleNamespace(k=Kd, dom_fc_host=L.dom_fc_host), cfg)
+    assert np.array_equal(knd.view(torch.int16).numpy().reshape(want.shape), want)
+    n = np.asarray(lens)
+    Lh = types.SimpleNamespace(cfg=cfg, q=L.q, k=Kd.cpu(), v=Vh, seq_lens_host=n + 1, pos_host=n,
+                               dom_fc_host=L.dom_fc_host)
+    _check_units(Lh, cfg, *res[1])
+
+
 def test_split_keys_cover_both_fused_kernels():
     """The two cases above run on different fused kernels (the
     single-exchange kernel and the cluster kernel)."""
