@@ -422,8 +422,12 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
     if (fac_slots(w) + pt_bytes <= room) wst = w;
   if (!wst) return FASA_ERR_UNSUPPORTED;
   const int spec = (C > 1 && cap1 <= wst * FNW * GR) ? 1 : 0;
+  // the listed rows' scores, [G_MAX heads][cap1 + 8], beside the slots,
+  // then each attending warp's compacted selection (cap1 16-bit entries)
+  const int s_bytes = G_MAX * (cap1 + 8) * 4 + align_up((D / 16) * cap1 * 2, 16);
+  const int rfac = (spec && fac_slots(wst) + s_bytes <= room) ? 1 : 0;
   const int reload = (s_cap == 0 && !spec && chunkT * 4 <= room) ? 1 : 0;
-  int big = std::max(tip_bytes, fac_slots(wst) + pt_bytes);
+  int big = std::max(tip_bytes, fac_slots(wst) + (rfac ? std::max(pt_bytes, s_bytes) : pt_bytes));
   big = std::max(big, std::max(rec_bytes, recv2_bytes));
   if (reload) big = std::max(big, chunkT * 4);
   if (big > room) return FASA_ERR_UNSUPPORTED;
@@ -435,6 +439,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.cap1 = cap1;
   p.cap2 = cap2;
   p.spec = spec;
+  p.rfac = rfac;
   p.fac_wst = wst;
   p.rows_cap = rows_cap;
   p.reload = reload;

@@ -111,6 +111,9 @@ struct StepParams {
   int rho;         // first-round list length per CTA
   int cap1, cap2;  // receive slots per source CTA, first and second round
   int spec;        // gather the first-round list before the selection is final
+  int rfac;        // spec, and the listed rows' scores fit beside the resident slots:
+                   // the scores are taken during the selection, the FAC after it
+                   // splits the head dims over warps (no per-warp records)
   int fac_wst;     // FAC groups in flight per warp (1 or 2)
   int rows_cap;    // capacity of the own-selection list
   int reload;      // copy workspace scores back into shared memory for the sweeps

@@ -99,9 +99,18 @@ __device__ unsigned long long* g_step_trace;
       tr_[64 + (i)] = clock64();                                                                       \
     }                                                                                                  \
   } while (0)
+#define STEP_TRACE_VAL(i, v)                                                                           \
+  do {                                                                                                 \
+    if ((threadIdx.x & 31) == 0 && g_step_trace)                                                       \
+      g_step_trace[(((size_t)blockIdx.y * gridDim.x + blockIdx.x) * SNW + (threadIdx.x >> 5)) * 128 + (i)] = \
+          (unsigned long long)(v);                                                                     \
+  } while (0)
 #else
 #define STEP_TRACE(i) \
   do {                \
+  } while (0)
+#define STEP_TRACE_VAL(i, v) \
+  do {                       \
   } while (0)
 #endif
 
@@ -1276,6 +1285,33 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     for (int i0 = w * RPI; i0 < nfirst; i0 += nw * RPI) row_copy(i0 + g_sub);
     cp_async_commit();
   };
+  // Resident FAC (p.rfac): the scores of resident group g (its slot as
+  // row_copy places it; every group of the list is resident at once) on the
+  // tensor cores, S^T = K Q^T as in the FAC below, stored unmasked (log2
+  // units) as s_rows[head][row], row stride srs.  One warp.
+  float* s_rows = reinterpret_cast<float*>(smem + p.off_pt);
+  const int srs = p.cap1 + 8;
+  auto qk_group = [&](int g) {
+    constexpr int KSG = D / 16;
+    const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3;
+    const uint32_t k_row = ((lane & 7) + 8 * (mi & 1)) * ROWB;
+    const int k_c = mi >> 1, sw = lane & 7;
+    const uint32_t Ks = smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + g / FNW) * GSLOT_B;
+    float sh[4] = {0.f, 0.f, 0.f, 0.f}, slo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KSG; ++ks) {
+      const uint4 f = reinterpret_cast<const uint4*>(qrot)[ks * 32 + lane];
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(Ks + k_row + (((2 * ks + k_c) ^ sw) << 4), a0, a1, a2, a3);
+      mma_bf16_16816(sh, a0, a1, a2, a3, f.x, f.z);
+      mma_bf16_16816(slo, a0, a1, a2, a3, f.y, f.w);
+    }
+    const int r = g * GR + gq;
+    s_rows[(2 * tq) * srs + r] = sh[0] + slo[0];
+    s_rows[(2 * tq + 1) * srs + r] = sh[1] + slo[1];
+    s_rows[(2 * tq) * srs + r + 8] = sh[2] + slo[2];
+    s_rows[(2 * tq + 1) * srs + r + 8] = sh[3] + slo[3];
+  };
 
   if (need_select) {
     // the sweeps read shared memory: scores kept there, or workspace scores
@@ -1361,6 +1397,14 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       if (total >= k_eff) union_select(recv1, stride1, p.cap1, C, k_eff, hist, ms->chist, ms, nuw, p.u_wps, p.u_inv_wps);
     } else {
       fac_start(warp - nuw, SNW - nuw);
+      if (spec && p.rfac) {  // the listed rows' scores, once these warps' copies have landed
+        cp_async_wait<0>();
+        named_bar_sync(5, (SNW - nuw) * 32);
+        STEP_TRACE(32);
+#pragma unroll 1
+        for (int g = warp - nuw; g < (fr_n + GR - 1) / GR; g += SNW - nuw) qk_group(g);
+        STEP_TRACE(33);
+      }
     }
     __syncthreads();
     // lane r reads source r's header (every warp, so the result is everywhere)
@@ -1437,205 +1481,319 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   STEP_TRACE(7);
 
   // ---------------------------------------------------------------- FAC
-  // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
-  // flash-decoding pass per warp over its own 16-row groups: QK as
-  // S^T = K Q^T (16 rows x 8 heads), PV as O^T = V^T P^T (16 head dims x 8
-  // heads per MMA).  q and the softmax weights P are split into bf16 hi + lo
-  // parts, so the products keep ~16 mantissa bits.  Lane (gq, tq) holds rows
-  // gq, gq + 8 of S^T and head dims gq, gq + 8 of O^T, heads 2tq, 2tq + 1.
-  constexpr int KS = D / 16;
-  const int ngrp = (fr_n + GR - 1) / GR;
-  const int nrec = min(FNW, ngrp);  // warps that attend rows
-  float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
-  cp_async_wait<0>();  // the CTA-wide first groups
-  __syncthreads();
-  if (warp < nrec) {
-    const int gq = lane >> 2, tq = lane & 3;
-    uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo], built in the set-up
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint4 f = reinterpret_cast<const uint4*>(qrot)[ks * 32 + lane];
-      qb[ks][0][0] = f.x;
-      qb[ks][0][1] = f.y;
-      qb[ks][1][0] = f.z;
-      qb[ks][1][1] = f.w;
-    }
-    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1
-    float l0 = 0.f, l1 = 0.f;
-    float oc[KS][4];
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
-    float* pt = reinterpret_cast<float*>(smem + p.off_pt) + warp * (G_MAX * PTS);
-    const int mi = lane >> 3;
-    const int kr = (lane & 7) + 8 * (mi & 1), vr = (lane & 7) + 8 * (mi >> 1);
-    const uint32_t k_row = kr * ROWB, v_row = vr * ROWB;
-    const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
-    const int wst = p.fac_wst;
-    int it = 0;
-    for (int g = warp; g < ngrp; g += FNW, ++it) {
-      const int s = wst == 2 ? (it & 1) : 0;
-      if (it > 0) {
-        if (wst == 2) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        __syncwarp();
-      }
-      const uint32_t Ks = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
-      const uint32_t Vs = Ks + GR * ROWB;
-      float sh[4] = {0.f, 0.f, 0.f, 0.f}, slo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(Ks + k_row + (((2 * ks + k_c) ^ sw) << 4), a0, a1, a2, a3);
-        mma_bf16_16816(sh, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
-        mma_bf16_16816(slo, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
-      }
-      const int r0 = g * GR + gq, r1 = r0 + 8;
-      const bool v0 = r0 < fr_n && !(fslot && fslot[r0] < theta);
-      const bool v1 = r1 < fr_n && !(fslot && fslot[r1] < theta);
-      const float s0 = v0 ? sh[0] + slo[0] : -CUDART_INF_F, s1 = v0 ? sh[1] + slo[1] : -CUDART_INF_F;
-      const float s2 = v1 ? sh[2] + slo[2] : -CUDART_INF_F, s3 = v1 ? sh[3] + slo[3] : -CUDART_INF_F;
-      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
-      }
-      const float n0 = fmaxf(m0, x0), n1m = fmaxf(m1, x1);
-      // every row so far may be masked: then nothing is rescaled or added
-      const float c0 = n0 == -CUDART_INF_F ? 1.f : ex2_approx(m0 - n0);
-      const float c1 = n1m == -CUDART_INF_F ? 1.f : ex2_approx(m1 - n1m);
-      const float p0 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s0 - n0);
-      const float p2 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s2 - n0);
-      const float p1 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s1 - n1m);
-      const float p3 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s3 - n1m);
-      l0 = l0 * c0 + p0 + p2;
-      l1 = l1 * c1 + p1 + p3;
-      m0 = n0;
-      m1 = n1m;
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        oc[mt][0] *= c0;
-        oc[mt][1] *= c1;
-        oc[mt][2] *= c0;
-        oc[mt][3] *= c1;
-      }
-      // P^T as the B operand: lane (gq, tq) needs head gq, rows 2tq.. --
-      // transposed through the warp's tile
-      pt[(2 * tq) * PTS + gq] = p0;
-      pt[(2 * tq + 1) * PTS + gq] = p1;
-      pt[(2 * tq) * PTS + gq + 8] = p2;
-      pt[(2 * tq + 1) * PTS + gq + 8] = p3;
-      __syncwarp();
-      const float2 pa = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq);
-      const float2 pb = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq + 8);
-      uint32_t b0h, b0l, b1h, b1l;
-      split_bf16(pa.x, pa.y, b0h, b0l);
-      split_bf16(pb.x, pb.y, b1h, b1l);
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(Vs + v_row + (((2 * mt + v_c) ^ sw) << 4), a0, a1, a2, a3);
-        mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0h, b1h);
-        mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
-      }
-      __syncwarp();  // the slot and the P tile are free again
-      // the warp's next group after the ones in flight: two lanes per row,
-      // each half of its chunks (commits a group even when empty: the waits
-      // count groups)
-      const int gn = g + wst * FNW;
-      if (gn < ngrp) {
-#pragma unroll 4
-        for (int r = 0; r < GR; r += RPI) row_copy(gn * GR + r + g_sub);
-      }
-      cp_async_commit();
-    }
-    cp_async_wait<0>();
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    __syncwarp();
-    // the warp's record, once every warp is done with its slots
-    asm volatile("bar.sync 1, %0;" ::"r"(nrec * 32) : "memory");
-    if (big_ok) {
-      const int h0 = 2 * tq, h1 = 2 * tq + 1;
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int dd = mt * 16 + gq;
-        if (h0 < G) {
-          rec[(h0 * FNW + warp) * (D + 2) + dd] = oc[mt][0];
-          rec[(h0 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][2];
-        }
-        if (h1 < G) {
-          rec[(h1 * FNW + warp) * (D + 2) + dd] = oc[mt][1];
-          rec[(h1 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][3];
-        }
-      }
-      if (gq == 0) {
-        if (h0 < G) {
-          rec[(h0 * FNW + warp) * (D + 2) + D] = m0;
-          rec[(h0 * FNW + warp) * (D + 2) + D + 1] = l0;
-        }
-        if (h1 < G) {
-          rec[(h1 * FNW + warp) * (D + 2) + D] = m1;
-          rec[(h1 * FNW + warp) * (D + 2) + D + 1] = l1;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  STEP_TRACE(8);
-  // ---------------------------------------------------------------- combine
-  // The G*D outputs are cut into C slices of sl float4 groups (the last one
-  // shorter).  The records of the warps that attended rows are merged per
-  // head -- each thread takes the head's maximum M over the records and the
-  // weights exp2(m_w - M) itself, then one multiply-add per warp; no rows:
-  // m = -inf, l = 0 -- and written straight into the combine slots: slice r
-  // with (m, l) of every head goes to slot r of the staging (CTA r's share;
-  // this CTA's own share into its receive slot), each slot then one bulk
-  // copy to CTA r (issued by warp r), which finishes slice r.
+  // The combine staging: the G*D outputs are cut into C slices of sl float4
+  // groups (the last one shorter); slice r with (m, l) of every head goes to
+  // slot r of the staging (CTA r's share; this CTA's own share into its
+  // receive slot), each slot then one bulk copy to CTA r, which finishes
+  // slice r.
   const int ngrp4 = G * (D / 4);
   const int sl = p.comb_sl;  // ceil(ngrp4 / C)
   const int cs = p.comb_slot;  // bytes: sl float4, then G (m, l) float2 (padded)
   const float inv_sl = p.comb_inv_sl;
   unsigned char* crcv = smem + p.off_comb;      // [C][cs], slot r from CTA r
   unsigned char* csnd = smem + p.off_comb_snd;  // [C][cs], slot r for CTA r
+  auto stage_out = [&](int g, int e, float val) {  // output element (head g, dim e)
+    const int q = g * (D / 4) + (e >> 2);
+    const int r = __float2int_rz(((float)q + 0.5f) * inv_sl);  // q / sl, exact for these sizes
+    unsigned char* dst = (r == (int)crank ? crcv : csnd) + r * cs;
+    *reinterpret_cast<float*>(dst + (q - r * sl) * 16 + (e & 3) * 4) = val;
+  };
+  if (spec && p.rfac && need_select && !second) {
+    // Resident FAC: every row of the own first-round list sits in its slot
+    // and its scores are in s_rows (taken by the gather warps during the
+    // selection, or now).  Warp w < D/16 takes head dims 16w..16w+15 of
+    // every head over all rows: lane (gq, tq) reads the scores of head gq at
+    // the rows of its B fragments (2tq, 2tq+1, 2tq+8, 2tq+9 of each group),
+    // masks the rows below theta, and forms the head's maximum M and the
+    // weights P = exp2(s - M) (M and L = sum P come out the same in every
+    // warp); then O^T = V^T P^T on the tensor cores, P split into bf16
+    // hi + lo.  The warp's slice of the CTA's (M, L, acc) record goes
+    // straight into the combine slots: no per-warp records to merge.
+    constexpr int KS = D / 16;
+    const int ngrp = (fr_n + GR - 1) / GR;
+    if (p.u_nuw == SNW) {  // (uniform) every warp gathered: the scores now
+      cp_async_wait<0>();
+      __syncthreads();
 #pragma unroll 1
-  for (int x = tid; x < G * (D + 2); x += SNT) {
-    const int g = x / (D + 2), e = x - g * (D + 2);
-    float val = e == D ? -CUDART_INF_F : 0.f;
-    if (big_ok && nrec > 0) {
-      // (unrolled over the at most FNW records, so the loads overlap)
-      const float* rg = rec + g * FNW * (D + 2);
-      float mr[FNW], M = -CUDART_INF_F;
+      for (int g = warp; g < ngrp; g += SNW) qk_group(g);
+      __syncthreads();
+    }
+    if (warp < KS) {
+      // Every attending warp compacts the selected entries of the list (key
+      // >= theta, in list order) into its own index array sp and takes each
+      // head's maximum M over them (rolled loops: this code runs once per
+      // launch, and its instruction fetch is much of its cost).
+      uint16_t* sp = reinterpret_cast<uint16_t*>(s_rows + G_MAX * srs) + warp * p.cap1;
+      const int gq = lane >> 2, tq = lane & 3, mt = warp;
+      float mx[G_MAX];
 #pragma unroll
-      for (int r = 0; r < FNW; ++r) {
-        mr[r] = r < nrec ? rg[r * (D + 2) + D] : -CUDART_INF_F;
-        M = fmaxf(M, mr[r]);
+      for (int h = 0; h < G_MAX; ++h) mx[h] = -CUDART_INF_F;
+      int n_sel = 0;
+#pragma unroll 1
+      for (int e0 = 0; e0 < fr_n; e0 += 32) {
+        const int e = e0 + lane;
+        const bool v = e < fr_n && fslot[e] >= theta;
+        const unsigned bal = __ballot_sync(0xffffffffu, v);
+        if (v) {
+#pragma unroll
+          for (int h = 0; h < G_MAX; ++h)
+            if (h < G) mx[h] = fmaxf(mx[h], s_rows[h * srs + e]);
+          sp[n_sel + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)e;
+        }
+        n_sel += __popc(bal);
       }
-      if (e == D) {
-        val = M;
-      } else {  // (e == D + 1: the record's l)
-        float acc = 0.f;
+      // head gq's maximum over the warp (order-preserving unsigned keys)
+      float M = 0.f;
 #pragma unroll
-        for (int r = 0; r < FNW; ++r)
-          if (r < nrec) {
-            const float w = mr[r] != -CUDART_INF_F ? ex2_approx(mr[r] - M) : 0.f;
-            acc = fmaf(w, rg[r * (D + 2) + e], acc);
+      for (int h = 0; h < G_MAX; ++h) {
+        uint32_t u = __float_as_uint(mx[h]);
+        u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        u = __reduce_max_sync(0xffffffffu, u);
+        if (gq == h && h < G) M = __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+      }
+      __syncwarp();
+      const float* Sh = s_rows + gq * srs;
+      auto row_at = [&](int ci) { return (int)sp[ci < n_sel ? ci : 0]; };
+      // ldmatrix (transposed) of V: lane gives row vr of matrix (lane >> 3),
+      // chunk 2 mt + v_c; the row's chunk sits at c ^ (slot row & 7).
+      // Selected rows past n_sel: a real row with weight 0.
+      const int vr = (lane & 7) + 8 * ((lane >> 3) >> 1), v_c = (lane >> 3) & 1;
+      const int ngs = (n_sel + GR - 1) / GR;
+      float L = 0.f, oc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int vg = 0; vg < ngs; ++vg) {
+        const int c0 = vg * GR + 2 * tq;
+        const float p0 = c0 < n_sel ? ex2_approx(Sh[row_at(c0)] - M) : 0.f;
+        const float p1 = c0 + 1 < n_sel ? ex2_approx(Sh[row_at(c0 + 1)] - M) : 0.f;
+        const float p2 = c0 + 8 < n_sel ? ex2_approx(Sh[row_at(c0 + 8)] - M) : 0.f;
+        const float p3 = c0 + 9 < n_sel ? ex2_approx(Sh[row_at(c0 + 9)] - M) : 0.f;
+        L += (p0 + p1) + (p2 + p3);
+        uint32_t b0h, b0l, b1h, b1l;
+        split_bf16(p0, p1, b0h, b0l);
+        split_bf16(p2, p3, b1h, b1l);
+        const int pr = row_at(vg * GR + vr);
+        const int pg = pr / GR, rr = pr & (GR - 1);
+        const uint32_t va = smem_u32(big) + (uint32_t)((pg % FNW) * p.fac_wst + pg / FNW) * GSLOT_B +
+                            (uint32_t)(GR + rr) * ROWB + (uint32_t)(((2 * mt + v_c) ^ (rr & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(va, a0, a1, a2, a3);
+        mma_bf16_16816(oc, a0, a1, a2, a3, b0h, b1h);
+        mma_bf16_16816(oc, a0, a1, a2, a3, b0l, b1l);
+      }
+      L += __shfl_xor_sync(0xffffffffu, L, 1);
+      L += __shfl_xor_sync(0xffffffffu, L, 2);
+      STEP_TRACE(36);
+      // oc: head dims 16 mt + gq (+ 8) x heads 2tq, 2tq + 1
+      if (2 * tq < G) {
+        stage_out(2 * tq, mt * 16 + gq, oc[0]);
+        stage_out(2 * tq, mt * 16 + gq + 8, oc[2]);
+      }
+      if (2 * tq + 1 < G) {
+        stage_out(2 * tq + 1, mt * 16 + gq, oc[1]);
+        stage_out(2 * tq + 1, mt * 16 + gq + 8, oc[3]);
+      }
+      // every head's (M, L) into each slot: warp w the slots w, w + D/16, ..
+      if (tq == 0 && gq < G)
+#pragma unroll 1
+        for (int r = warp; r < C; r += KS)
+          *reinterpret_cast<float2*>((r == (int)crank ? crcv : csnd) + r * cs + sl * 16 + gq * 8) = make_float2(M, L);
+    }
+    STEP_TRACE(8);
+  } else {
+    // Tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
+    // flash-decoding pass per warp over its own 16-row groups: QK as
+    // S^T = K Q^T (16 rows x 8 heads), PV as O^T = V^T P^T (16 head dims x 8
+    // heads per MMA).  q and the softmax weights P are split into bf16 hi + lo
+    // parts, so the products keep ~16 mantissa bits.  Lane (gq, tq) holds rows
+    // gq, gq + 8 of S^T and head dims gq, gq + 8 of O^T, heads 2tq, 2tq + 1.
+    constexpr int KS = D / 16;
+    const int ngrp = (fr_n + GR - 1) / GR;
+    const int nrec = min(FNW, ngrp);  // warps that attend rows
+    float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
+    cp_async_wait<0>();  // the CTA-wide first groups
+    __syncthreads();
+    if (warp < nrec) {
+      const int gq = lane >> 2, tq = lane & 3;
+      uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo], built in the set-up
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint4 f = reinterpret_cast<const uint4*>(qrot)[ks * 32 + lane];
+        qb[ks][0][0] = f.x;
+        qb[ks][0][1] = f.y;
+        qb[ks][1][0] = f.z;
+        qb[ks][1][1] = f.w;
+      }
+      float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max (log2 units), heads 2tq, 2tq + 1
+      float l0 = 0.f, l1 = 0.f;
+      float oc[KS][4];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+      float* pt = reinterpret_cast<float*>(smem + p.off_pt) + warp * (G_MAX * PTS);
+      const int mi = lane >> 3;
+      const int kr = (lane & 7) + 8 * (mi & 1), vr = (lane & 7) + 8 * (mi >> 1);
+      const uint32_t k_row = kr * ROWB, v_row = vr * ROWB;
+      const int k_c = mi >> 1, v_c = mi & 1, sw = lane & 7;
+      const int wst = p.fac_wst;
+      int it = 0;
+      for (int g = warp; g < ngrp; g += FNW, ++it) {
+        const int s = wst == 2 ? (it & 1) : 0;
+        if (it > 0) {
+          if (wst == 2) cp_async_wait<1>();
+          else cp_async_wait<0>();
+          __syncwarp();
+        }
+        const uint32_t Ks = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
+        const uint32_t Vs = Ks + GR * ROWB;
+        float sh[4] = {0.f, 0.f, 0.f, 0.f}, slo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(Ks + k_row + (((2 * ks + k_c) ^ sw) << 4), a0, a1, a2, a3);
+          mma_bf16_16816(sh, a0, a1, a2, a3, qb[ks][0][0], qb[ks][1][0]);
+          mma_bf16_16816(slo, a0, a1, a2, a3, qb[ks][0][1], qb[ks][1][1]);
+        }
+        const int r0 = g * GR + gq, r1 = r0 + 8;
+        const bool v0 = r0 < fr_n && !(fslot && fslot[r0] < theta);
+        const bool v1 = r1 < fr_n && !(fslot && fslot[r1] < theta);
+        const float s0 = v0 ? sh[0] + slo[0] : -CUDART_INF_F, s1 = v0 ? sh[1] + slo[1] : -CUDART_INF_F;
+        const float s2 = v1 ? sh[2] + slo[2] : -CUDART_INF_F, s3 = v1 ? sh[3] + slo[3] : -CUDART_INF_F;
+        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+          x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+        }
+        const float n0 = fmaxf(m0, x0), n1m = fmaxf(m1, x1);
+        // every row so far may be masked: then nothing is rescaled or added
+        const float c0 = n0 == -CUDART_INF_F ? 1.f : ex2_approx(m0 - n0);
+        const float c1 = n1m == -CUDART_INF_F ? 1.f : ex2_approx(m1 - n1m);
+        const float p0 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s0 - n0);
+        const float p2 = n0 == -CUDART_INF_F ? 0.f : ex2_approx(s2 - n0);
+        const float p1 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s1 - n1m);
+        const float p3 = n1m == -CUDART_INF_F ? 0.f : ex2_approx(s3 - n1m);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+        m0 = n0;
+        m1 = n1m;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          oc[mt][0] *= c0;
+          oc[mt][1] *= c1;
+          oc[mt][2] *= c0;
+          oc[mt][3] *= c1;
+        }
+        // P^T as the B operand: lane (gq, tq) needs head gq, rows 2tq.. --
+        // transposed through the warp's tile
+        pt[(2 * tq) * PTS + gq] = p0;
+        pt[(2 * tq + 1) * PTS + gq] = p1;
+        pt[(2 * tq) * PTS + gq + 8] = p2;
+        pt[(2 * tq + 1) * PTS + gq + 8] = p3;
+        __syncwarp();
+        const float2 pa = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq);
+        const float2 pb = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq + 8);
+        uint32_t b0h, b0l, b1h, b1l;
+        split_bf16(pa.x, pa.y, b0h, b0l);
+        split_bf16(pb.x, pb.y, b1h, b1l);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(Vs + v_row + (((2 * mt + v_c) ^ sw) << 4), a0, a1, a2, a3);
+          mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0h, b1h);
+          mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
+        }
+        __syncwarp();  // the slot and the P tile are free again
+        // the warp's next group after the ones in flight: two lanes per row,
+        // each half of its chunks (commits a group even when empty: the waits
+        // count groups)
+        const int gn = g + wst * FNW;
+        if (gn < ngrp) {
+#pragma unroll 4
+          for (int r = 0; r < GR; r += RPI) row_copy(gn * GR + r + g_sub);
+        }
+        cp_async_commit();
+      }
+      cp_async_wait<0>();
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      __syncwarp();
+      // the warp's record, once every warp is done with its slots
+      asm volatile("bar.sync 1, %0;" ::"r"(nrec * 32) : "memory");
+      if (big_ok) {
+        const int h0 = 2 * tq, h1 = 2 * tq + 1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int dd = mt * 16 + gq;
+          if (h0 < G) {
+            rec[(h0 * FNW + warp) * (D + 2) + dd] = oc[mt][0];
+            rec[(h0 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][2];
           }
-        val = acc;
+          if (h1 < G) {
+            rec[(h1 * FNW + warp) * (D + 2) + dd] = oc[mt][1];
+            rec[(h1 * FNW + warp) * (D + 2) + dd + 8] = oc[mt][3];
+          }
+        }
+        if (gq == 0) {
+          if (h0 < G) {
+            rec[(h0 * FNW + warp) * (D + 2) + D] = m0;
+            rec[(h0 * FNW + warp) * (D + 2) + D + 1] = l0;
+          }
+          if (h1 < G) {
+            rec[(h1 * FNW + warp) * (D + 2) + D] = m1;
+            rec[(h1 * FNW + warp) * (D + 2) + D + 1] = l1;
+          }
+        }
       }
     }
-    if (e < D) {
-      const int q = g * (D / 4) + (e >> 2);
-      const int r = __float2int_rz(((float)q + 0.5f) * inv_sl);  // q / sl, exact for these sizes
-      unsigned char* dst = (r == (int)crank ? crcv : csnd) + r * cs;
-      *reinterpret_cast<float*>(dst + (q - r * sl) * 16 + (e & 3) * 4) = val;
-    } else {
+    __syncthreads();
+    STEP_TRACE(8);
+    // ---------------------------------------------------------------- combine
+    // The G*D outputs are cut into C slices of sl float4 groups (the last one
+    // shorter).  The records of the warps that attended rows are merged per
+    // head -- each thread takes the head's maximum M over the records and the
+    // weights exp2(m_w - M) itself, then one multiply-add per warp; no rows:
+    // m = -inf, l = 0 -- and written straight into the combine slots: slice r
+    // with (m, l) of every head goes to slot r of the staging (CTA r's share;
+    // this CTA's own share into its receive slot), each slot then one bulk
+    // copy to CTA r (issued by warp r), which finishes slice r.
 #pragma unroll 1
-      for (int r = 0; r < C; ++r)
-        *reinterpret_cast<float*>((r == (int)crank ? crcv : csnd) + r * cs + sl * 16 + g * 8 + (e - D) * 4) = val;
+    for (int x = tid; x < G * (D + 2); x += SNT) {
+      const int g = x / (D + 2), e = x - g * (D + 2);
+      float val = e == D ? -CUDART_INF_F : 0.f;
+      if (big_ok && nrec > 0) {
+        // (unrolled over the at most FNW records, so the loads overlap)
+        const float* rg = rec + g * FNW * (D + 2);
+        float mr[FNW], M = -CUDART_INF_F;
+#pragma unroll
+        for (int r = 0; r < FNW; ++r) {
+          mr[r] = r < nrec ? rg[r * (D + 2) + D] : -CUDART_INF_F;
+          M = fmaxf(M, mr[r]);
+        }
+        if (e == D) {
+          val = M;
+        } else {  // (e == D + 1: the record's l)
+          float acc = 0.f;
+#pragma unroll
+          for (int r = 0; r < FNW; ++r)
+            if (r < nrec) {
+              const float w = mr[r] != -CUDART_INF_F ? ex2_approx(mr[r] - M) : 0.f;
+              acc = fmaf(w, rg[r * (D + 2) + e], acc);
+            }
+          val = acc;
+        }
+      }
+      if (e < D) {
+        const int q = g * (D / 4) + (e >> 2);
+        const int r = __float2int_rz(((float)q + 0.5f) * inv_sl);  // q / sl, exact for these sizes
+        unsigned char* dst = (r == (int)crank ? crcv : csnd) + r * cs;
+        *reinterpret_cast<float*>(dst + (q - r * sl) * 16 + (e & 3) * 4) = val;
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < C; ++r)
+          *reinterpret_cast<float*>((r == (int)crank ? crcv : csnd) + r * cs + sl * 16 + g * 8 + (e - D) * 4) = val;
+      }
     }
   }
   fence_proxy_async();  // the staging's generic writes, before the async proxy reads them
