@@ -36,7 +36,7 @@ int cuda_fail(cudaError_t e) {
 
 constexpr int SMEM_LIMIT = 232448;  // 227 KB per CTA
 constexpr int S_CAP_MAX = 8192;     // scores per CTA kept in shared memory
-constexpr int STEP_MIN_C = 8;       // smallest cluster the single-exchange step kernel serves
+constexpr int STEP_MIN_C = 4;       // smallest cluster the single-exchange step kernel serves
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -354,14 +354,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   off += std::max(G * D * 4, (D / 16) * 32 * 16);
   p.off_qbar = off;
   off += align_up(2 * nfc * 4, 16);
-  p.off_hist = off;
-  off += HLOC_BINS * 4;
   p.off_uh = off;
   off += UH_BINS * 4;
-  p.off_sc = off;
-  off += s_cap * 4;
-  p.off_recv1 = off;
-  off += C * (cap1 + 2) * 8;  // per source: a 16-byte header, then the entries
   p.off_rows = off;
   off += align_up(rows_cap * 4, 16);
   const int comb_slot = sl * 16 + align_up(G * 8, 16);
@@ -369,6 +363,15 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   off += C * comb_slot;
   p.off_comb_snd = off;
   off += C * comb_slot;
+  // the selection's regions, dead once the own selection is compacted, sit
+  // right before `big`: a gather after the selection may use them too
+  off = align_up(off, 128);
+  p.off_hist = off;
+  off += HLOC_BINS * 4;
+  p.off_sc = off;
+  off += s_cap * 4;
+  p.off_recv1 = off;
+  off += C * (cap1 + 2) * 8;  // per source: a 16-byte header, then the entries
   off = align_up(off, 128);
   p.off_big = off;
   const int room = limit - off;
@@ -376,7 +379,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   // after TIP: FAC slots (then the P tiles), the second-round slots (written
   // only once every CTA drained its gathers), the warp records
   auto fac_slots = [&](int wst) { return wst * FNW * 2 * GR * D * ES; };
-  const int pt_bytes = FNW * G_MAX * PTS * 4;
+  const int pt_bytes = FNW * G * PTS * 4;  // each attending warp's P tile, heads x PTS
   const int rec_bytes = (G_MAX * FNW * (D + 2) + G_MAX * FNW + G_MAX) * 4;
   const int recv2_bytes = C == 1 ? 0 : C * (cap2 + 2) * 8;
   // TIP staging: the whole range at once (no refill) with the smallest tile
@@ -421,7 +424,22 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   for (int w = 2; w >= 1 && !wst; --w)
     if (fac_slots(w) + pt_bytes <= room) wst = w;
   if (!wst) return FASA_ERR_UNSUPPORTED;
+  // the first-round list is gathered during the exchange when it fits the
+  // slots (a longer list streamed after the selection measured slower: the
+  // early copies slow the selection and leave fewer slots per warp)
   const int spec = (C > 1 && cap1 <= wst * FNW * GR) ? 1 : 0;
+  // Without the first-round gather, every gather follows the selection and
+  // its slots start at the histogram: up to FAC_WST_MAX groups in flight per
+  // warp over the selection's dead regions and `big`.
+  int off_fac = p.off_big, wst_fac = wst;
+  if (!spec) {
+    off_fac = p.off_hist;
+    for (int w = FAC_WST_MAX; w > wst; --w)
+      if (off_fac + fac_slots(w) + pt_bytes <= limit) {
+        wst_fac = w;
+        break;
+      }
+  }
   // the listed rows' scores, [G_MAX heads][cap1 + 8], beside the slots,
   // then each attending warp's compacted selection (cap1 16-bit entries)
   const int s_bytes = G_MAX * (cap1 + 8) * 4 + align_up((D / 16) * cap1 * 2, 16);
@@ -440,7 +458,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.cap2 = cap2;
   p.spec = spec;
   p.rfac = rfac;
-  p.fac_wst = wst;
+  p.fac_wst = wst_fac;
+  p.off_fac = off_fac;
   p.rows_cap = rows_cap;
   p.reload = reload;
   p.comb_slot = comb_slot;
@@ -454,8 +473,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   p.u_wps = std::max(1, p.u_nuw / C);
   p.u_inv_wps = 1.f / (float)p.u_wps;
   p.off_recv2 = p.off_big;
-  p.off_pt = p.off_big + fac_slots(wst);
-  p.smem_total = p.off_big + big;
+  p.off_pt = off_fac + fac_slots(wst_fac);
+  p.smem_total = std::max(p.off_big + big, p.off_pt + pt_bytes);
   *ws = s_cap == 0 ? (size_t)d->batch * d->n_kv_heads * d->t_max * 4 : 0;
   return FASA_OK;
 }

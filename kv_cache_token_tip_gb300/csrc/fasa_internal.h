@@ -77,6 +77,7 @@ struct Params {
 constexpr int SNT = 512;           // threads of a step CTA
 constexpr int SNW = SNT / 32;      // its warps
 constexpr int FNW = 8;             // warps that attend rows (one 16-row group slot set each)
+constexpr int FAC_WST_MAX = 4;     // FAC groups in flight per attending warp, at most
 constexpr int ST_MAX_STAGES = 12;  // TIP stage mbarriers [0, 12)
 constexpr int ST_BARS = 16;        // + two selection exchanges, the combine, the score reload
 constexpr int ST_MISC_BYTES = 1152;
@@ -114,7 +115,9 @@ struct StepParams {
   int rfac;        // spec, and the listed rows' scores fit beside the resident slots:
                    // the scores are taken during the selection, the FAC after it
                    // splits the head dims over warps (no per-warp records)
-  int fac_wst;     // FAC groups in flight per warp (1 or 2)
+  int fac_wst;     // FAC groups in flight per warp (1 .. FAC_WST_MAX)
+  int off_fac;     // the FAC group slots: `big`, or (no first-round gather) the
+                   // histogram onwards, the selection's regions being dead by then
   int rows_cap;    // capacity of the own-selection list
   int reload;      // copy workspace scores back into shared memory for the sweeps
   int comb_slot;   // bytes of one combine slot: an output slice and every head's (m, l)

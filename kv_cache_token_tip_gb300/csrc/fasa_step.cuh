@@ -891,6 +891,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   unsigned long long* recv1 = reinterpret_cast<unsigned long long*>(smem + p.off_recv1);
   int* rows = reinterpret_cast<int*>(smem + p.off_rows);
   unsigned char* big = smem + p.off_big;
+  const uint32_t fbase = smem_u32(smem + p.off_fac);  // the FAC group slots
 
   STEP_TRACE(0);
   constexpr int QW = 8;  // query warps
@@ -1268,7 +1269,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   const int g_kv = g_cc >= CPR ? 1 : 0, g_ch = g_cc - g_kv * CPR;
   auto row_copy = [&](int i) {  // this lane's chunk of row i
     const int g = i / GR, rr = i & (GR - 1);
-    const uint32_t dst = smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B +
+    const uint32_t dst = fbase + (uint32_t)((g % FNW) * p.fac_wst + (g / FNW) % p.fac_wst) * GSLOT_B +
                          (uint32_t)(g_kv * GR + rr) * ROWB + (uint32_t)((g_ch ^ (rr & 7)) << 4);
     const bool real = i < fr_n;
     const int tok = real ? row_token(i) : 0;
@@ -1296,7 +1297,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3;
     const uint32_t k_row = ((lane & 7) + 8 * (mi & 1)) * ROWB;
     const int k_c = mi >> 1, sw = lane & 7;
-    const uint32_t Ks = smem_u32(big) + (uint32_t)((g % FNW) * p.fac_wst + g / FNW) * GSLOT_B;
+    const uint32_t Ks = fbase + (uint32_t)((g % FNW) * p.fac_wst + g / FNW) * GSLOT_B;
     float sh[4] = {0.f, 0.f, 0.f, 0.f}, slo[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < KSG; ++ks) {
@@ -1573,7 +1574,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
         split_bf16(p2, p3, b1h, b1l);
         const int pr = row_at(vg * GR + vr);
         const int pg = pr / GR, rr = pr & (GR - 1);
-        const uint32_t va = smem_u32(big) + (uint32_t)((pg % FNW) * p.fac_wst + pg / FNW) * GSLOT_B +
+        const uint32_t va = fbase + (uint32_t)((pg % FNW) * p.fac_wst + pg / FNW) * GSLOT_B +
                             (uint32_t)(GR + rr) * ROWB + (uint32_t)(((2 * mt + v_c) ^ (rr & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(va, a0, a1, a2, a3);
@@ -1628,7 +1629,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       float oc[KS][4];
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
-      float* pt = reinterpret_cast<float*>(smem + p.off_pt) + warp * (G_MAX * PTS);
+      float* pt = reinterpret_cast<float*>(smem + p.off_pt) + warp * (G * PTS);  // [head < G][PTS]
       const int mi = lane >> 3;
       const int kr = (lane & 7) + 8 * (mi & 1), vr = (lane & 7) + 8 * (mi >> 1);
       const uint32_t k_row = kr * ROWB, v_row = vr * ROWB;
@@ -1636,13 +1637,15 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       const int wst = p.fac_wst;
       int it = 0;
       for (int g = warp; g < ngrp; g += FNW, ++it) {
-        const int s = wst == 2 ? (it & 1) : 0;
-        if (it > 0) {
-          if (wst == 2) cp_async_wait<1>();
+        const int s = it % wst;
+        if (it > 0) {  // at most wst - 1 of this thread's later groups may still be in flight
+          if (wst >= 4) cp_async_wait<3>();
+          else if (wst == 3) cp_async_wait<2>();
+          else if (wst == 2) cp_async_wait<1>();
           else cp_async_wait<0>();
           __syncwarp();
         }
-        const uint32_t Ks = smem_u32(big) + (uint32_t)(warp * wst + s) * GSLOT_B;
+        const uint32_t Ks = fbase + (uint32_t)(warp * wst + s) * GSLOT_B;
         const uint32_t Vs = Ks + GR * ROWB;
         float sh[4] = {0.f, 0.f, 0.f, 0.f}, slo[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1684,13 +1687,17 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
         }
         // P^T as the B operand: lane (gq, tq) needs head gq, rows 2tq.. --
         // transposed through the warp's tile
-        pt[(2 * tq) * PTS + gq] = p0;
-        pt[(2 * tq + 1) * PTS + gq] = p1;
-        pt[(2 * tq) * PTS + gq + 8] = p2;
-        pt[(2 * tq + 1) * PTS + gq + 8] = p3;
+        if (2 * tq < G) {
+          pt[(2 * tq) * PTS + gq] = p0;
+          pt[(2 * tq) * PTS + gq + 8] = p2;
+        }
+        if (2 * tq + 1 < G) {
+          pt[(2 * tq + 1) * PTS + gq] = p1;
+          pt[(2 * tq + 1) * PTS + gq + 8] = p3;
+        }
         __syncwarp();
-        const float2 pa = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq);
-        const float2 pb = *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq + 8);
+        const float2 pa = gq < G ? *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq) : make_float2(0.f, 0.f);
+        const float2 pb = gq < G ? *reinterpret_cast<const float2*>(pt + gq * PTS + 2 * tq + 8) : make_float2(0.f, 0.f);
         uint32_t b0h, b0l, b1h, b1l;
         split_bf16(pa.x, pa.y, b0h, b0l);
         split_bf16(pb.x, pb.y, b1h, b1l);

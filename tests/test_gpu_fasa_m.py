@@ -197,8 +197,12 @@ def _nondom_expected(L, cfg):
     return out
 
 
-@pytest.mark.parametrize("name,over", [("llama3_8b_ctx32k", dict(context=8192, batch=1)),
-                                       ("qwen25_7b_b8_ctx16k", dict(context=4096))])
+SPLIT_CASES = [("llama3_8b_ctx32k", dict(context=8192, batch=1)),    # single-exchange, list resident
+               ("qwen25_7b_b8_ctx16k", dict(context=4096)),            # single-exchange, list streamed
+               ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=16))]  # cluster kernel
+
+
+@pytest.mark.parametrize("name,over", SPLIT_CASES)
 def test_split_keys_against_oracle(name, over):
     """FASA-M with split keys: K^nondom and V in host memory, K^dom on the
     GPU.  fasa_build_knondom writes exactly each token's non-dominant pairs;
@@ -238,7 +242,9 @@ def test_split_keys_against_oracle(name, over):
 
 
 @pytest.mark.parametrize("name,over,lens", [("llama3_8b_ctx32k", dict(context=8192, batch=2), (8000, 300)),
-                                            ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2), (4000, 1234))])
+                                            ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=2), (4000, 1234)),
+                                            ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=16),
+                                             (4000, 1234, 3500, 4095, 17, 3097, 3098, 2000) * 2)])
 def test_split_keys_append_against_oracle(name, over, lens):
     """The append step over split keys: the new token's non-dominant pairs
     land in its k_nondom row (host memory) exactly as fasa_build_knondom
@@ -291,13 +297,11 @@ def test_split_keys_append_against_oracle(name, over, lens):
 
 
 def test_split_keys_cover_both_fused_kernels():
-    """The two cases above run on different fused kernels (the
-    single-exchange kernel and the cluster kernel)."""
+    """The cases above run on both fused kernels (the single-exchange kernel
+    and the cluster kernel)."""
     from kv_cache_token_tip_gb300 import dims_for, fasa_step_kernel
-    kinds = {fasa_step_kernel(dims_for(configs.CONFIGS[n].with_(**o)))
-             for n, o in (("llama3_8b_ctx32k", dict(context=8192, batch=1)),
-                          ("qwen25_7b_b8_ctx16k", dict(context=4096)))}
-    assert len(kinds) == 2
+    kinds = [fasa_step_kernel(dims_for(configs.CONFIGS[n].with_(**o))) for n, o in SPLIT_CASES]
+    assert kinds == [1, 1, 0]
 
 
 def test_split_keys_reject_what_the_layout_cannot_hold():

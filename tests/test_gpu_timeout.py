@@ -27,8 +27,11 @@ def _built(cuda_ok):
 
 
 # the two fused kernels: the single-exchange kernel at the 32K single-sequence
-# shape, the cluster kernel at batch 8 (32 units, clusters of fewer than 8)
-CASES = [("llama3_8b_ctx32k", {}, 1), ("qwen25_7b_b8_ctx16k", dict(context=4096), 0)]
+# shape (its whole first-round list resident) and at batch 8 (32 units,
+# clusters of 4, the list streamed), the cluster kernel at batch 16 (64
+# units, clusters of 2)
+CASES = [("llama3_8b_ctx32k", {}, 1), ("qwen25_7b_b8_ctx16k", dict(context=4096), 1),
+         ("qwen25_7b_b8_ctx16k", dict(context=4096, batch=16), 0)]
 
 
 def _setup(name="llama3_8b_ctx32k", over=None, kernel=1):
