@@ -239,11 +239,13 @@ __device__ __forceinline__ void tip4(const unsigned char* row, int nfc_rt, const
 }
 
 // The four scores at scr[tl..tl+4) as keys; ok marks those below `end`.
-// tl is a multiple of 4 and the score buffers extend to a multiple of 4
-// (shared memory: the CTA's whole token chunk; workspace: T_max), so the
-// 16-byte load stays inside them.
+// tl is a multiple of 4; a group starting at or past `end` is not read (a
+// sweep's last lanes would otherwise read past the CTA's scores, past the
+// workspace for the last unit), and one starting below it stays inside the
+// score buffer, which extends to a multiple of 4 (shared memory: the CTA's
+// whole token chunk; workspace: T_max, a multiple of 64).
 __device__ __forceinline__ void keys4(const float* scr, int tl, int end, uint32_t (&key)[4], bool (&ok)[4]) {
-  const float4 x = *reinterpret_cast<const float4*>(scr + tl);
+  const float4 x = tl < end ? *reinterpret_cast<const float4*>(scr + tl) : make_float4(0.f, 0.f, 0.f, 0.f);
   key[0] = score_key(x.x);
   key[1] = score_key(x.y);
   key[2] = score_key(x.z);
