@@ -339,7 +339,11 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   const double e = (double)k / C;
   int rho = C == 1 ? k : (int)ceil(e + 4.0 * sqrt(e) + 4.0);
   rho = std::max(1, std::min(rho, chunkT));
-  const int cap1 = align_up(rho + std::max(64, rho / 4), 16);
+  // (slack for the whole threshold bin, which grows with the scores per CTA:
+  // with tens of thousands a 12-bit bin near the list's end holds hundreds
+  // of keys, and a list that cannot take it is refined with two more
+  // histogram sweeps)
+  const int cap1 = align_up(rho + std::max(std::max(64, rho / 4), chunkT / 128), 16);
   const int cap2 = C == 1 ? 0 : align_up(k + std::max(32, k / 8), 16);
   const int s_cap = chunkT <= S_CAP_MAX ? chunkT : 0;
   const int rows_cap = std::min(k, std::max(cap1, cap2));
