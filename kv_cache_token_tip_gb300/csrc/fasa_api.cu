@@ -352,6 +352,8 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   int off = 0;
   p.off_bar = off;
   off += ST_BARS * 8;
+  p.off_fbar = off;  // the FAC slots' full and empty barriers
+  off += 2 * FNW * FAC_WST_MAX * 8;
   p.off_misc = off;
   off += ST_MISC_BYTES;
   p.off_qrot = off;  // the rotated query, then the FAC's query fragments over it

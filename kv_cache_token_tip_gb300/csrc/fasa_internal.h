@@ -129,8 +129,8 @@ struct StepParams {
   // the union select: warps taking part, and warps per source list
   int u_nuw, u_wps;
   float u_inv_wps;
-  int off_bar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb, off_comb_snd,
-      off_big, off_recv2, off_pt, smem_total;
+  int off_bar, off_fbar, off_misc, off_qrot, off_qbar, off_hist, off_uh, off_sc, off_recv1, off_rows, off_comb,
+      off_comb_snd, off_big, off_recv2, off_pt, smem_total;
 };
 
 // Kernel launchers (one translation unit per storage type).

@@ -884,6 +884,11 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
   const int G = p.G;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  // FAC slot s of attending warp c: full (32 producer-lane arrivals, each
+  // once its copies have landed) and empty (one arrival by the attending warp)
+  uint64_t* fbars = reinterpret_cast<uint64_t*>(smem + p.off_fbar);
+  auto fbar_full = [&](int c, int s) { return smem_u32(fbars + c * FAC_WST_MAX + s); };
+  auto fbar_empty = [&](int c, int s) { return smem_u32(fbars + (FNW + c) * FAC_WST_MAX + s); };
   StepMisc* ms = reinterpret_cast<StepMisc*>(smem + p.off_misc);
   float* qrot = reinterpret_cast<float*>(smem + p.off_qrot);
   float* qbar = reinterpret_cast<float*>(smem + p.off_qbar);
@@ -1111,6 +1116,11 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const T* vnp = reinterpret_cast<const T*>(p.v_new) + (size_t)unit * D + 2 * tid;
     kn = __halves2bfloat162(knp[0], knp[1]);
     vn = __halves2bfloat162(vnp[0], vnp[1]);
+  }
+  if (warp == SNW - 1) {  // (idle in the set-up) the FAC slots' barriers
+#pragma unroll 1
+    for (int i = lane; i < 2 * FNW * FAC_WST_MAX; i += 32) mbar_init(smem_u32(fbars + i), i < FNW * FAC_WST_MAX ? 32u : 1u);
+    fence_mbar_init();
   }
   {
     uint4* z = reinterpret_cast<uint4*>(hist);
@@ -1609,13 +1619,37 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     // heads per MMA).  q and the softmax weights P are split into bf16 hi + lo
     // parts, so the products keep ~16 mantissa bits.  Lane (gq, tq) holds rows
     // gq, gq + 8 of S^T and head dims gq, gq + 8 of O^T, heads 2tq, 2tq + 1.
+    //
+    // The first fac_wst groups of every attending warp come from the CTA-wide
+    // first issue.  Rows gathered after the selection (no first-round list in
+    // the slots): warp FNW + c is the producer of attending warp c's later
+    // groups -- it refills c's slots in turn, each once c has released it
+    // (empty), and arms the slot's full barrier with its lanes' completion
+    // arrivals.  Otherwise (the listed rows) each attending warp refills its
+    // own slots.
     constexpr int KS = D / 16;
     const int ngrp = (fr_n + GR - 1) / GR;
     const int nrec = min(FNW, ngrp);  // warps that attend rows
+    const bool pc = fslot == nullptr;  // (uniform)
     float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
-    cp_async_wait<0>();  // the CTA-wide first groups
+    cp_async_wait<0>();  // the CTA-wide first groups (listed rows)
     __syncthreads();
-    if (warp < nrec) {
+    if (pc && warp >= FNW) {
+      const int c = warp - FNW, wst = p.fac_wst;
+      int it = wst;
+#pragma unroll 1
+      for (int g = c + wst * FNW; g < ngrp; g += FNW, ++it) {
+        const int s = it % wst, n = it / wst;  // use n >= 1 of slot s
+        if (!mbar_wait_bounded(fbar_empty(c, s), (uint32_t)(n - 1) & 1u, p.wait_ns)) {
+          atomicOr(p.status, FASA_DEV_TIMEOUT);
+          break;
+        }
+#pragma unroll 4
+        for (int r = 0; r < GR; r += RPI) row_copy(g * GR + r + g_sub);
+        cp_async_mbar_arrive(fbar_full(c, s));
+      }
+      cp_async_wait<0>();
+    } else if (warp < nrec) {
       const int gq = lane >> 2, tq = lane & 3;
       uint32_t qb[KS][2][2];  // [k-step][b0 / b1][hi / lo], built in the set-up
 #pragma unroll
@@ -1640,7 +1674,11 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
       int it = 0;
       for (int g = warp; g < ngrp; g += FNW, ++it) {
         const int s = it % wst;
-        if (it > 0) {  // at most wst - 1 of this thread's later groups may still be in flight
+        if (pc) {  // a refill: the producer's copies into this slot have landed
+          if (it >= wst && !mbar_wait_bounded(fbar_full(warp, s), (uint32_t)(it / wst - 1) & 1u, p.wait_ns))
+            atomicOr(p.status, FASA_DEV_TIMEOUT);
+          __syncwarp();
+        } else if (it > 0) {  // at most wst - 1 of this thread's later groups may still be in flight
           if (wst >= 4) cp_async_wait<3>();
           else if (wst == 3) cp_async_wait<2>();
           else if (wst == 2) cp_async_wait<1>();
@@ -1711,15 +1749,18 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
           mma_bf16_16816(oc[mt], a0, a1, a2, a3, b0l, b1l);
         }
         __syncwarp();  // the slot and the P tile are free again
-        // the warp's next group after the ones in flight: two lanes per row,
-        // each half of its chunks (commits a group even when empty: the waits
-        // count groups)
-        const int gn = g + wst * FNW;
-        if (gn < ngrp) {
+        if (pc) {
+          if (lane == 0) mbar_arrive(fbar_empty(warp, s));
+        } else {
+          // the warp's next group after the ones in flight (commits a group
+          // even when empty: the waits count groups)
+          const int gn = g + wst * FNW;
+          if (gn < ngrp) {
 #pragma unroll 4
-          for (int r = 0; r < GR; r += RPI) row_copy(gn * GR + r + g_sub);
+            for (int r = 0; r < GR; r += RPI) row_copy(gn * GR + r + g_sub);
+          }
+          cp_async_commit();
         }
-        cp_async_commit();
       }
       cp_async_wait<0>();
 #pragma unroll
