@@ -379,22 +379,26 @@ int fasa_device_status(fasa_stream_t stream, int32_t* status);
 /*
  * Fault injection for tests (the pages have no counterpart).  Sets, for the
  * calls launched after it in this process, the bound of every device wait
- * (wait_limit_ns > 0; the default is 1 s) and, when drop_tip_tile >= 0,
- * makes the fused step's TIP stage of that tile index arm its barrier but
- * never issue the copy, so the waits on it run out: the launch then returns
- * with FASA_DEV_TIMEOUT (and FASA_DEV_UNDRAINED) in the status word, no copy
- * left in flight, and the stream usable.  fasa_test_fault_injection(1000000000, -1)
- * restores the defaults.  FASA_ERR_INVALID_ARG for a zero limit or a tile
- * below -1.
+ * (wait_limit_ns > 0; the default is 1 s) and:
+ *  - drop_tip_tile >= 0: the fused step's TIP stage of that tile index arms
+ *    its barrier but never issues the copy, so the waits on it run out;
+ *  - drop_fac_refill >= 0: in the single-exchange kernel's FAC after the
+ *    selection, the warp that refills attending warp 0's slots withholds
+ *    its completion arrivals for that refill (0 = the first), so warp 0's
+ *    wait on the slot runs out (the copies themselves are issued and land).
+ * The launch then returns with FASA_DEV_TIMEOUT (with a dropped tile also
+ * FASA_DEV_UNDRAINED) in the status word, no copy left in flight, and the
+ * stream usable.  fasa_test_fault_injection(1000000000, -1, -1) restores
+ * the defaults.  FASA_ERR_INVALID_ARG for a zero limit or an index below -1.
  */
-int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile);
+int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile, int32_t drop_fac_refill);
 
 /* Cluster size (CTAs per (b, KV head)) the fused kernels use on this device. */
 int fasa_cluster_size(const fasa_dims_t* dims, int32_t* ctas);
 
 /* Which fused kernel serves fasa_decode_step (and the _append and _noalloc
  * forms) for these dims on this device: FASA_KERNEL_SINGLE_EXCHANGE (bf16
- * caches, clusters of 8 or more CTAs per unit: one list exchange, a verified
+ * caches, clusters of 4 or more CTAs per unit: one list exchange, a verified
  * union top-k, one combine exchange) or FASA_KERNEL_CLUSTER (every other
  * plan: the radix-select cluster kernel).  Both compute the same step; the
  * selected set and the output agree up to the documented rounding. */

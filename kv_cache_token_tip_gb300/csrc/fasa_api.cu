@@ -27,6 +27,7 @@ thread_local int t_last_cuda_error = 0;
 // the test hook that leaves one TIP tile's copy unissued (-1: none).
 unsigned long long g_wait_ns = 1000000000ull;
 int g_drop_tip_tile = -1;
+int g_drop_fac_refill = -1;
 
 
 int cuda_fail(cudaError_t e) {
@@ -499,6 +500,7 @@ void fill_step(StepParams& p, const fasa_dims_t* d, int32_t budget) {
   memcpy(p.rope_turns, tmp.rope_turns, sizeof(p.rope_turns));
   p.wait_ns = g_wait_ns;
   p.drop_stage = g_drop_tip_tile;
+  p.drop_refill = g_drop_fac_refill;
 }
 
 // The bf16 step kernel serves fasa_decode_step when these dims plan.
@@ -1170,10 +1172,11 @@ int fasa_select_dominant_fcs(const float* ca_mean, int32_t n_tip, int32_t* dom_f
 }
 
 
-int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile) {
-  if (wait_limit_ns == 0 || drop_tip_tile < -1) return FASA_ERR_INVALID_ARG;
+int fasa_test_fault_injection(uint64_t wait_limit_ns, int32_t drop_tip_tile, int32_t drop_fac_refill) {
+  if (wait_limit_ns == 0 || drop_tip_tile < -1 || drop_fac_refill < -1) return FASA_ERR_INVALID_ARG;
   g_wait_ns = wait_limit_ns;
   g_drop_tip_tile = drop_tip_tile;
+  g_drop_fac_refill = drop_fac_refill;
   return FASA_OK;
 }
 

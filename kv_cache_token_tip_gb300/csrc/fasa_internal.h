@@ -104,6 +104,8 @@ struct StepParams {
   int* status;
   unsigned long long wait_ns; // bound of every device wait
   int drop_stage;             // test hook: this TIP tile's copy is never issued (-1: none)
+  int drop_refill;            // test hook: this refill of attending warp 0's slots is never
+                              // reported complete (-1: none)
   // plan (host)
   int s_cap;       // scores per CTA kept in shared memory (0: workspace)
   int tip_tile;    // tokens per TIP stage (multiple of TIP_UNIT)

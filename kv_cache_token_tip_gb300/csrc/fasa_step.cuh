@@ -1646,7 +1646,8 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
         }
 #pragma unroll 4
         for (int r = 0; r < GR; r += RPI) row_copy(g * GR + r + g_sub);
-        cp_async_mbar_arrive(fbar_full(c, s));
+        if (c != 0 || it - wst != p.drop_refill)  // (test hook: a withheld completion report)
+          cp_async_mbar_arrive(fbar_full(c, s));
       }
       cp_async_wait<0>();
     } else if (warp < nrec) {

@@ -100,7 +100,7 @@ def lib():
             "fasa_fc_agreement": ([vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_compound_agreement": ([vp, vp, vp, vp, i32, vp, vp, sz, dp, vp], ctypes.c_int),
             "fasa_select_dominant_fcs": ([vp, i32, vp, dp, vp], ctypes.c_int),
-            "fasa_test_fault_injection": ([ctypes.c_uint64, i32], ctypes.c_int),
+            "fasa_test_fault_injection": ([ctypes.c_uint64, i32, i32], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -371,7 +371,11 @@ def fasa_device_status(stream=None) -> int:
     return out.value
 
 
-def fasa_test_fault_injection(wait_limit_ns: int = 1_000_000_000, drop_tip_tile: int = -1) -> None:
-    """Test hook: bound of every device wait, and one TIP tile whose copy the
-    fused step never issues (-1: none).  The defaults restore normal runs."""
-    _check("fasa_test_fault_injection", lib().fasa_test_fault_injection(int(wait_limit_ns), int(drop_tip_tile)))
+def fasa_test_fault_injection(wait_limit_ns: int = 1_000_000_000, drop_tip_tile: int = -1,
+                              drop_fac_refill: int = -1) -> None:
+    """Test hook: bound of every device wait, one TIP tile whose copy the
+    fused step never issues, and one refill of the single-exchange kernel's
+    FAC whose completion is never reported (-1: none).  The defaults restore
+    normal runs."""
+    _check("fasa_test_fault_injection", lib().fasa_test_fault_injection(int(wait_limit_ns), int(drop_tip_tile),
+                                                                         int(drop_fac_refill)))

@@ -235,3 +235,14 @@ def test_variant_workloads():
     tot_py = sum(bench.algorithmic_bytes(py, lens, py.layer_budget(l))["fac"] for l in range(py.layers))
     tot_uni = bench.algorithmic_bytes(uni, lens)["fac"] * uni.layers
     assert abs(tot_py - tot_uni) < 0.01 * tot_uni   # same mean budget, lengths mostly above 384
+
+
+def test_fault_injection_arguments_validated(L):
+    """The test hook rejects a zero wait bound and indices below -1, and
+    accepts (then restores) the defaults; it only sets host-side values."""
+    f = L.fasa_test_fault_injection
+    assert f(0, -1, -1) == 1
+    assert f(1000000000, -2, -1) == 1
+    assert f(1000000000, -1, -2) == 1
+    assert f(2000000, 0, 3) == 0
+    assert f(1000000000, -1, -1) == 0

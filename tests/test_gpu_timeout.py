@@ -104,3 +104,36 @@ def test_unissued_tip_copy_times_out_and_the_stream_stays_usable(name, over, ker
     assert np.array_equal(idx2.cpu().numpy(), idx0.cpu().numpy())
     assert np.array_equal(cnt2.cpu().numpy(), cnt0.cpu().numpy())
     assert np.array_equal(out2.cpu().numpy(), out0.cpu().numpy())
+
+
+def test_withheld_fac_refill_times_out_and_the_stream_stays_usable():
+    """The single-exchange kernel's FAC after the selection (batch 8,
+    clusters of 4): when the warp that refills attending warp 0's slots
+    withholds the completion report of one refill, warp 0's wait on that
+    slot runs out within the bound (and the later waits of that warp, one
+    phase behind, each within the bound too); FASA_DEV_TIMEOUT is reported,
+    the launch ends, and the next clean step matches the one before it bit
+    for bit.  The copies themselves are issued and land: nothing is left in
+    flight."""
+    import torch
+    from kv_cache_token_tip_gb300 import FASA_DEV_TIMEOUT, fasa_device_status, fasa_test_fault_injection
+    cfg, dims, L, kd, ws = _setup("qwen25_7b_b8_ctx16k", dict(context=4096), 1)
+    fasa_device_status()
+    out0, idx0, cnt0 = _step(cfg, dims, L, kd, ws)
+    assert fasa_device_status() == 0
+    try:
+        fasa_test_fault_injection(wait_limit_ns=SHORT_NS, drop_fac_refill=0)
+        t0 = time.perf_counter()
+        _step(cfg, dims, L, kd, ws)
+        st = fasa_device_status()
+        elapsed = time.perf_counter() - t0
+    finally:
+        fasa_test_fault_injection()
+    assert st & FASA_DEV_TIMEOUT, f"status {st}"
+    assert elapsed < 2.0, f"faulted step took {elapsed:.3f} s"
+    out2, idx2, cnt2 = _step(cfg, dims, L, kd, ws)
+    assert fasa_device_status() == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(idx2.cpu().numpy(), idx0.cpu().numpy())
+    assert np.array_equal(cnt2.cpu().numpy(), cnt0.cpu().numpy())
+    assert np.array_equal(out2.cpu().numpy(), out0.cpu().numpy())
