@@ -425,8 +425,7 @@ int plan_step(StepParams& p, const fasa_dims_t* d, int C, size_t* ws, int limit)
   }
   if (!tile) return FASA_ERR_UNSUPPORTED;
   const int tip_bytes = stages * tile * fc_tok;
-  // FAC staging: two groups in flight per warp when they fit; the first
-  // round's list is gathered during the exchange when it fits the first issue
+  // FAC slots in `big`: two groups in flight per attending warp when they fit
   int wst = 0;
   for (int w = 2; w >= 1 && !wst; --w)
     if (fac_slots(w) + pt_bytes <= room) wst = w;

@@ -1515,12 +1515,13 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     // Resident FAC: every row of the own first-round list sits in its slot
     // and its scores are in s_rows (taken by the gather warps during the
     // selection, or now).  Warp w < D/16 takes head dims 16w..16w+15 of
-    // every head over all rows: lane (gq, tq) reads the scores of head gq at
-    // the rows of its B fragments (2tq, 2tq+1, 2tq+8, 2tq+9 of each group),
-    // masks the rows below theta, and forms the head's maximum M and the
-    // weights P = exp2(s - M) (M and L = sum P come out the same in every
-    // warp); then O^T = V^T P^T on the tensor cores, P split into bf16
-    // hi + lo.  The warp's slice of the CTA's (M, L, acc) record goes
+    // every head: it compacts the list's entries at or above theta, takes
+    // each head's maximum M over them, and attends those rows only, 16 per
+    // step -- lane (gq, tq) reads the scores of head gq at the step's rows
+    // 2tq, 2tq+1, 2tq+8, 2tq+9 and forms P = exp2(s - M), and the warp
+    // computes O^T = V^T P^T on the tensor cores (ldmatrix rows gathered by
+    // index, P split into bf16 hi + lo).  M and L = sum P come out the same
+    // in every warp.  The warp's slice of the CTA's (M, L, acc) record goes
     // straight into the combine slots: no per-warp records to merge.
     constexpr int KS = D / 16;
     const int ngrp = (fr_n + GR - 1) / GR;
@@ -1534,8 +1535,8 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     if (warp < KS) {
       // Every attending warp compacts the selected entries of the list (key
       // >= theta, in list order) into its own index array sp and takes each
-      // head's maximum M over them (rolled loops: this code runs once per
-      // launch, and its instruction fetch is much of its cost).
+      // head's maximum M over them (each warp on its own: one warp doing it
+      // for all and a barrier measured slower).
       uint16_t* sp = reinterpret_cast<uint16_t*>(s_rows + G_MAX * srs) + warp * p.cap1;
       const int gq = lane >> 2, tq = lane & 3, mt = warp;
       float mx[G_MAX];
@@ -1632,7 +1633,7 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     const int nrec = min(FNW, ngrp);  // warps that attend rows
     const bool pc = fslot == nullptr;  // (uniform)
     float* rec = reinterpret_cast<float*>(big);  // [G][FNW][D + 2]
-    cp_async_wait<0>();  // the CTA-wide first groups (listed rows)
+    cp_async_wait<0>();  // the CTA-wide first groups
     __syncthreads();
     if (pc && warp >= FNW) {
       const int c = warp - FNW, wst = p.fac_wst;
