@@ -1349,11 +1349,13 @@ __global__ void __launch_bounds__(SNT, 1) fasa_step_kernel(const __grid_constant
     }
     STEP_TRACE(14);
     // one sweep into per-warp segments of the idle staging when it is free
-    // (scores not reloaded there), else the two-pass listing
+    // (scores not reloaded there) and a segment holds at least twice a
+    // warp's share of the list, else (or when a warp's entries overflow its
+    // segment) the two-pass listing
     n1 = -1;
-    if (R1.need == INT_MAX && !p.reload && p.smem_total - p.off_big >= SNW * p.cap1 * 8)
-      n1 = list_rule_1p(R1, scr, nloc, t0, own1 + 2, p.cap1, ms, reinterpret_cast<unsigned long long*>(big),
-                        p.cap1);
+    const int scap = min(p.cap1, (p.smem_total - p.off_big) / (SNW * 8));
+    if (R1.need == INT_MAX && !p.reload && big_ok && scap >= max(64, 2 * p.cap1 / SNW))
+      n1 = list_rule_1p(R1, scr, nloc, t0, own1 + 2, p.cap1, ms, reinterpret_cast<unsigned long long*>(big), scap);
     if (n1 < 0)
       n1 = R1.need == INT_MAX ? list_rule_t<false>(R1, scr, nloc, t0, own1 + 2, p.cap1, ms)
                               : list_rule_any(R1, scr, nloc, t0, own1 + 2, p.cap1, ms);
