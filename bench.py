@@ -748,7 +748,10 @@ def run_gpu(args):
                                 for kk in ("tip", "fac", "q", "out", "small", "append")
                                 if kk in model},
             "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved_gbs / peak, 4), "traffic": ncu_traffic(cfg.name),
+                         "frac": round(achieved_gbs / peak, 4),
+                         # (the committed captures are of the plain step with the caches in device
+                         # memory: no figure for the split-key or append forms)
+                         "traffic": None if (args.fasa_m or args.append) else ncu_traffic(cfg.name),
                          "peak_kind": peak_kind, "kernel": kernel_name},
             "dense": {"us_per_step": round(dense_sec * 1e6, 3),
                       "achieved_gbs": round(model["dense_total"] * layers / dense_sec / 1e9, 1),
